@@ -1,0 +1,411 @@
+"""Benchmark: selected-block attention (selector + block-sparse forward) on GB300.
+
+One step = one pass of the whole hot path over one batch: bsa_select (block
+pooling, block scores, top-k with the prefix forced in, compaction) followed
+by bsa_forward (tcgen05 attention over the selected blocks), on the 720p
+video-latent workload (B=1, Hq=32, Hkv=8, d=128, prefix 1024 + 172,800
+generation tokens, blocks 256x128, keep 25% of the non-prefix key blocks).
+
+value = effective TFLOP/s of the step: 4*d*sum over work tiles of
+block_q*count*block_k (the selected tiles' work, never the dense work they
+skip) divided by the step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bsa|reference] [--config NAME]
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+the method here) on a bounded sample of the same workload, extrapolated to
+the full workload.  Under torchrun every rank runs its own replica (weak
+scaling, no collective on the data path); rank 0 prints the JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-sparse attn fwd ms/call & effective TFLOP/s vs GB300 bf16 peak @75% sparsity"
+UNIT = "TFLOP/s"
+DEFAULT_CONFIG = "720p_75"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="bsa", choices=["bsa", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sustained=d["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def tile_flops(counts, d, bq, bk) -> float:
+    """4*d*block_q*block_k per selected (work tile, key block) pair."""
+    return 4.0 * d * bq * bk * float(counts.sum())
+
+
+def valid_pair_flops(counts_np, indices_np, seq_lens, prefix, d, bq, bk) -> float:
+    """4*d per (real query row, real selected key) pair."""
+    tot = 0
+    B, H, nQ = counts_np.shape
+    for b in range(B):
+        L = seq_lens[b]
+        for qb in range(nQ):
+            rows = max(0, min(bq, L - qb * bq))
+            if rows == 0:
+                continue
+            for h in range(H):
+                c = counts_np[b, h, qb]
+                idx = indices_np[b, h, qb, :c]
+                keys = (idx.size * bk) - int(max(0, (idx[-1] + 1) * bk - (prefix + L))) if c else 0
+                tot += rows * keys
+    return 4.0 * d * tot
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(inp, idx, cnt, n_tiles_sample=3, budget_s=25.0):
+    """The oracle, as it stands, on a bounded sample of the workload: the full
+    selector for one query head and the attention of a few work tiles,
+    extrapolated linearly to the whole workload (units: effective TFLOP/s)."""
+    import numpy as np
+    import torch
+    from oracle import bsa_oracle as O
+
+    c = inp["cfg"]
+    G = c.Hq // c.Hkv
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    t_host = lambda t: t.float().cpu().numpy()
+    h0 = 0
+    q1, k1 = t_host(q[:, :, h0:h0 + 1]), t_host(k[:, :, h0 // G:h0 // G + 1])
+    keep = inp["keep_ratio"] if len(inp["keep_ratio"]) == 1 else [inp["keep_ratio"][h0]]
+    t0 = time.perf_counter()
+    O.select_blocks(q1, k1, c.prefix, inp["seq_lens"], c.block_q, c.block_k, keep)
+    t_sel_head = time.perf_counter() - t0
+    cnt_np = cnt.cpu().numpy()
+    idx_np = idx.cpu().numpy()
+    rng = np.random.default_rng(0)
+    nz = np.argwhere(cnt_np > 0)
+    picks = nz[rng.choice(len(nz), size=min(n_tiles_sample, len(nz)), replace=False)]
+    t_att, sampled_pairs = 0.0, 0
+    done = 0
+    for b, h, qb in picks:
+        hk = h // G
+        qh, kh, vh = t_host(q[b:b + 1, :, h:h + 1]), t_host(k[b:b + 1, :, hk:hk + 1]), t_host(v[b:b + 1, :, hk:hk + 1])
+        cc = int(cnt_np[b, h, qb])
+        t0 = time.perf_counter()
+        O.attention_tile(qh, kh, vh, 0, 0, int(qb), idx_np[b, h, qb, :cc], c.prefix, inp["seq_lens"][b],
+                         c.block_q, c.block_k, 1.0 / math.sqrt(c.d))
+        t_att += time.perf_counter() - t0
+        sampled_pairs += cc
+        done += 1
+        if t_att + t_sel_head > budget_s:
+            break
+    total_pairs = float(cnt_np.sum())
+    est_time = t_sel_head * c.Hq + t_att * (total_pairs / max(1, sampled_pairs))
+    flops = tile_flops(cnt_np, c.d, c.block_q, c.block_k)
+    return {
+        "value": flops / est_time / 1e12,
+        "unit": UNIT,
+        "cores": torch.get_num_threads(),
+        "kind": "oracle",
+        "sample": (f"fp64 numpy oracle: full selector for 1 of {c.Hq} query heads ({t_sel_head:.2f} s) and "
+                   f"attention of {done} work tiles ({sampled_pairs} selected key blocks, {t_att:.2f} s), "
+                   f"extrapolated linearly to all heads and all {int(total_pairs)} selected blocks "
+                   f"(est. {est_time:.0f} s per step)"),
+        "est_seconds_per_step": est_time,
+    }
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 oracle on the host cores, K timed steps of a
+    bounded sample each; only rank 0 works."""
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    from bsa_inputs import CONFIGS, make_inputs
+    from oracle import bsa_oracle as O
+
+    cfg = CONFIGS[args.config]
+    inp = make_inputs(cfg, "cpu", pad_fill=0.0)
+    # selection lists for the sampled tiles come from the oracle itself (one head)
+    G = cfg.Hq // cfg.Hkv
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    t_host = lambda t: t.float().numpy()
+    rng = np.random.default_rng(1)
+    steps_t, steps_flops_est = [], []
+    sizes = [None]
+
+    def one_step(i):
+        h = int(rng.integers(cfg.Hq))
+        hk = h // G
+        keep = inp["keep_ratio"] if len(inp["keep_ratio"]) == 1 else [inp["keep_ratio"][h]]
+        qh, kh, vh = t_host(q[:, :, h:h + 1]), t_host(k[:, :, hk:hk + 1]), t_host(v[:, :, hk:hk + 1])
+        t0 = time.perf_counter()
+        sel = O.select_blocks(qh, kh, cfg.prefix, inp["seq_lens"], cfg.block_q, cfg.block_k, keep)
+        t_sel = time.perf_counter() - t0
+        b = int(rng.integers(cfg.B))
+        nqv = O.cdiv(inp["seq_lens"][b], cfg.block_q)
+        qb = int(rng.integers(nqv))
+        c = int(sel["counts"][b, 0, qb])
+        t0 = time.perf_counter()
+        O.attention_tile(qh, kh, vh, b, 0, qb, sel["indices"][b, 0, qb, :c], cfg.prefix, inp["seq_lens"][b],
+                         cfg.block_q, cfg.block_k, 1.0 / math.sqrt(cfg.d))
+        t_att = time.perf_counter() - t0
+        # whole-workload estimate: selector x Hq heads, attention x all selected blocks
+        tot_blocks = 0
+        for bb in range(cfg.B):
+            for hh in range(cfg.Hq):
+                r = inp["keep_ratio"][0] if len(inp["keep_ratio"]) == 1 else inp["keep_ratio"][hh]
+                geo = O.kv_geometry(cfg.prefix, inp["seq_lens"][bb], cfg.block_k)
+                per_row = geo["n_prefix_blocks"] + O.keep_count(r, geo["n_candidates"])
+                tot_blocks += per_row * O.cdiv(inp["seq_lens"][bb], cfg.block_q)
+        est = t_sel * cfg.Hq + t_att * tot_blocks / max(1, c)
+        flops = 4.0 * cfg.d * cfg.block_q * cfg.block_k * tot_blocks
+        return est, flops, t_sel + t_att
+
+    for _ in range(args.warmup):
+        one_step(-1)
+    wall = 0.0
+    for i in range(args.steps):
+        est, flops, w = one_step(i)
+        steps_t.append(est)
+        steps_flops_est.append(flops)
+        wall += w
+    est_mean = sum(steps_t) / len(steps_t)
+    value = steps_flops_est[0] / est_mean / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": est_mean * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.config, "sample": "per step: full selector of one "
+                                        "random query head + attention of one random work tile, "
+                                        "extrapolated to the whole workload"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
+                         "sample": f"{args.steps} steps, {wall:.1f} s of measured oracle work"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import block_sparse_attention_bsa_gb300 as bsa
+    from bsa_inputs import CONFIGS, make_inputs
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    bsa.build()
+    cfg = CONFIGS[args.config]
+    inp = make_inputs(cfg, "cuda", pad_fill=0.0)
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    P, lens, bq, bk, keep = cfg.prefix, inp["seq_lens"], cfg.block_q, cfg.block_k, inp["keep_ratio"]
+    B, Sq, Hq, d = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    nQb, nKb = -(-Sq // bq), -(-Skv // bk)
+    idx = torch.empty((B, Hq, nQb, nKb), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((B, Hq, nQb), dtype=torch.int32, device="cuda")
+    ws = torch.empty(bsa.bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, bq, bk), dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    launches_per_step = 4     # pool(Q), pool(K), score/top-k, forward
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        bsa.bsa_select(q, k, P, lens, bq, bk, keep, indices=idx, counts=cnt, workspace=ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        bsa.bsa_forward(q, k, v, idx, cnt, P, lens, bq, bk, out=out, lse=lse, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    bsa.bsa_device_status(stream)
+    flops = tile_flops(cnt, d, bq, bk)
+    sampler = ClockSampler(local)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    bsa.bsa_device_status(stream)
+    total_ms = t_start.elapsed_time(t_end)
+    sel_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    ms_step = total_ms / args.steps
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    pk = peaks()
+    fwd_mean = sum(fwd_ms) / len(fwd_ms)
+    fwd_tflops = flops / (fwd_mean * 1e-3) / 1e12
+    cnt_np, idx_np = cnt.cpu().numpy(), idx.cpu().numpy()
+    exact_flops = valid_pair_flops(cnt_np, idx_np, lens, P, d, bq, bk)
+    dense_tiles = sum(-(-(P + L) // bk) * -(-L // bq) for L in lens) * Hq
+    tile_sparsity = 1.0 - float(cnt_np.sum()) / dense_tiles
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        hq, hk_, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk_, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(2, min(args.steps, 5))
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b_) / n_e2e
+        if world > 1:
+            t = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk_, hv))
+        d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, idx, cnt)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.config, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "prefix": P,
+                       "seq_lens": lens, "block_q": bq, "block_k": bk, "keep_ratio": keep[:4],
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": f"inputs larger than L2 ({(q.numel() + k.numel() + v.numel()) * 2 / 1e9:.2f} GB)"},
+            "select_ms": sum(sel_ms) / len(sel_ms),
+            "fwd_ms": fwd_mean,
+            "fwd_tflops_effective": fwd_tflops,
+            "tile_sparsity": tile_sparsity,
+            "exact_pair_tflop_per_step": exact_flops / 1e12,
+            "effective_tflop_per_step": flops / 1e12,
+            "roofline": {"bound": "tensor", "kernel": "fmha_fwd_kernel<128,128,2>", "achieved": fwd_tflops,
+                         "peak": pk["bf16"], "unit": "TFLOP/s", "frac": fwd_tflops / pk["bf16"],
+                         "peak_source": f"{pk['source']} bf16 burst", "traffic": None},
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": launches_per_step * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+"""Python binding of libbsa: argument marshalling only.
+
+Each function has the name of the C entry point it calls (include/bsa.h) and
+turns torch tensors into pointers, sizes and strides.  Every step of the
+selector and of the attention runs in the library's CUDA kernels; there is no
+other path, and a missing library or a non-CUDA tensor raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+
+BLOCK_Q_SUPPORTED = (64, 128, 256)
+BLOCK_K_SUPPORTED = (64, 128)
+
+
+class BsaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.status_name = _lib.STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{self.status_name}: {message}")
+
+
+def _check(status: int):
+    if status != 0:
+        msg = _lib.load().bsa_get_last_error().decode(errors="replace")
+        raise BsaError(status, msg)
+
+
+def _desc(t: torch.Tensor, name: str) -> _lib.BsaTensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16 (got {t.dtype})")
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be 4-D [B, S, H, d] (got {tuple(t.shape)})")
+    if t.stride(3) != 1:
+        raise ValueError(f"{name} must have a contiguous last dim")
+    B, S, H, D = t.shape
+    sb, ss, sh, _ = t.stride()
+    return _lib.BsaTensor(t.data_ptr(), B, S, H, D, sb, ss, sh)
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _i32_array(vals: Optional[Sequence[int]]):
+    if vals is None:
+        return None
+    return (ctypes.c_int32 * len(vals))(*[int(x) for x in vals])
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def bsa_version() -> int:
+    return _lib.load().bsa_version()
+
+
+def bsa_get_last_error() -> str:
+    return _lib.load().bsa_get_last_error().decode(errors="replace")
+
+
+def bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, block_q, block_k) -> int:
+    return int(_lib.load().bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, block_q, block_k))
+
+
+def bsa_forward_workspace_size(B, Hq, Sq, block_q) -> int:
+    return int(_lib.load().bsa_forward_workspace_size(B, Hq, Sq, block_q))
+
+
+def _workspace(nbytes: int, device, given: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return given
+    if given is not None:
+        return given
+    # torch's allocator returns 512-byte aligned blocks
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def bsa_select(q: torch.Tensor, k: torch.Tensor, prefix_len: int, seq_lens: Optional[Sequence[int]],
+               block_q: int, block_k: int, keep_ratio, *, indices: Optional[torch.Tensor] = None,
+               counts: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+               stream=None):
+    """Selected key blocks per (request, query head, query block).
+
+    Returns ``(indices [B, Hq, nQb, nKb] int32, counts [B, Hq, nQb] int32)``;
+    entries of ``indices`` past a row's count are not written (new buffers
+    start at -1).  ``keep_ratio``: a float or a sequence of 1 or Hq floats.
+    """
+    qd, kd = _desc(q, "q"), _desc(k, "k")
+    B, Sq, Hq, d = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    nQb, nKb = _cdiv(Sq, block_q), _cdiv(Skv, block_k)
+    if isinstance(keep_ratio, (int, float)):
+        keep_ratio = [float(keep_ratio)]
+    keep = (ctypes.c_float * len(keep_ratio))(*[float(x) for x in keep_ratio])
+    if indices is None:
+        indices = torch.full((B, Hq, nQb, nKb), -1, dtype=torch.int32, device=q.device)
+    if counts is None:
+        counts = torch.empty((B, Hq, nQb), dtype=torch.int32, device=q.device)
+    for name, t, shape in (("indices", indices, (B, Hq, nQb, nKb)), ("counts", counts, (B, Hq, nQb))):
+        if t.dtype != torch.int32 or tuple(t.shape) != shape or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of shape {shape}")
+    need = bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, block_q, block_k)
+    ws = _workspace(need, q.device, workspace)
+    lib = _lib.load()
+    st = lib.bsa_select(ctypes.byref(qd), ctypes.byref(kd), int(prefix_len), _i32_array(seq_lens),
+                        int(block_q), int(block_k), keep, len(keep_ratio), indices.data_ptr(),
+                        counts.data_ptr(), ws.data_ptr() if ws is not None else None,
+                        ws.numel() if ws is not None else 0, _stream_ptr(stream))
+    _check(st)
+    return indices, counts
+
+
+def bsa_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, indices: Optional[torch.Tensor],
+                counts: Optional[torch.Tensor], prefix_len: int, seq_lens: Optional[Sequence[int]],
+                block_q: int, block_k: int, softmax_scale: float = 0.0, *,
+                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                return_lse: bool = True, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Attention over the listed key blocks (``indices=None``: dense pass).
+
+    Returns ``(out [B, Sq, Hq, d] bf16, lse [B, Hq, Sq] fp32 or None)``.
+    """
+    qd, kd, vd = _desc(q, "q"), _desc(k, "k"), _desc(v, "v")
+    B, Sq, Hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device=q.device)
+    if tuple(out.shape) != (B, Sq, Hq, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor [B, Sq, Hq, d]")
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if lse is not None and (tuple(lse.shape) != (B, Hq, Sq) or lse.dtype != torch.float32
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, Sq]")
+    for name, t in (("indices", indices), ("counts", counts)):
+        if t is not None and (t.dtype != torch.int32 or not t.is_contiguous() or t.device != q.device):
+            raise ValueError(f"{name} must be a contiguous int32 tensor on {q.device}")
+    need = bsa_forward_workspace_size(B, Hq, Sq, block_q)
+    ws = _workspace(need, q.device, workspace)
+    lib = _lib.load()
+    st = lib.bsa_forward(ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd),
+                         indices.data_ptr() if indices is not None else None,
+                         counts.data_ptr() if counts is not None else None,
+                         int(prefix_len), _i32_array(seq_lens), int(block_q), int(block_k),
+                         float(softmax_scale), out.data_ptr(),
+                         lse.data_ptr() if lse is not None else None,
+                         ws.data_ptr() if ws is not None else None,
+                         ws.numel() if ws is not None else 0, _stream_ptr(stream))
+    _check(st)
+    return out, lse
+
+
+def bsa_validate_indices(indices: torch.Tensor, counts: torch.Tensor, B: int, Hq: int, Sq: int, Skv: int,
+                         prefix_len: int, seq_lens: Optional[Sequence[int]], block_q: int, block_k: int,
+                         require_prefix: bool = True, stream=None) -> int:
+    """Number of malformed rows (synchronises the stream to read it)."""
+    bad = torch.zeros(1, dtype=torch.int32, device=indices.device)
+    lib = _lib.load()
+    st = lib.bsa_validate_indices(indices.data_ptr(), counts.data_ptr(), B, Hq, Sq, Skv, int(prefix_len),
+                                  _i32_array(seq_lens), block_q, block_k, 1 if require_prefix else 0,
+                                  bad.data_ptr(), _stream_ptr(stream))
+    _check(st)
+    return int(bad.item())
+
+
+def bsa_device_status(stream=None) -> None:
+    """Synchronises and raises BsaError if a bounded device wait gave up."""
+    _check(_lib.load().bsa_device_status(_stream_ptr(stream)))

@@ -1,0 +1,545 @@
+// Selected-block attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes is fixed by the vllm-omni pull request "[Core] Add shared
+// block-sparse attention adapters with FlashAttention-4" (Purpose: execute
+// exactly the selector's per-query-head block lists, native GQA mapping,
+// protected prefix, suffix padding masked, no dense fallback) and by
+// cosmos_parallel.py (cosmos3_cp_attention: non-causal attention of
+// generation queries over cat(und, gen); build_gen_key_mask: padded keys
+// never contribute).  The FA4 kernel the pages run is prior art; this is a
+// fresh design for GB300:
+//
+//  * Persistent CTAs (one per SM) walk work tiles (b, query block, head),
+//    heads innermost so GQA siblings run together and share K/V in L2.
+//  * Warp 0 is the TMA producer: Q tile once per work tile, then K and V
+//    tiles of the listed blocks, gathered by index (row = index * block_k),
+//    into a ring of shared-memory stages.  Per-request tensor maps bound the
+//    rows at prefix + L_b, so padded keys/values load as zeros.
+//  * Warp 1 issues tcgen05.mma (one thread): S_h = Q_h K^T into TMEM for
+//    each 128-row half h of the query block, then O_h += P_h V with P_h read
+//    from TMEM (bf16, written over S_h by the softmax), ping-ponging the two
+//    halves so one half's softmax overlaps the other half's MMAs.
+//  * Warps 4.. are one softmax warpgroup per half: thread r owns query row r
+//    (TMEM lane r): tcgen05.ld of its S row, key mask, online softmax in the
+//    log2 domain with a lazy rescale (O is rescaled in TMEM only when the
+//    running max grows by more than 2^8), P back to TMEM, and the epilogue
+//    (O / l to bf16, LSE = ln-sum-exp of the scaled logits).
+//  * Every mbarrier wait is bounded (see mbar_wait); a CTA that gives up
+//    raises the device error word, leaves its loops and frees its TMEM.
+#include <cuda_bf16.h>
+
+#include <cfloat>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "bsa_internal.h"
+#include "bsa_ptx.cuh"
+
+namespace bsa {
+
+namespace {
+
+struct FmhaParams {   // CUtensorMap members make it 128-byte aligned
+  CUtensorMap tq[kMaxFwdBatch];
+  CUtensorMap tk[kMaxFwdBatch];
+  CUtensorMap tv[kMaxFwdBatch];
+  int seq_lens[kMaxFwdBatch];
+  int b0;           // first request of this launch
+  int Bn;           // requests in this launch
+  int Hq, G, Sq, nQb, nKb, block_q, prefix_len, n_tiles;
+  const int32_t* indices;  // NULL = dense pass
+  const int32_t* counts;
+  float scale_log2;        // softmax scale * log2(e)
+  __nv_bfloat16* out;      // [B, Sq, Hq, D]
+  float* lse;              // [B, Hq, Sq] or NULL
+};
+
+template <int D, int BK, int NH>
+struct Cfg {
+  static constexpr int kChunks = D / 64;                  // 128-byte chunks per row
+  static constexpr int kQHalfBytes = 128 * 128 * kChunks; // 128 rows x D bf16
+  static constexpr int kQBytes = NH * kQHalfBytes;
+  static constexpr int kTileBytes = BK * 128 * kChunks;   // one K or V tile
+  static constexpr int kBarBytes = 256;
+  static constexpr int kAlignSlack = 1024;
+  static constexpr int kSmemMax = 232448;                 // 227 KB per CTA
+  static constexpr int kStagesFit = (kSmemMax - kQBytes - kBarBytes - kAlignSlack) / kTileBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kSmemBytes = kQBytes + kStages * kTileBytes + kBarBytes + kAlignSlack;
+  static constexpr int kThreads = 128 + 128 * NH;
+  static constexpr uint32_t kTmemCols = NH == 2 ? 512 : 256;
+  static constexpr uint32_t kOCol = NH * 128;             // O_h at kOCol + 128 h
+  static_assert(kStages >= 2, "not enough shared memory for a K/V ring");
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(BK == 64 || BK == 128, "key block");
+};
+
+struct TileInfo {
+  int bl, b, qb, h, hk, L, valid_kv, n;
+  const int32_t* idx;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const FmhaParams& p, int t, int BK) {
+  TileInfo ti;
+  ti.h = t % p.Hq;
+  const int r = t / p.Hq;
+  ti.qb = r % p.nQb;
+  ti.bl = r / p.nQb;
+  ti.b = p.b0 + ti.bl;
+  ti.hk = ti.h / p.G;
+  ti.L = p.seq_lens[ti.bl];
+  ti.valid_kv = p.prefix_len + ti.L;
+  const int64_t row = ((int64_t)ti.b * p.Hq + ti.h) * p.nQb + ti.qb;
+  if (ti.qb * p.block_q >= ti.L) {
+    ti.n = 0;
+  } else if (p.indices == nullptr) {
+    ti.n = (ti.valid_kv + BK - 1) / BK;
+  } else {
+    const int c = p.counts[row];
+    ti.n = c < 0 ? 0 : (c > p.nKb ? p.nKb : c);
+  }
+  ti.idx = p.indices ? p.indices + row * p.nKb : nullptr;
+  return ti;
+}
+
+struct Ring {
+  uint32_t stage = 0, phase = 0;
+  template <int S>
+  __device__ __forceinline__ void next() {
+    if (++stage == S) { stage = 0; phase ^= 1u; }
+  }
+};
+
+template <int D, int BK, int NH>
+__global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
+    fmha_fwd_kernel(const __grid_constant__ FmhaParams p) {
+  using C = Cfg<D, BK, NH>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* q_smem = smem;
+  uint8_t* kv_smem = smem + C::kQBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(kv_smem + C::kStages * C::kTileBytes);
+  // barrier slots
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* s_full = bars + 2;            // [2]
+  uint64_t* p_full = bars + 4;            // [2]
+  uint64_t* o_full = bars + 6;            // [2]
+  uint64_t* kv_full = bars + 8;           // [kStages]
+  uint64_t* kv_empty = bars + 8 + C::kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * C::kStages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(q_full), 1);
+    mbar_init(smem_u32(q_empty), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(s_full + i), 1);
+      mbar_init(smem_u32(p_full + i), 128);
+      mbar_init(smem_u32(o_full + i), 1);
+    }
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(smem_u32(kv_full + i), 1);
+      mbar_init(smem_u32(kv_empty + i), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < p.Bn; ++i) {
+      tma_prefetch_desc(&p.tq[i]);
+      tma_prefetch_desc(&p.tk[i]);
+      tma_prefetch_desc(&p.tv[i]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer ---
+    Ring ring;
+    uint32_t qi = 0;
+    const uint32_t q_base = smem_u32(q_smem);
+    const uint32_t kv_base = smem_u32(kv_smem);
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+      const TileInfo ti = decode_tile(p, t, BK);
+      if (ti.n == 0) continue;
+      if (lane == 0) {
+        ok = mbar_wait(smem_u32(q_empty), (qi & 1u) ^ 1u, abort_flag);
+        if (ok) {
+          mbar_arrive_expect_tx(smem_u32(q_full), C::kQBytes);
+          for (int hh = 0; hh < NH; ++hh)
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(q_base + (hh * C::kChunks + c) * 16384, &p.tq[ti.bl], smem_u32(q_full),
+                          c * 64, ti.qb * p.block_q + hh * 128, ti.h);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ++qi;
+      for (int j0 = 0; j0 < ti.n && ok; j0 += 32) {
+        const int my_kb = ti.idx ? (j0 + lane < ti.n ? __ldg(ti.idx + j0 + lane) : 0) : j0 + lane;
+        const int m = min(32, ti.n - j0);
+        for (int jj = 0; jj < m && ok; ++jj) {
+          int kb = __shfl_sync(0xffffffffu, my_kb, jj);
+          if (kb < 0 || kb >= p.nKb) kb = p.nKb;   // out of range: rows past the end read zeros
+          if (lane == 0) {
+            for (int which = 0; which < 2 && ok; ++which) {
+              ok = mbar_wait(smem_u32(kv_empty + ring.stage), ring.phase ^ 1u, abort_flag);
+              if (!ok) break;
+              const uint32_t fb = smem_u32(kv_full + ring.stage);
+              mbar_arrive_expect_tx(fb, C::kTileBytes);
+              const CUtensorMap* tm = which == 0 ? &p.tk[ti.bl] : &p.tv[ti.bl];
+              for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(kv_base + ring.stage * C::kTileBytes + c * (BK * 128), tm, fb, c * 64,
+                            kb * BK, ti.hk);
+              ring.next<C::kStages>();
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer ---
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BK, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
+      const uint32_t q_base = smem_u32(q_smem);
+      const uint32_t kv_base = smem_u32(kv_smem);
+      Ring ring;
+      uint32_t qi = 0;
+      uint32_t pph[2] = {0u, 0u};
+      bool ok = true;
+      auto issue_s = [&](int hh, uint32_t stage) {
+        const uint32_t d_t = tmem + hh * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int c = kk / 4;
+          const uint32_t off = (kk % 4) * 32;
+          const uint64_t a = sdesc_sw128(q_base + (hh * C::kChunks + c) * 16384 + off, 16, 1024);
+          const uint64_t b = sdesc_sw128(kv_base + stage * C::kTileBytes + c * (BK * 128) + off, 16, 1024);
+          mma_ss(d_t, a, b, idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int hh, uint32_t stage, bool acc) {
+        const uint32_t d_t = tmem + C::kOCol + hh * 128;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint32_t a_t = tmem + hh * 128 + kk * 8;
+          const uint64_t b = sdesc_sw128(kv_base + stage * C::kTileBytes + kk * 16 * 128, BK * 128, 1024);
+          mma_ts(d_t, a_t, b, idesc_o, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p, t, BK);
+        const int n = ti.n;
+        if (n == 0) continue;
+        ok = mbar_wait(smem_u32(q_full), qi & 1u, abort_flag);
+        ++qi;
+        if (!ok) break;
+        // S_h(0) for every half
+        uint32_t sK = ring.stage;
+        ok = mbar_wait(smem_u32(kv_full + sK), ring.phase, abort_flag);
+        ring.next<C::kStages>();
+        if (!ok) break;
+        tc_fence_after();
+        for (int hh = 0; hh < NH; ++hh) {
+          issue_s(hh, sK);
+          mma_commit(smem_u32(s_full + hh));
+        }
+        mma_commit(smem_u32(kv_empty + sK));
+        if (n == 1) mma_commit(smem_u32(q_empty));
+        for (int j = 0; j < n && ok; ++j) {
+          const uint32_t sV = ring.stage;
+          ok = mbar_wait(smem_u32(kv_full + sV), ring.phase, abort_flag);
+          ring.next<C::kStages>();
+          if (!ok) break;
+          const bool has_next = j + 1 < n;
+          uint32_t sKn = 0, sKn_phase = 0;
+          if (has_next) {
+            sKn = ring.stage;
+            sKn_phase = ring.phase;
+            ring.next<C::kStages>();
+          }
+          for (int hh = 0; hh < NH && ok; ++hh) {
+            ok = mbar_wait(smem_u32(p_full + hh), pph[hh] & 1u, abort_flag);
+            ++pph[hh];
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(hh, sV, j > 0);
+            if (j == n - 1) mma_commit(smem_u32(o_full + hh));
+            if (has_next) {
+              if (hh == 0) {
+                ok = mbar_wait(smem_u32(kv_full + sKn), sKn_phase, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              issue_s(hh, sKn);
+              mma_commit(smem_u32(s_full + hh));
+            }
+          }
+          if (!ok) break;
+          mma_commit(smem_u32(kv_empty + sV));
+          if (has_next) {
+            mma_commit(smem_u32(kv_empty + sKn));
+            if (j + 2 == n) mma_commit(smem_u32(q_empty));
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // --------------------------------------------------- softmax + epilogue ---
+    const int hh = (warp - 4) / 4;
+    const int wq = warp % 4;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_t = tmem + lane_base + hh * 128;
+    const uint32_t o_t = tmem + lane_base + C::kOCol + hh * 128;
+    uint32_t sph = 0, oph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+      const TileInfo ti = decode_tile(p, t, BK);
+      const int row_in_blk = hh * 128 + r;
+      const int row = ti.qb * p.block_q + row_in_blk;
+      const bool row_exists = row_in_blk < p.block_q && row < p.Sq;
+      const bool row_ok = row_exists && row < ti.L;
+      __nv_bfloat16* orow = p.out + (((int64_t)ti.b * p.Sq + row) * p.Hq + ti.h) * D;
+      float* lrow = p.lse ? p.lse + ((int64_t)ti.b * p.Hq + ti.h) * p.Sq + row : nullptr;
+      if (ti.n == 0) {
+        if (row_exists) {
+          uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) reinterpret_cast<uint4*>(orow)[i] = z;
+          if (lrow) *lrow = -INFINITY;
+        }
+        continue;
+      }
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      for (int j = 0; j < ti.n; ++j) {
+        int kb = ti.idx ? __ldg(ti.idx + j) : j;
+        if (kb < 0 || kb >= p.nKb) kb = p.nKb;     // same clamp as the producer: fully masked
+        ok = mbar_wait(smem_u32(s_full + hh), sph & 1u, abort_flag);
+        ++sph;
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[BK];
+#pragma unroll
+        for (int c = 0; c < BK / 32; ++c)
+          tmem_ld32(s_t + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        tmem_wait_ld();
+        float* s = reinterpret_cast<float*>(sr);
+        const int kvalid = ti.valid_kv - kb * BK;
+        if (kvalid < BK) {
+#pragma unroll
+          for (int c = 0; c < BK; ++c)
+            if (c >= kvalid) s[c] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < BK; ++c) mx = fmaxf(mx, s[c]);
+        const float m_new = fmaxf(m_ref, mx * p.scale_log2);
+        const bool grow = m_new > m_ref + 8.0f;
+        const bool rescale_o = grow && m_ref != -INFINITY;
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          const float alpha = rescale_o ? ex2_approx(m_ref - m_new) : 1.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t orr[32];
+            tmem_ld32(o_t + c * 32, orr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tmem_st32(o_t + c * 32, orr);
+          }
+          tmem_wait_st();
+          if (rescale_o) l *= alpha;
+        }
+        if (grow) m_ref = m_new;
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        float lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < BK; ++c) {
+          const float e = ex2_approx(fmaf(s[c], p.scale_log2, -m_use));
+          s[c] = e;
+          lsum += e;
+        }
+        l += lsum;
+        // P (bf16 pairs) over the first BK/2 columns of S_h.
+#pragma unroll
+        for (int c = 0; c < BK / 64; ++c) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[c * 64 + 2 * i], s[c * 64 + 2 * i + 1]);
+          tmem_st32(s_t + c * 32, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(p_full + hh));
+      }
+      if (!ok) break;
+      ok = mbar_wait(smem_u32(o_full + hh), oph & 1u, abort_flag);
+      ++oph;
+      if (!ok) break;
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t orr[32];
+        tmem_ld32(o_t + c * 32, orr);
+        tmem_wait_ld();
+        if (row_exists) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = row_ok ? pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
+                                         __uint_as_float(orr[2 * i + 1]) * inv_l)
+                           : 0u;
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (row_exists && lrow)
+        *lrow = (row_ok && l > 0.f) ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      tc_fence_before();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------- host side ---
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// [rows, H, D] bf16 view starting at `base`: dims (D, rows, H), box (64, box_rows, 1),
+// 128-byte swizzle; rows past `rows` read as zeros.
+bsa_status encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int D,
+                      int64_t ss, int64_t sh, int box_rows, const char* name) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return set_error(BSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)H};
+  cuuint64_t strides[2] = {(cuuint64_t)(ss * 2), (cuuint64_t)(sh * 2)};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(BSA_ERR_CUDA, std::string("cuTensorMapEncodeTiled failed for ") + name +
+                                       " (CUresult " + std::to_string((int)r) + ")");
+  return BSA_OK;
+}
+
+template <int D, int BK, int NH>
+bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
+  using C = Cfg<D, BK, NH>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  bsa_status st;
+  if (dev < 64 && !attr_set[dev]) {
+    if ((st = cuda_check(cudaFuncSetAttribute(fmha_fwd_kernel<D, BK, NH>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              C::kSmemBytes),
+                         "cudaFuncSetAttribute(fmha_fwd_kernel)")) != BSA_OK)
+      return st;
+    attr_set[dev] = true;
+  }
+  const int sms = num_sms();
+  for (int b0 = 0; b0 < a.B; b0 += kMaxFwdBatch) {
+    const int Bn = std::min(kMaxFwdBatch, a.B - b0);
+    FmhaParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int i = 0; i < Bn; ++i) {
+      const int b = b0 + i;
+      const int L = a.seq_lens ? a.seq_lens[b] : a.Sq;
+      p.seq_lens[i] = L;
+      const char* qb = static_cast<const char*>(a.q) + (int64_t)b * a.q_sb * 2;
+      const char* kb = static_cast<const char*>(a.k) + (int64_t)b * a.k_sb * 2;
+      const char* vb = static_cast<const char*>(a.v) + (int64_t)b * a.v_sb * 2;
+      if ((st = encode_map(&p.tq[i], qb, L, a.Hq, D, a.q_ss, a.q_sh, 128, "Q")) != BSA_OK) return st;
+      if ((st = encode_map(&p.tk[i], kb, a.prefix_len + L, a.Hkv, D, a.k_ss, a.k_sh, BK, "K")) != BSA_OK)
+        return st;
+      if ((st = encode_map(&p.tv[i], vb, a.prefix_len + L, a.Hkv, D, a.v_ss, a.v_sh, BK, "V")) != BSA_OK)
+        return st;
+    }
+    p.b0 = b0;
+    p.Bn = Bn;
+    p.Hq = a.Hq;
+    p.G = a.Hq / a.Hkv;
+    p.Sq = a.Sq;
+    p.nQb = a.nQb;
+    p.nKb = a.nKb;
+    p.block_q = a.block_q;
+    p.prefix_len = a.prefix_len;
+    p.n_tiles = Bn * a.nQb * a.Hq;
+    p.indices = a.indices;
+    p.counts = a.counts;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.lse = a.lse;
+    const int grid = std::min(p.n_tiles, sms);
+    if (grid <= 0) continue;
+    fmha_fwd_kernel<D, BK, NH><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
+    if ((st = cuda_check(cudaGetLastError(), "fmha_fwd_kernel launch")) != BSA_OK) return st;
+  }
+  return BSA_OK;
+}
+
+}  // namespace
+
+unsigned int read_and_clear_device_error() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_bsa_error, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (v != 0) cudaMemcpyToSymbol(g_bsa_error, &zero, sizeof(zero));
+  return v;
+}
+
+bsa_status launch_forward(const ForwardArgs& a, cudaStream_t stream) {
+  const int nh = a.block_q > 128 ? 2 : 1;
+  if (a.d == 128 && a.block_k == 128) return nh == 2 ? launch_t<128, 128, 2>(a, stream) : launch_t<128, 128, 1>(a, stream);
+  if (a.d == 128 && a.block_k == 64) return nh == 2 ? launch_t<128, 64, 2>(a, stream) : launch_t<128, 64, 1>(a, stream);
+  if (a.d == 64 && a.block_k == 128) return nh == 2 ? launch_t<64, 128, 2>(a, stream) : launch_t<64, 128, 1>(a, stream);
+  if (a.d == 64 && a.block_k == 64) return nh == 2 ? launch_t<64, 64, 2>(a, stream) : launch_t<64, 64, 1>(a, stream);
+  return set_error(BSA_ERR_UNSUPPORTED, "bsa_forward: unsupported (d, block_k)");
+}
+
+}  // namespace bsa

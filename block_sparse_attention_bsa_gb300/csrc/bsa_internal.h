@@ -1,0 +1,68 @@
+// Host-side declarations shared by the translation units of libbsa.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "../../include/bsa.h"
+
+namespace bsa {
+
+constexpr int kMaxSelectBatch = 64;   // batch elements per select launch
+constexpr int kMaxHeads = 256;        // query heads (keep ratios in kernel params)
+constexpr int kMaxFwdBatch = 8;       // batch elements per forward launch (tensor maps)
+
+inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Records `msg` as this thread's last error and returns `st`.
+bsa_status set_error(bsa_status st, const std::string& msg);
+void clear_error();
+
+// Checks a CUDA call; on failure records the call site and returns BSA_ERR_CUDA.
+bsa_status cuda_check(cudaError_t e, const char* what);
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// ---- selector (bsa_select.cu) ----
+struct SelectArgs {
+  const void* q; int64_t q_sb, q_ss, q_sh;
+  const void* k; int64_t k_sb, k_ss, k_sh;
+  int B, Hq, Hkv, Sq, Skv, d, block_q, block_k, prefix_len;
+  int nQb, nKb;
+  const int32_t* seq_lens;   // host
+  const float* keep;         // host, Hq values (expanded)
+  int32_t* indices;
+  int32_t* counts;
+  float* qbar;               // workspace [B,Hq,nQb,d]
+  float* kbar;               // workspace [B,Hkv,nKb,d]
+};
+bsa_status launch_select(const SelectArgs& a, cudaStream_t stream);
+
+// ---- forward (bsa_fmha.cu) ----
+struct ForwardArgs {
+  const void* q; int64_t q_sb, q_ss, q_sh;
+  const void* k; int64_t k_sb, k_ss, k_sh;
+  const void* v; int64_t v_sb, v_ss, v_sh;
+  int B, Hq, Hkv, Sq, Skv, d, block_q, block_k, prefix_len;
+  int nQb, nKb;
+  const int32_t* seq_lens;   // host, B values
+  const int32_t* indices;    // NULL = dense
+  const int32_t* counts;
+  float scale;
+  void* out;
+  float* lse;
+};
+bsa_status launch_forward(const ForwardArgs& a, cudaStream_t stream);
+
+// Device error word of the current device (0xFFFFFFFF if it cannot be read);
+// cleared after reading.
+unsigned int read_and_clear_device_error();
+
+// ---- validation (bsa_api.cu) ----
+size_t select_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int d, int bq, int bk);
+
+}  // namespace bsa

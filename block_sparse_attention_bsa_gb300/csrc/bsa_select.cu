@@ -1,0 +1,278 @@
+// Selector kernels: block mean pooling of Q and K, block scores, per-row
+// top-k with the protected prefix forced in and the lowest-index tie rule,
+// and compaction to ascending index lists.
+//
+// The selector's contract is the one of the vllm-omni pull request "[Core]
+// Add shared block-sparse attention adapters with FlashAttention-4"
+// (Purpose): per-query-head block indices and counts, protected KV prefix,
+// suffix padding excluded, native GQA mapping (query head h scores against
+// KV head h / G, as _repeat_kv_heads in cosmos_parallel.py pairs them).
+#include <cuda_bf16.h>
+
+#include <cfloat>
+#include <cmath>
+#include <cstdint>
+
+#include "bsa_internal.h"
+
+namespace bsa {
+namespace {
+
+// ------------------------------------------------------------- pooling ---
+// One CTA per (block, batch element, 64 16-byte columns).  Thread column c
+// covers 8 channels of one head; the 4 row groups of the CTA split the
+// block's rows and are summed in shared memory.  HBM-bound: every element of
+// Q and K is read exactly once with 16-byte loads.
+
+constexpr int kPoolCols = 64;
+constexpr int kPoolGroups = 4;
+
+struct PoolParams {
+  const __nv_bfloat16* x;
+  int64_t sb, ss, sh;        // element strides
+  int H, D, block, nb, cols; // cols = H * D / 8
+  int valid[kMaxSelectBatch];
+  float* out;                // [B, H, nb, D]
+};
+
+__global__ void __launch_bounds__(kPoolCols* kPoolGroups)
+    pool_kernel(const __grid_constant__ PoolParams p) {
+  const int blk = blockIdx.x;
+  const int b = blockIdx.y;
+  const int tc = threadIdx.x % kPoolCols;
+  const int g = threadIdx.x / kPoolCols;
+  const int c = blockIdx.z * kPoolCols + tc;
+  const int r0 = blk * p.block;
+  const int r1 = min(r0 + p.block, p.valid[b]);
+  const int dc = p.D / 8;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  int h = 0, d0 = 0;
+  if (c < p.cols) {
+    h = c / dc;
+    d0 = (c % dc) * 8;
+    const __nv_bfloat16* base = p.x + (int64_t)b * p.sb + (int64_t)h * p.sh + d0;
+#pragma unroll 4
+    for (int r = r0 + g; r < r1; r += kPoolGroups) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)r * p.ss));
+      const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(v2[i]);
+        acc[2 * i] += f.x;
+        acc[2 * i + 1] += f.y;
+      }
+    }
+  }
+  __shared__ float red[kPoolGroups][kPoolCols][9];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[g][tc][i] = acc[i];
+  __syncthreads();
+  if (g == 0 && c < p.cols) {
+    const int n = max(r1 - r0, 0);
+    const float inv = n > 0 ? 1.f / (float)n : 0.f;
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float s = red[0][tc][i];
+#pragma unroll
+      for (int gg = 1; gg < kPoolGroups; ++gg) s += red[gg][tc][i];
+      m[i] = s * inv;
+    }
+    float* o = p.out + (((int64_t)b * p.H + h) * p.nb + blk) * p.D + d0;
+    reinterpret_cast<float4*>(o)[0] = make_float4(m[0], m[1], m[2], m[3]);
+    reinterpret_cast<float4*>(o)[1] = make_float4(m[4], m[5], m[6], m[7]);
+  }
+}
+
+// ---------------------------------------------------- score + top-k -------
+// One CTA per (batch element, query head, kRows query blocks); one warp per
+// query block (row).  Candidate block means are staged 32 at a time in
+// shared memory; each lane scores one candidate (fp32 dot product of the
+// two means).  Selection: the kh-th largest score key is found bit by bit
+// (32 counting passes), then one pass in ascending block order writes the
+// blocks above it plus the lowest-index blocks equal to it.
+
+constexpr int kRows = 8;
+
+struct TopkParams {
+  const float* qbar;   // [B, Hq, nQb, D]
+  const float* kbar;   // [B, Hkv, nKb, D]
+  int Hq, Hkv, nQb, nKb, D, block_q, block_k, prefix_len;
+  int seq_lens[kMaxSelectBatch];
+  float keep[kMaxHeads];
+  int32_t* indices;    // [B, Hq, nQb, nKb]
+  int32_t* counts;     // [B, Hq, nQb]
+};
+
+// Monotone map float -> uint32 (larger float => larger key); -0 and +0 map to
+// the same key because the score is canonicalised first.
+__device__ __forceinline__ uint32_t order_key(float s) {
+  const uint32_t u = __float_as_uint(s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// k = min(N, ceil(r * N)) in double precision (same expression as the host).
+__device__ __forceinline__ int keep_count_dev(float r, int n) {
+  if (n <= 0 || !(r > 0.f)) return 0;
+  const double v = ceil((double)r * (double)n);
+  return v >= (double)n ? n : (int)v;
+}
+
+__global__ void __launch_bounds__(kRows * 32) score_topk_kernel(const __grid_constant__ TopkParams p) {
+  extern __shared__ float sm[];
+  const int D = p.D;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int qb = blockIdx.x * kRows + warp;
+  const int L = p.seq_lens[b];
+  const int valid_kv = p.prefix_len + L;
+  const int nkv = (valid_kv + p.block_k - 1) / p.block_k;
+  const int npb = min((p.prefix_len + p.block_k - 1) / p.block_k, nkv);
+  const int N = nkv - npb;
+  const int kh = keep_count_dev(p.keep[h], N);
+  const int nqv = (L + p.block_q - 1) / p.block_q;
+  const int hk = h / (p.Hq / p.Hkv);
+  const bool row_on = qb < p.nQb;
+  const bool row_valid = qb < nqv;
+
+  float* qs = sm;                       // [kRows][D]
+  float* ks = qs + kRows * D;           // [32][D + 1]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(ks + 32 * (D + 1));   // [kRows][nKb]
+  uint32_t* my_keys = keys + (size_t)warp * p.nKb;
+
+  const bool need_scores = row_valid && kh > 0 && kh < N;
+  // Every warp of the CTA takes part in staging, so the CTA-wide decision
+  // is whether any row needs scores.
+  const int cta_rows_valid = min(kRows, max(0, nqv - (int)blockIdx.x * kRows));
+  const bool cta_scores = cta_rows_valid > 0 && kh > 0 && kh < N;
+
+  if (cta_scores) {
+    for (int i = threadIdx.x; i < kRows * D; i += blockDim.x) {
+      const int r = i / D, e = i % D;
+      const int qbr = blockIdx.x * kRows + r;
+      qs[i] = (qbr < nqv) ? p.qbar[(((int64_t)b * p.Hq + h) * p.nQb + qbr) * D + e] : 0.f;
+    }
+    const float* kb_base = p.kbar + ((int64_t)b * p.Hkv + hk) * p.nKb * D;
+    for (int kb0 = npb; kb0 < nkv; kb0 += 32) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < 32 * D; i += blockDim.x) {
+        const int r = i / D, e = i % D;
+        ks[r * (D + 1) + e] = (kb0 + r < nkv) ? kb_base[(int64_t)(kb0 + r) * D + e] : 0.f;
+      }
+      __syncthreads();
+      if (need_scores && kb0 + lane < nkv) {
+        const float* qr = qs + warp * D;
+        const float* kr = ks + lane * (D + 1);
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        for (int e = 0; e < D; e += 4) {
+          s0 = fmaf(qr[e], kr[e], s0);
+          s1 = fmaf(qr[e + 1], kr[e + 1], s1);
+          s2 = fmaf(qr[e + 2], kr[e + 2], s2);
+          s3 = fmaf(qr[e + 3], kr[e + 3], s3);
+        }
+        const float s = ((s0 + s1) + (s2 + s3)) + 0.f;   // -0 -> +0
+        my_keys[kb0 + lane - npb] = order_key(s);
+      }
+    }
+    __syncwarp();
+  }
+  if (!row_on) return;
+  const int64_t row_id = ((int64_t)b * p.Hq + h) * p.nQb + qb;
+  int32_t* out_idx = p.indices + row_id * p.nKb;
+  if (!row_valid) {
+    if (lane == 0) p.counts[row_id] = 0;
+    return;
+  }
+  for (int i = lane; i < npb; i += 32) out_idx[i] = i;
+  if (lane == 0) p.counts[row_id] = npb + kh;
+  if (kh == 0) return;
+  if (kh >= N) {
+    for (int i = lane; i < N; i += 32) out_idx[npb + i] = npb + i;
+    return;
+  }
+  // Threshold T = largest key with count(key >= T) >= kh, i.e. the kh-th key.
+  uint32_t T = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = T | (1u << bit);
+    int cnt = 0;
+    for (int i = lane; i < N; i += 32) cnt += (my_keys[i] >= cand) ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (cnt >= kh) T = cand;
+  }
+  int c_gt = 0;
+  for (int i = lane; i < N; i += 32) c_gt += (my_keys[i] > T) ? 1 : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c_gt += __shfl_xor_sync(0xffffffffu, c_gt, o);
+  const int need_eq = kh - c_gt;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int written = 0, eq_seen = 0;
+  for (int i0 = 0; i0 < N; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = (i < N) ? my_keys[i] : 0u;
+    const bool gt = (i < N) && key > T;
+    const bool eq = (i < N) && key == T;
+    const uint32_t eq_ball = __ballot_sync(0xffffffffu, eq);
+    const int eq_rank = eq_seen + __popc(eq_ball & lt_mask);
+    const bool sel = gt || (eq && eq_rank < need_eq);
+    const uint32_t sel_ball = __ballot_sync(0xffffffffu, sel);
+    if (sel) out_idx[npb + written + __popc(sel_ball & lt_mask)] = npb + i;
+    written += __popc(sel_ball);
+    eq_seen += __popc(eq_ball);
+  }
+}
+
+}  // namespace
+
+bsa_status launch_select(const SelectArgs& a, cudaStream_t stream) {
+  bsa_status st;
+  // Pool Q over real query rows and K over real keys of every block.
+  {
+    PoolParams p{};
+    p.x = static_cast<const __nv_bfloat16*>(a.q);
+    p.sb = a.q_sb; p.ss = a.q_ss; p.sh = a.q_sh;
+    p.H = a.Hq; p.D = a.d; p.block = a.block_q; p.nb = a.nQb; p.cols = a.Hq * a.d / 8;
+    for (int b = 0; b < a.B; ++b) p.valid[b] = a.seq_lens ? a.seq_lens[b] : a.Sq;
+    p.out = a.qbar;
+    dim3 grid(a.nQb, a.B, (p.cols + kPoolCols - 1) / kPoolCols);
+    pool_kernel<<<grid, kPoolCols * kPoolGroups, 0, stream>>>(p);
+    if ((st = cuda_check(cudaGetLastError(), "pool_kernel(Q) launch")) != BSA_OK) return st;
+  }
+  {
+    PoolParams p{};
+    p.x = static_cast<const __nv_bfloat16*>(a.k);
+    p.sb = a.k_sb; p.ss = a.k_ss; p.sh = a.k_sh;
+    p.H = a.Hkv; p.D = a.d; p.block = a.block_k; p.nb = a.nKb; p.cols = a.Hkv * a.d / 8;
+    for (int b = 0; b < a.B; ++b) p.valid[b] = a.prefix_len + (a.seq_lens ? a.seq_lens[b] : a.Sq);
+    p.out = a.kbar;
+    dim3 grid(a.nKb, a.B, (p.cols + kPoolCols - 1) / kPoolCols);
+    pool_kernel<<<grid, kPoolCols * kPoolGroups, 0, stream>>>(p);
+    if ((st = cuda_check(cudaGetLastError(), "pool_kernel(K) launch")) != BSA_OK) return st;
+  }
+  {
+    TopkParams p{};
+    p.qbar = a.qbar; p.kbar = a.kbar;
+    p.Hq = a.Hq; p.Hkv = a.Hkv; p.nQb = a.nQb; p.nKb = a.nKb; p.D = a.d;
+    p.block_q = a.block_q; p.block_k = a.block_k; p.prefix_len = a.prefix_len;
+    for (int b = 0; b < a.B; ++b) p.seq_lens[b] = a.seq_lens ? a.seq_lens[b] : a.Sq;
+    for (int h = 0; h < a.Hq; ++h) p.keep[h] = a.keep[h];
+    p.indices = a.indices; p.counts = a.counts;
+    const size_t smem = sizeof(float) * ((size_t)kRows * a.d + 32 * (a.d + 1)) +
+                        sizeof(uint32_t) * (size_t)kRows * a.nKb;
+    if (smem > 227 * 1024)
+      return set_error(BSA_ERR_UNSUPPORTED, "bsa_select: too many key blocks (nKb=" +
+                                                std::to_string(a.nKb) + ") for one CTA's shared memory");
+    if ((st = cuda_check(cudaFuncSetAttribute(score_topk_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                         "cudaFuncSetAttribute(score_topk_kernel)")) != BSA_OK)
+      return st;
+    dim3 grid((a.nQb + kRows - 1) / kRows, a.Hq, a.B);
+    score_topk_kernel<<<grid, kRows * 32, smem, stream>>>(p);
+    if ((st = cuda_check(cudaGetLastError(), "score_topk_kernel launch")) != BSA_OK) return st;
+  }
+  return BSA_OK;
+}
+
+}  // namespace bsa

@@ -1,0 +1,175 @@
+/*
+ * bsa.h -- C ABI of libbsa, selected-block (block-sparse) attention on GB300.
+ *
+ * The operations come from the vllm-omni pull request "[Core] Add shared
+ * block-sparse attention adapters with FlashAttention-4" (Purpose): a
+ * selector produces per-query-head key-block indices and counts, and an
+ * attention adapter executes exactly that selection, keeping a protected KV
+ * prefix, the native MHA/MQA/GQA head mapping and the block geometry, masking
+ * single-document suffix padding, and never falling back to dense attention
+ * or expanding K/V.  The attention semantics (generation queries attend
+ * non-causally over cat(understanding, generation) keys; query head i reads
+ * KV head i / (Hq/Hkv); padded keys are masked) are those of
+ * cosmos_parallel.py (cosmos3_cp_attention, _repeat_kv_heads,
+ * build_gen_key_mask).  The default softmax scale head_dim^-1/2 is the one
+ * mstar PR 927 ("What the review checked") names.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor memory is device memory owned by the caller.  The library
+ *    allocates nothing, never synchronises, and enqueues all work on the
+ *    caller's stream (NULL = the legacy default stream).
+ *  - Q: [B, Sq, Hq, d] bf16; K, V: [B, Skv, Hkv, d] bf16, described by
+ *    bsa_tensor (element strides, innermost dim contiguous, base and every
+ *    stride 16-byte aligned).  Key position t < prefix_len is the protected
+ *    prefix; position prefix_len + i is generation token i.
+ *  - seq_lens (HOST array of B int32, or NULL = every request has length Sq):
+ *    request b has L_b real query rows [0, L_b) and real keys
+ *    [0, prefix_len + L_b); everything after is suffix padding that is never
+ *    read into a result.  Requires L_b <= Sq and prefix_len + L_b <= Skv.
+ *  - Blocks: query block qb = rows [qb*block_q, (qb+1)*block_q); key block kb
+ *    = key positions [kb*block_k, (kb+1)*block_k), tiling the concatenated
+ *    sequence from position 0.  nQb = ceil(Sq/block_q), nKb = ceil(Skv/block_k).
+ *    A key block holding any prefix position is a prefix block:
+ *    npb = ceil(prefix_len/block_k).
+ *  - Supported: d in {64, 128}; (block_q, block_k) in {(64,64), (128,128),
+ *    (256,128), (128,64), (256,64)}; Hq % Hkv == 0; bf16 only.  Anything else
+ *    returns BSA_ERR_UNSUPPORTED (no fallback path exists).
+ *  - Errors: every call validates its arguments on the host before launching
+ *    and returns a status; bsa_get_last_error() gives a message naming the
+ *    argument and value (thread-local, valid until the next call on the
+ *    thread).  Launch failures return BSA_ERR_CUDA.  Device-side waits are
+ *    bounded: a wait that gives up sets a device error word that
+ *    bsa_device_status() reports as BSA_ERR_TIMEOUT.
+ */
+#ifndef BSA_H_
+#define BSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BSA_API __attribute__((visibility("default")))
+#else
+#define BSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bsa_status {
+  BSA_OK = 0,
+  BSA_ERR_INVALID_ARG = 1,      /* bad shape, pointer, stride or value */
+  BSA_ERR_UNSUPPORTED = 2,      /* valid but not implemented (d, geometry, dtype) */
+  BSA_ERR_WORKSPACE = 3,        /* workspace missing, misaligned or too small */
+  BSA_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed */
+  BSA_ERR_INVALID_INDICES = 5,  /* bsa_validate_indices found malformed rows */
+  BSA_ERR_TIMEOUT = 6           /* a bounded device wait gave up */
+} bsa_status;
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st* bsa_stream_t;
+
+/* A 4-D bf16 tensor [B, S, H, D] in device memory.  Strides are in elements;
+ * the D axis has stride 1.  ptr, stride_b, stride_s and stride_h must give
+ * 16-byte aligned rows (stride_* * 2 bytes a multiple of 16). */
+typedef struct bsa_tensor {
+  const void* ptr;
+  int64_t B, S, H, D;
+  int64_t stride_b, stride_s, stride_h;
+} bsa_tensor;
+
+/* Library version as 10000*major + 100*minor + patch. */
+BSA_API int bsa_version(void);
+
+/* Message for the last failed call on this thread ("" if none). */
+BSA_API const char* bsa_get_last_error(void);
+
+/* ---------------------------------------------------------------- select ---
+ * Workspace bytes bsa_select needs: fp32 block means of Q [B,Hq,nQb,d] and K
+ * [B,Hkv,nKb,d], each 256-byte aligned. */
+BSA_API size_t bsa_select_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int d,
+                                 int block_q, int block_k);
+
+/* Selector: per (request b, query head h, query block qb) the list of key
+ * blocks to attend (PR 8335, Purpose: "the selector produces per-query-head
+ * block indices/counts").
+ *
+ * For each valid query block (qb < ceil(L_b/block_q)):
+ *   qbar = mean of Q[b, rows, h, :] over the block's real rows, and for each
+ *   key block kbar = mean of K[b, keys, h / (Hq/Hkv), :] over its real keys
+ *   (fp32 sums); score(kb) = qbar . kbar (fp32) for the N_b non-prefix valid
+ *   key blocks; k_h = min(N_b, ceil(r_h * N_b)) computed in double precision
+ *   from the float keep ratio; the row lists the npb prefix blocks followed
+ *   by the k_h best candidates under (score descending, block index
+ *   ascending) -- ties go to the lower index -- all written ascending.
+ *   counts = npb + k_h.  Query blocks with no real row get count 0.
+ *
+ * keep_ratio: HOST array of n_keep floats in [0,1]; n_keep is 1 (shared) or
+ *   Hq (per query head).
+ * indices: device int32 [B, Hq, nQb, nKb]; entries past a row's count are
+ *   left untouched.  counts: device int32 [B, Hq, nQb].
+ * workspace: device, >= bsa_select_workspace_size(...) bytes, 256-B aligned.
+ * Returns BSA_OK once the kernels are enqueued. */
+BSA_API bsa_status bsa_select(const bsa_tensor* q, const bsa_tensor* k, int32_t prefix_len,
+                      const int32_t* seq_lens, int32_t block_q, int32_t block_k,
+                      const float* keep_ratio, int32_t n_keep,
+                      int32_t* indices, int32_t* counts,
+                      void* workspace, size_t ws_bytes, bsa_stream_t stream);
+
+/* --------------------------------------------------------------- forward ---
+ * Workspace bytes bsa_forward needs (the work-tile order list). */
+BSA_API size_t bsa_forward_workspace_size(int B, int Hq, int Sq, int block_q);
+
+/* Selected-block attention forward (PR 8335, Purpose: the adapter executes
+ * the selection; cosmos_parallel.py cosmos3_cp_attention: non-causal
+ * attention of generation queries over cat(und, gen) keys).
+ *
+ * For each request b, query head h and real query row i < L_b in block qb:
+ *   keys = positions of the listed blocks indices[b,h,qb,0:count] that are
+ *   < prefix_len + L_b, read from KV head h / (Hq/Hkv);
+ *   z_j = (q_i . k_j) * softmax_scale;  out_i = sum_j softmax(z)_j v_j (bf16);
+ *   lse_i = ln sum_j exp(z_j)  (fp32, natural log of the scaled logits).
+ * Padded rows (i >= L_b) and rows with no key: out 0, lse -inf.
+ *
+ * indices/counts: device int32 as written by bsa_select, or indices == NULL
+ *   for the dense pass (every valid key block; counts is then ignored and may
+ *   be NULL).  A count above nKb is clamped to nKb; indices are not checked
+ *   here (see bsa_validate_indices); an out-of-range index reads zeros.
+ * softmax_scale <= 0 selects head_dim^-1/2.
+ * out: device bf16 [B, Sq, Hq, d] contiguous.  lse: device fp32 [B, Hq, Sq]
+ *   contiguous, or NULL.
+ * workspace: device, >= bsa_forward_workspace_size(...) bytes, 256-B aligned.
+ * Q, K, V may not alias out. */
+BSA_API bsa_status bsa_forward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tensor* v,
+                       const int32_t* indices, const int32_t* counts,
+                       int32_t prefix_len, const int32_t* seq_lens,
+                       int32_t block_q, int32_t block_k, float softmax_scale,
+                       void* out, float* lse,
+                       void* workspace, size_t ws_bytes, bsa_stream_t stream);
+
+/* ------------------------------------------------------------ validation ---
+ * Debug check of index lists (PR 8335, Purpose: provider failures propagate
+ * as errors).  Counts the rows (b, h, qb) whose list is malformed: count
+ * outside [0, nKb_valid(b)], an index outside [0, nKb_valid(b)), indices not
+ * strictly ascending, or (require_prefix != 0) a valid row whose first npb
+ * entries are not 0..npb-1.  Rows of query blocks without real rows must have
+ * count 0.  Writes the number of bad rows to *bad_rows (device int32),
+ * asynchronously; the caller reads it after synchronising. */
+BSA_API bsa_status bsa_validate_indices(const int32_t* indices, const int32_t* counts,
+                                int32_t B, int32_t Hq, int32_t Sq, int32_t Skv,
+                                int32_t prefix_len, const int32_t* seq_lens,
+                                int32_t block_q, int32_t block_k, int32_t require_prefix,
+                                int32_t* bad_rows, bsa_stream_t stream);
+
+/* Synchronises `stream`, then reports and clears the device error word of the
+ * current device: BSA_ERR_TIMEOUT if a bounded wait in a kernel gave up since
+ * the last call, BSA_ERR_CUDA if the stream reports an error, else BSA_OK. */
+BSA_API bsa_status bsa_device_status(bsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_H_ */

@@ -1,0 +1,193 @@
+"""The C-ABI library loads, exports what include/bsa.h declares, and rejects
+bad arguments on the host before anything reaches a GPU (CPU only).
+
+Every call below fails host-side validation, so none of them launches a
+kernel: they are safe with fake device pointers and without a GPU.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_attention_bsa_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _lib.load()
+
+
+def declared_symbols():
+    txt = open(os.path.join(ROOT, "include", "bsa.h")).read()
+    return sorted(set(re.findall(r"BSA_API\s+[\w\s\*]+?\b(bsa_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_expected_calls():
+    assert declared_symbols() == sorted([
+        "bsa_version", "bsa_get_last_error", "bsa_select_workspace_size", "bsa_select",
+        "bsa_forward_workspace_size", "bsa_forward", "bsa_validate_indices", "bsa_device_status",
+    ])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) == set(_lib.SIGNATURES)
+
+
+def test_only_api_symbols_are_exported():
+    build()
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.lib_path()], capture_output=True, text=True).stdout
+    ours = sorted({l.split()[-1] for l in out.splitlines() if l.split() and l.split()[-1].startswith("bsa_")})
+    assert ours == declared_symbols()
+
+
+def test_version(lib):
+    assert lib.bsa_version() == 100
+
+
+FAKE = 0x10000   # 16-byte aligned, never dereferenced: every call below fails validation first
+
+
+def T(B=1, S=512, H=4, D=128, sb=None, ss=None, sh=None, ptr=FAKE):
+    sh = D if sh is None else sh
+    ss = H * D if ss is None else ss
+    sb = S * H * D if sb is None else sb
+    return _lib.BsaTensor(ptr, B, S, H, D, sb, ss, sh)
+
+
+def call_select(lib, q, k, prefix=0, lens=None, bq=256, bk=128, keep=(0.25,), n_keep=None,
+                ind=FAKE, cnt=FAKE, ws=FAKE, ws_bytes=1 << 40):
+    keep_arr = (ctypes.c_float * len(keep))(*keep)
+    lens_arr = (ctypes.c_int32 * len(lens))(*lens) if lens is not None else None
+    return lib.bsa_select(ctypes.byref(q) if q is not None else None, ctypes.byref(k), prefix, lens_arr,
+                          bq, bk, keep_arr, len(keep) if n_keep is None else n_keep, ind, cnt, ws,
+                          ws_bytes, None)
+
+
+def call_forward(lib, q, k, v, prefix=0, lens=None, bq=256, bk=128, scale=0.0, out=FAKE, ws=None, ws_bytes=0):
+    lens_arr = (ctypes.c_int32 * len(lens))(*lens) if lens is not None else None
+    return lib.bsa_forward(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), None, None, prefix, lens_arr,
+                           bq, bk, scale, out, None, ws, ws_bytes, None)
+
+
+def err(lib):
+    return lib.bsa_get_last_error().decode()
+
+
+@pytest.mark.parametrize("case,status,needle", [
+    ("null_q", 1, "q descriptor is NULL"),
+    ("head_dim", 2, "head dim 96"),
+    ("gqa", 1, "not a multiple of Hkv"),
+    ("geometry", 2, "block geometry"),
+    ("misaligned", 1, "16-byte aligned"),
+    ("stride", 1, "multiples of 8"),
+    ("seq_len", 1, "seq_lens[0]"),
+    ("prefix_overflow", 1, "exceeds Skv"),
+    ("neg_prefix", 1, "negative"),
+    ("keep_range", 1, "outside [0, 1]"),
+    ("n_keep", 1, "n_keep"),
+    ("workspace_small", 3, "smaller than"),
+    ("workspace_null", 3, "workspace is NULL"),
+    ("workspace_align", 3, "256-byte aligned"),
+    ("batch_mismatch", 1, "batch of q"),
+])
+def test_select_rejects_bad_arguments(lib, case, status, needle):
+    q, k = T(H=4), T(H=2, S=512 + 256)
+    kw = dict(prefix=256)
+    if case == "null_q":
+        q = None
+    elif case == "head_dim":
+        q, k = T(D=96), T(D=96, S=768)
+    elif case == "gqa":
+        q, k = T(H=3), T(H=2, S=768)
+    elif case == "geometry":
+        kw["bq"] = 96
+    elif case == "misaligned":
+        q = T(ptr=FAKE + 2)
+    elif case == "stride":
+        q = T(ss=4 * 128 + 4)
+    elif case == "seq_len":
+        kw["lens"] = [513]
+    elif case == "prefix_overflow":
+        kw["prefix"] = 300
+    elif case == "neg_prefix":
+        kw["prefix"] = -1
+    elif case == "keep_range":
+        kw["keep"] = (1.5,)
+    elif case == "n_keep":
+        kw["keep"] = (0.2, 0.3)
+    elif case == "workspace_small":
+        kw["ws_bytes"] = 16
+    elif case == "workspace_null":
+        kw["ws"] = None
+    elif case == "workspace_align":
+        kw["ws"] = FAKE + 16
+    elif case == "batch_mismatch":
+        k = T(B=2, H=2, S=768)
+    st = call_select(lib, q, k, **kw)
+    assert st == status, (case, st, err(lib))
+    assert needle in err(lib), err(lib)
+
+
+def test_select_workspace_size_formula(lib):
+    # fp32 means of Q [B,Hq,nQb,d] and K [B,Hkv,nKb,d], each rounded up to 256 B
+    B, Hq, Hkv, Sq, Skv, d, bq, bk = 1, 32, 8, 172800, 173824, 128, 256, 128
+    want = ((B * Hq * 675 * d * 4 + 255) // 256) * 256 + ((B * Hkv * 1358 * d * 4 + 255) // 256) * 256
+    assert lib.bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, bq, bk) == want
+    assert lib.bsa_select_workspace_size(0, Hq, Hkv, Sq, Skv, d, bq, bk) == 0
+
+
+@pytest.mark.parametrize("case,status,needle", [
+    ("v_shape", 1, "v shape"),
+    ("out_null", 1, "out is NULL"),
+    ("out_align", 1, "out is not 16-byte aligned"),
+    ("scale_nan", 1, "softmax_scale"),
+    ("geometry", 2, "block geometry"),
+])
+def test_forward_rejects_bad_arguments(lib, case, status, needle):
+    q, k, v = T(H=4), T(H=2, S=768), T(H=2, S=768)
+    kw = dict(prefix=256)
+    if case == "v_shape":
+        v = T(H=2, S=700)
+    elif case == "out_null":
+        kw["out"] = None
+    elif case == "out_align":
+        kw["out"] = FAKE + 8
+    elif case == "scale_nan":
+        kw["scale"] = float("nan")
+    elif case == "geometry":
+        kw["bk"] = 256
+    st = call_forward(lib, q, k, v, **kw)
+    assert st == status, (case, st, err(lib))
+    assert needle in err(lib), err(lib)
+
+
+def test_forward_counts_required_with_indices(lib):
+    q, k, v = T(H=4), T(H=2, S=768), T(H=2, S=768)
+    st = lib.bsa_forward(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), FAKE, None, 256, None, 256, 128,
+                         0.0, FAKE, None, None, 0, None)
+    assert st == 1 and "counts is NULL" in err(lib)
+
+
+def test_validate_rejects_bad_sizes(lib):
+    st = lib.bsa_validate_indices(FAKE, FAKE, 0, 4, 512, 768, 256, None, 256, 128, 1, FAKE, None)
+    assert st == 1
+    st = lib.bsa_validate_indices(None, FAKE, 1, 4, 512, 768, 256, None, 256, 128, 1, FAKE, None)
+    assert st == 1
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    import block_sparse_attention_bsa_gb300 as bsa
+    q = torch.zeros(1, 256, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        bsa.bsa_select(q, q, 0, None, 64, 64, 0.5)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        bsa.bsa_forward(q, q, q, None, None, 0, None, 64, 64)

@@ -1,0 +1,257 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases compare every element; the five workload configs compare every
+selection row and sampled attention tiles, in the launch configuration the
+bench times.  Invariants that must hold bit for bit on the GPU (dense pass ==
+keep 1, dropped blocks do not matter, NaN padding is never read, GQA == MHA
+with repeated K/V, strided views) are checked directly.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_bsa_gb300 as bsa
+from bsa_inputs import CONFIGS, WORKLOAD_CONFIGS, make_inputs
+from oracle import bsa_oracle as O
+from parity_utils import (check_structure, compare_attention, compare_selection, sample_tiles,
+                          to_f32_np)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["tiny", "small_gqa", "small_mqa_d64", "small_mha_perhead", "small_64x64_d128"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    bsa.build()
+
+
+def cuda_inputs(name, pad_fill=float("nan"), **kw):
+    inp = make_inputs(CONFIGS[name], "cpu", pad_fill=pad_fill, **kw)
+    for key in ("q", "k", "v"):
+        inp[key] = inp[key].cuda()
+    return inp
+
+
+def run_select(inp, keep=None):
+    c = inp["cfg"]
+    idx, cnt = bsa.bsa_select(inp["q"], inp["k"], c.prefix, inp["seq_lens"], c.block_q, c.block_k,
+                              inp["keep_ratio"] if keep is None else keep)
+    bsa.bsa_device_status()
+    return idx, cnt
+
+
+def run_forward(inp, idx, cnt, q=None, k=None, v=None):
+    c = inp["cfg"]
+    out, lse = bsa.bsa_forward(inp["q"] if q is None else q, inp["k"] if k is None else k,
+                               inp["v"] if v is None else v, idx, cnt, c.prefix, inp["seq_lens"],
+                               c.block_q, c.block_k)
+    bsa.bsa_device_status()
+    return out, lse
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_select_parity_small(name):
+    inp = cuda_inputs(name)
+    c = inp["cfg"]
+    idx, cnt = run_select(inp)
+    ref = O.select_blocks(to_f32_np(inp["q"]), to_f32_np(inp["k"]), c.prefix, inp["seq_lens"],
+                          c.block_q, c.block_k, inp["keep_ratio"])
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    stats = compare_selection(gi, gc, ref)
+    check_structure(gi, gc, c.prefix, inp["seq_lens"], c.block_q, c.block_k)
+    assert bsa.bsa_validate_indices(idx, cnt, c.B, c.Hq, c.Sq, c.Skv, c.prefix, inp["seq_lens"],
+                                    c.block_q, c.block_k) == 0
+    print(name, stats)
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_forward_parity_small(name):
+    inp = cuda_inputs(name)
+    c = inp["cfg"]
+    idx, cnt = run_select(inp)
+    out, lse = run_forward(inp, idx, cnt)
+    q, k, v = (to_f32_np(inp[x]).astype(np.float64) for x in ("q", "k", "v"))
+    o_ref, l_ref = O.attention(q, k, v, idx.cpu().numpy(), cnt.cpu().numpy(), c.prefix, inp["seq_lens"],
+                               c.block_q, c.block_k)
+    stats = compare_attention(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, inp["seq_lens"])
+    print(name, stats)
+
+
+@pytest.mark.parametrize("name", ["small_gqa", "tiny", "small_64x64_d128"])
+def test_dense_pass_equals_keep_one_and_oracle(name):
+    inp = cuda_inputs(name)
+    c = inp["cfg"]
+    idx1, cnt1 = run_select(inp, keep=[1.0])
+    o_null, l_null = run_forward(inp, None, None)
+    o_k1, l_k1 = run_forward(inp, idx1, cnt1)
+    assert torch.equal(o_null, o_k1)
+    assert torch.equal(l_null, l_k1)
+    q, k, v = (to_f32_np(inp[x]).astype(np.float64) for x in ("q", "k", "v"))
+    di, dc = O.dense_indices(c.prefix, inp["seq_lens"], c.Sq, c.Skv, c.block_q, c.block_k, c.Hq)
+    o_ref, l_ref = O.attention(q, k, v, di, dc, c.prefix, inp["seq_lens"], c.block_q, c.block_k)
+    compare_attention(o_null.float().cpu().numpy(), l_null.cpu().numpy(), o_ref, l_ref, inp["seq_lens"])
+
+
+def test_dropped_blocks_leave_output_bitwise_unchanged():
+    inp = cuda_inputs("small_gqa")
+    c = inp["cfg"]
+    idx, cnt = run_select(inp)
+    out, lse = run_forward(inp, idx, cnt)
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    G = c.Hq // c.Hkv
+    k2, v2 = inp["k"].clone(), inp["v"].clone()
+    gen = torch.Generator(device="cuda").manual_seed(9)
+    changed = 0
+    for b in range(c.B):
+        for hk in range(c.Hkv):
+            used = set()
+            for h in range(hk * G, (hk + 1) * G):
+                for qb in range(gc.shape[2]):
+                    used.update(gi[b, h, qb, :gc[b, h, qb]].tolist())
+            for kb in range(O.cdiv(c.Skv, c.block_k)):
+                if kb not in used:
+                    sl = slice(kb * c.block_k, (kb + 1) * c.block_k)
+                    shape = k2[b, sl, hk].shape
+                    k2[b, sl, hk] = (100 * torch.randn(shape, generator=gen, device="cuda")).bfloat16()
+                    v2[b, sl, hk] = (100 * torch.randn(shape, generator=gen, device="cuda")).bfloat16()
+                    changed += 1
+    assert changed > 0
+    out2, lse2 = run_forward(inp, idx, cnt, k=k2, v=v2)
+    assert torch.equal(out, out2)
+    assert torch.equal(lse, lse2)
+
+
+def test_rows_sum_to_one():
+    inp = cuda_inputs("small_gqa")
+    idx, cnt = run_select(inp)
+    ones = torch.ones_like(inp["v"])
+    out, _ = run_forward(inp, idx, cnt, v=ones)
+    for b, L in enumerate(inp["seq_lens"]):
+        err = (out[b, :L].float() - 1).abs().max().item()
+        assert err <= 2 ** -7, err
+
+
+def test_nan_padding_is_never_read():
+    a = cuda_inputs("small_gqa", pad_fill=float("nan"))
+    z = cuda_inputs("small_gqa", pad_fill=0.0)
+    ia, ca = run_select(a)
+    iz, cz = run_select(z)
+    assert torch.equal(ca, cz)
+    for b in range(a["cfg"].B):
+        for h in range(a["cfg"].Hq):
+            for qb in range(ca.shape[2]):
+                c = int(ca[b, h, qb])
+                assert torch.equal(ia[b, h, qb, :c], iz[b, h, qb, :c])
+    oa, la = run_forward(a, ia, ca)
+    oz, lz = run_forward(z, iz, cz)
+    assert torch.equal(oa, oz)
+    assert torch.equal(la, lz)
+    assert torch.isfinite(oa).all()
+
+
+def test_gqa_matches_mha_with_repeated_kv_bitwise():
+    inp = cuda_inputs("small_gqa")
+    c = inp["cfg"]
+    G = c.Hq // c.Hkv
+    idx, cnt = run_select(inp)
+    out, lse = run_forward(inp, idx, cnt)
+    kr = inp["k"].repeat_interleave(G, dim=2).contiguous()
+    vr = inp["v"].repeat_interleave(G, dim=2).contiguous()
+    idx2, cnt2 = bsa.bsa_select(inp["q"], kr, c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    assert torch.equal(cnt, cnt2)
+    out2, lse2 = run_forward(inp, idx2, cnt2, k=kr, v=vr)
+    assert torch.equal(out, out2)
+    assert torch.equal(lse, lse2)
+
+
+def test_strided_views_match_contiguous():
+    inp = cuda_inputs("small_gqa", pad_fill=0.0)
+    c = inp["cfg"]
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    # packed buffers: Q inside [B, Sq, Hq + 8, d]; K/V inside one [B, Skv, 2, Hkv, d] tensor
+    qp = torch.zeros(c.B, c.Sq, c.Hq + 8, c.d, dtype=torch.bfloat16, device="cuda")
+    qp[:, :, 3:3 + c.Hq] = q
+    kv = torch.stack([k, v], dim=2)
+    qs, ks, vs = qp[:, :, 3:3 + c.Hq], kv[:, :, 0], kv[:, :, 1]
+    assert not qs.is_contiguous() and not ks.is_contiguous()
+    idx, cnt = run_select(inp)
+    out, lse = run_forward(inp, idx, cnt)
+    idx2, cnt2 = bsa.bsa_select(qs, ks, c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    assert torch.equal(cnt, cnt2)
+    out2, lse2 = run_forward(inp, idx2, cnt2, q=qs, k=ks, v=vs)
+    assert torch.equal(out, out2)
+    assert torch.equal(lse, lse2)
+
+
+def test_keep_zero_without_prefix_gives_empty_rows():
+    inp = cuda_inputs("small_mha_perhead")
+    idx, cnt = run_select(inp, keep=[0.0])
+    assert int(cnt.max()) == 0
+    out, lse = run_forward(inp, idx, cnt)
+    assert (out == 0).all()
+    assert torch.isneginf(lse).all()
+
+
+def test_validate_finds_corrupted_rows():
+    inp = cuda_inputs("small_gqa")
+    c = inp["cfg"]
+    idx, cnt = run_select(inp)
+    args = (c.B, c.Hq, c.Sq, c.Skv, c.prefix, inp["seq_lens"], c.block_q, c.block_k)
+    assert bsa.bsa_validate_indices(idx, cnt, *args) == 0
+    bad = idx.clone()
+    bad[0, 0, 0, 3] = bad[0, 0, 0, 2]            # not strictly ascending
+    bad[0, 1, 1, 0] = 5                          # prefix block 0 missing
+    bad[1, 2, 0, 4] = 10 ** 6                    # out of range
+    assert bsa.bsa_validate_indices(bad, cnt, *args) == 3
+    cnt2 = cnt.clone()
+    cnt2[1, 0, -1] = 1                           # padded query block with a count
+    assert bsa.bsa_validate_indices(idx, cnt2, *args) == 1
+
+
+def test_out_of_range_indices_are_clamped_not_read():
+    """Indices past the key blocks (and a count above nKb) are clamped by the
+    kernel: the block reads as fully masked, nothing faults."""
+    inp = cuda_inputs("small_gqa")
+    c = inp["cfg"]
+    idx, cnt = run_select(inp)
+    bad = idx.clone()
+    nkb = bad.shape[3]
+    bad[0, 0, 0, cnt[0, 0, 0] - 1] = 10 ** 6
+    cnt_big = cnt.clone()
+    cnt_big[0, 1, 0] = nkb + 50
+    run_forward(inp, bad, cnt_big)
+
+
+# ----------------------------------------------------------- full size ---
+
+def full_inputs(name):
+    cfg = CONFIGS[name]
+    return make_inputs(cfg, "cuda", pad_fill=float("nan"))
+
+
+@pytest.mark.parametrize("name", WORKLOAD_CONFIGS)
+def test_workload_config_parity(name):
+    inp = full_inputs(name)
+    c = inp["cfg"]
+    idx, cnt = run_select(inp)
+    out, lse = run_forward(inp, idx, cnt)
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    q32, k32 = to_f32_np(inp["q"]), to_f32_np(inp["k"])
+    ref = O.select_blocks(q32, k32, c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    sel_stats = compare_selection(gi, gc, ref)
+    check_structure(gi, gc, c.prefix, inp["seq_lens"], c.block_q, c.block_k)
+    tiles = sample_tiles(c.B, c.Hq, gc.shape[2], inp["seq_lens"], c.block_q, n_random=8, seed=c.seed)
+    v32 = to_f32_np(inp["v"])
+    o_ref, l_ref = O.attention(q32, k32, v32, gi, gc, c.prefix, inp["seq_lens"], c.block_q, c.block_k,
+                               tiles=tiles)
+    att = compare_attention(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, inp["seq_lens"])
+    if name == "480p_dense":
+        o_null, l_null = run_forward(inp, None, None)
+        assert torch.equal(o_null, out) and torch.equal(l_null, lse)
+    kept = gc.sum() / max(1, sum(O.cdiv(c.prefix + L, c.block_k) * O.cdiv(L, c.block_q)
+                                 for L in inp["seq_lens"]) * c.Hq)
+    print(name, sel_stats, att, f"tile keep fraction {kept:.4f}")
