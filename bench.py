@@ -133,7 +133,7 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(inp, idx, cnt, n_tiles_sample=3, budget_s=25.0):
+def cpu_baseline(inp, idx, cnt, n_tiles_sample=400, budget_s=20.0):
     """The oracle, as it stands, on a bounded sample of the workload: the full
     selector for one query head and the attention of a few work tiles,
     extrapolated linearly to the whole workload (units: effective TFLOP/s)."""
@@ -158,9 +158,14 @@ def cpu_baseline(inp, idx, cnt, n_tiles_sample=3, budget_s=25.0):
     picks = nz[rng.choice(len(nz), size=min(n_tiles_sample, len(nz)), replace=False)]
     t_att, sampled_pairs = 0.0, 0
     done = 0
-    for b, h, qb in picks:
+    cache = {}
+    for b, h, qb in sorted(map(tuple, picks))[:n_tiles_sample]:
         hk = h // G
-        qh, kh, vh = t_host(q[b:b + 1, :, h:h + 1]), t_host(k[b:b + 1, :, hk:hk + 1]), t_host(v[b:b + 1, :, hk:hk + 1])
+        if (b, h) not in cache:
+            cache.clear()
+            cache[(b, h)] = (t_host(q[b:b + 1, :, h:h + 1]), t_host(k[b:b + 1, :, hk:hk + 1]),
+                             t_host(v[b:b + 1, :, hk:hk + 1]))
+        qh, kh, vh = cache[(b, h)]
         cc = int(cnt_np[b, h, qb])
         t0 = time.perf_counter()
         O.attention_tile(qh, kh, vh, 0, 0, int(qb), idx_np[b, h, qb, :cc], c.prefix, inp["seq_lens"][b],
@@ -287,10 +292,11 @@ def main():
     idx = torch.empty((B, Hq, nQb, nKb), dtype=torch.int32, device="cuda")
     cnt = torch.empty((B, Hq, nQb), dtype=torch.int32, device="cuda")
     ws = torch.empty(bsa.bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, bq, bk), dtype=torch.uint8, device="cuda")
+    fws = torch.empty(max(256, bsa.bsa_forward_workspace_size(B, Hq, Sq, bq)), dtype=torch.uint8, device="cuda")
     out = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
-    launches_per_step = 4     # pool(Q), pool(K), score/top-k, forward
+    launches_per_step = 5     # pool(Q), pool(K), score/top-k, schedule, forward
 
     def step(ev=None):
         if ev is not None:
@@ -298,7 +304,7 @@ def main():
         bsa.bsa_select(q, k, P, lens, bq, bk, keep, indices=idx, counts=cnt, workspace=ws, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        bsa.bsa_forward(q, k, v, idx, cnt, P, lens, bq, bk, out=out, lse=lse, stream=stream)
+        bsa.bsa_forward(q, k, v, idx, cnt, P, lens, bq, bk, out=out, lse=lse, workspace=fws, stream=stream)
         if ev is not None:
             ev[2].record(stream)
 

@@ -214,8 +214,9 @@ bsa_status bsa_select(const bsa_tensor* q, const bsa_tensor* k, int32_t prefix_l
 }
 
 size_t bsa_forward_workspace_size(int B, int Hq, int Sq, int block_q) {
-  (void)B; (void)Hq; (void)Sq; (void)block_q;
-  return 0;
+  (void)Sq; (void)block_q;
+  if (B <= 0 || Hq <= 0) return 0;
+  return (size_t)cdiv64(B, kMaxFwdBatch) * forward_chunk_bytes(Hq);
 }
 
 bsa_status bsa_forward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tensor* v, const int32_t* indices,
@@ -246,7 +247,7 @@ bsa_status bsa_forward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tenso
   a.nQb = (int)cdiv64(q->S, block_q); a.nKb = (int)cdiv64(k->S, block_k);
   a.seq_lens = seq_lens; a.indices = indices; a.counts = counts;
   a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)q->D);
-  a.out = out; a.lse = lse;
+  a.out = out; a.lse = lse; a.workspace = workspace;
   return launch_forward(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

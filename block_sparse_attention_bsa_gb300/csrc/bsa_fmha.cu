@@ -47,9 +47,11 @@ struct FmhaParams {   // CUtensorMap members make it 128-byte aligned
   int seq_lens[kMaxFwdBatch];
   int b0;           // first request of this launch
   int Bn;           // requests in this launch
-  int Hq, G, Sq, nQb, nKb, block_q, prefix_len, n_tiles;
+  int Hq, Hkv, G, Sq, nQb, nKb, block_q, prefix_len, n_tiles;
   const int32_t* indices;  // NULL = dense pass
   const int32_t* counts;
+  int* counter;            // next work tile (zeroed by the schedule kernel)
+  const int* group_order;  // (request, KV head) groups, heaviest first
   float scale_log2;        // softmax scale * log2(e)
   __nv_bfloat16* out;      // [B, Sq, Hq, D]
   float* lse;              // [B, Hq, Sq] or NULL
@@ -80,14 +82,24 @@ struct TileInfo {
   const int32_t* idx;
 };
 
+// Work tile t -> (request, KV head, query block, query head of the group).
+// Tiles are grouped by (request, KV head); groups come in the order the
+// schedule kernel wrote (most selected work first), and inside a group the
+// GQA siblings are innermost, then neighbouring query blocks.  The CTAs
+// running at any moment therefore share one KV head's K/V (<= 90 MB at
+// 720p), which stays resident in the 126 MB L2.
 __device__ __forceinline__ TileInfo decode_tile(const FmhaParams& p, int t, int BK) {
   TileInfo ti;
-  ti.h = t % p.Hq;
-  const int r = t / p.Hq;
-  ti.qb = r % p.nQb;
-  ti.bl = r / p.nQb;
+  const int per_group = p.G * p.nQb;
+  const int gi = t / per_group;
+  const int grp = p.group_order ? p.group_order[gi] : gi;
+  const int w = t - gi * per_group;
+  const int g = w % p.G;
+  ti.qb = w / p.G;
+  ti.hk = grp % p.Hkv;
+  ti.bl = grp / p.Hkv;
+  ti.h = ti.hk * p.G + g;
   ti.b = p.b0 + ti.bl;
-  ti.hk = ti.h / p.G;
   ti.L = p.seq_lens[ti.bl];
   ti.valid_kv = p.prefix_len + ti.L;
   const int64_t row = ((int64_t)ti.b * p.Hq + ti.h) * p.nQb + ti.qb;
@@ -111,6 +123,23 @@ struct Ring {
   }
 };
 
+// Consumer side of the tile-id ring: waits for the next published id, reads
+// it, releases the slot.  Returns -1 at the end of the work (or on abort).
+struct TileRing {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++slot == 2) { slot = 0; phase ^= 1u; }
+  }
+  __device__ __forceinline__ int take(uint64_t* full, uint64_t* empty, volatile int* ids,
+                                      volatile int* abort, bool& ok) {
+    ok = mbar_wait(smem_u32(full + slot), phase, abort);
+    const int t = ok ? ids[slot] : -1;
+    if (ok) mbar_arrive(smem_u32(empty + slot));
+    next();
+    return t;
+  }
+};
+
 template <int D, int BK, int NH>
 __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ FmhaParams p) {
@@ -129,8 +158,11 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
   uint64_t* o_full = bars + 6;            // [2]
   uint64_t* kv_full = bars + 8;           // [kStages]
   uint64_t* kv_empty = bars + 8 + C::kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * C::kStages);
+  uint64_t* tile_full = bars + 8 + 2 * C::kStages;    // [2] tile-id ring
+  uint64_t* tile_empty = bars + 10 + 2 * C::kStages;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12 + 2 * C::kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* tile_ids = reinterpret_cast<volatile int*>(tmem_slot + 2);   // [2]
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -146,6 +178,10 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(smem_u32(kv_full + i), 1);
       mbar_init(smem_u32(kv_empty + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(tile_full + i), 1);
+      mbar_init(smem_u32(tile_empty + i), 1 + 128 * NH);   // MMA thread + softmax threads
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -172,8 +208,26 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
     uint32_t qi = 0;
     const uint32_t q_base = smem_u32(q_smem);
     const uint32_t kv_base = smem_u32(kv_smem);
+    const uint64_t q_policy = l2_policy_evict_first();   // Q is read once
     bool ok = true;
-    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+    TileRing tr;
+    while (ok) {
+      // Dynamic scheduling: take the next tile and publish its id to the
+      // MMA and softmax roles through the two-slot tile ring.
+      int t = -1;
+      if (lane == 0) {
+        t = atomicAdd(p.counter, 1);
+        if (t >= p.n_tiles) t = -1;
+        ok = mbar_wait(smem_u32(tile_empty + tr.slot), tr.phase ^ 1u, abort_flag);
+        if (ok) {
+          tile_ids[tr.slot] = t;
+          mbar_arrive(smem_u32(tile_full + tr.slot));
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      tr.next();
+      if (!ok || t < 0) break;
       const TileInfo ti = decode_tile(p, t, BK);
       if (ti.n == 0) continue;
       if (lane == 0) {
@@ -182,8 +236,8 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
           mbar_arrive_expect_tx(smem_u32(q_full), C::kQBytes);
           for (int hh = 0; hh < NH; ++hh)
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(q_base + (hh * C::kChunks + c) * 16384, &p.tq[ti.bl], smem_u32(q_full),
-                          c * 64, ti.qb * p.block_q + hh * 128, ti.h);
+              tma_load_3d_hint(q_base + (hh * C::kChunks + c) * 16384, &p.tq[ti.bl], smem_u32(q_full),
+                               c * 64, ti.qb * p.block_q + hh * 128, ti.h, q_policy);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -243,7 +297,10 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
           mma_ts(d_t, a_t, b, idesc_o, (acc || kk > 0) ? 1u : 0u);
         }
       };
-      for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+      TileRing tr;
+      while (ok) {
+        const int t = tr.take(tile_full, tile_empty, tile_ids, abort_flag, ok);
+        if (t < 0) break;
         const TileInfo ti = decode_tile(p, t, BK);
         const int n = ti.n;
         if (n == 0) continue;
@@ -311,7 +368,10 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
     const uint32_t o_t = tmem + lane_base + C::kOCol + hh * 128;
     uint32_t sph = 0, oph = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+    TileRing tr;
+    while (ok) {
+      const int t = tr.take(tile_full, tile_empty, tile_ids, abort_flag, ok);
+      if (t < 0) break;
       const TileInfo ti = decode_tile(p, t, BK);
       const int row_in_blk = hh * 128 + r;
       const int row = ti.qb * p.block_q + row_in_blk;
@@ -337,48 +397,39 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
         ++sph;
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[BK];
+        float s[BK];
 #pragma unroll
-        for (int c = 0; c < BK / 32; ++c)
-          tmem_ld32(s_t + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        for (int c = 0; c < BK / 32; ++c) tmem_ld32f(s_t + c * 32, s + c * 32);
         tmem_wait_ld();
-        float* s = reinterpret_cast<float*>(sr);
         const int kvalid = ti.valid_kv - kb * BK;
         if (kvalid < BK) {
 #pragma unroll
           for (int c = 0; c < BK; ++c)
             if (c >= kvalid) s[c] = -INFINITY;
         }
-        float mx = s[0];
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-        for (int c = 1; c < BK; ++c) mx = fmaxf(mx, s[c]);
+        for (int c = 4; c < BK; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         const float m_new = fmaxf(m_ref, mx * p.scale_log2);
         const bool grow = m_new > m_ref + 8.0f;
         const bool rescale_o = grow && m_ref != -INFINITY;
-        if (__any_sync(0xffffffffu, rescale_o)) {
-          const float alpha = rescale_o ? ex2_approx(m_ref - m_new) : 1.f;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t orr[32];
-            tmem_ld32(o_t + c * 32, orr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tmem_st32(o_t + c * 32, orr);
-          }
-          tmem_wait_st();
-          if (rescale_o) l *= alpha;
-        }
+        const float alpha = rescale_o ? ex2_approx(m_ref - m_new) : 1.f;
         if (grow) m_ref = m_new;
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        float lsum = 0.f;
+        float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < BK; ++c) {
-          const float e = ex2_approx(fmaf(s[c], p.scale_log2, -m_use));
-          s[c] = e;
-          lsum += e;
+        for (int c = 0; c < BK; c += 2) {
+          s[c] = ex2_approx(fmaf(s[c], p.scale_log2, -m_use));
+          s[c + 1] = ex2_approx(fmaf(s[c + 1], p.scale_log2, -m_use));
+          ls0 += s[c];
+          ls1 += s[c + 1];
         }
-        l += lsum;
         // P (bf16 pairs) over the first BK/2 columns of S_h.
 #pragma unroll
         for (int c = 0; c < BK / 64; ++c) {
@@ -386,6 +437,19 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[c * 64 + 2 * i], s[c * 64 + 2 * i + 1]);
           tmem_st32(s_t + c * 32, pk);
+        }
+        l = l * alpha + (ls0 + ls1);
+        // Lazy rescale of O (rare): after P is out of registers, before PV is issued.
+        if (__any_sync(0xffffffffu, rescale_o)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32f(o_t + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32f(o_t + c * 32, o);
+          }
         }
         tmem_wait_st();
         tc_fence_before();
@@ -399,16 +463,14 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t orr[32];
-        tmem_ld32(o_t + c * 32, orr);
+        float o[32];
+        tmem_ld32f(o_t + c * 32, o);
         tmem_wait_ld();
         if (row_exists) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            pk[i] = row_ok ? pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
-                                         __uint_as_float(orr[2 * i + 1]) * inv_l)
-                           : 0u;
+            pk[i] = row_ok ? pack_bf16x2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l) : 0u;
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -425,6 +487,55 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+}
+
+// ---------------------------------------------------------- scheduling ---
+// One CTA: total selected work of every (request, KV head) group (query rows
+// x listed blocks, summed over the group's query heads and query blocks),
+// groups ranked heaviest first (ties: lower group first), and the tile
+// counter reset for the forward launch that follows on the same stream.
+struct ScheduleParams {
+  const int32_t* counts;   // NULL = dense pass
+  int b0, Bn, Hq, Hkv, G, nQb, nKb, block_q, block_k, prefix_len;
+  int seq_lens[kMaxFwdBatch];
+  int* counter;
+  int* order;
+};
+
+constexpr int kMaxGroups = kMaxFwdBatch * kMaxHeads;
+
+__global__ void __launch_bounds__(1024) schedule_kernel(const __grid_constant__ ScheduleParams p) {
+  __shared__ long long cost[kMaxGroups];
+  const int ng = p.Bn * p.Hkv;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int gi = warp; gi < ng; gi += blockDim.x / 32) {
+    const int bl = gi / p.Hkv, hk = gi % p.Hkv;
+    const int b = p.b0 + bl;
+    const int L = p.seq_lens[bl];
+    const int nkv = (p.prefix_len + L + p.block_k - 1) / p.block_k;
+    long long c = 0;
+    for (int w = lane; w < p.G * p.nQb; w += 32) {
+      const int g = w % p.G, qb = w / p.G;
+      const int rows = min(p.block_q, L - qb * p.block_q);
+      if (rows <= 0) continue;
+      int n = nkv;
+      if (p.counts) {
+        n = p.counts[((int64_t)b * p.Hq + hk * p.G + g) * p.nQb + qb];
+        n = n < 0 ? 0 : min(n, p.nKb);
+      }
+      c += (long long)rows * n;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (lane == 0) cost[gi] = c;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < ng; i += blockDim.x) {
+    int rank = 0;
+    for (int j = 0; j < ng; ++j) rank += (cost[j] > cost[i]) || (cost[j] == cost[i] && j < i);
+    p.order[rank] = i;
+  }
+  if (threadIdx.x == 0) *p.counter = 0;
 }
 
 // ------------------------------------------------------------- host side ---
@@ -504,6 +615,7 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
     p.b0 = b0;
     p.Bn = Bn;
     p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
     p.G = a.Hq / a.Hkv;
     p.Sq = a.Sq;
     p.nQb = a.nQb;
@@ -513,11 +625,23 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
     p.n_tiles = Bn * a.nQb * a.Hq;
     p.indices = a.indices;
     p.counts = a.counts;
+    char* cws = static_cast<char*>(a.workspace) + (size_t)(b0 / kMaxFwdBatch) * forward_chunk_bytes(a.Hq);
+    p.counter = reinterpret_cast<int*>(cws);
+    p.group_order = reinterpret_cast<const int*>(cws + 256);
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.lse = a.lse;
     const int grid = std::min(p.n_tiles, sms);
     if (grid <= 0) continue;
+    ScheduleParams sp{};
+    sp.counts = a.indices ? a.counts : nullptr;
+    sp.b0 = b0; sp.Bn = Bn; sp.Hq = a.Hq; sp.Hkv = a.Hkv; sp.G = a.Hq / a.Hkv;
+    sp.nQb = a.nQb; sp.nKb = a.nKb; sp.block_q = a.block_q; sp.block_k = BK; sp.prefix_len = a.prefix_len;
+    for (int i = 0; i < Bn; ++i) sp.seq_lens[i] = p.seq_lens[i];
+    sp.counter = p.counter;
+    sp.order = const_cast<int*>(p.group_order);
+    schedule_kernel<<<1, 1024, 0, stream>>>(sp);
+    if ((st = cuda_check(cudaGetLastError(), "schedule_kernel launch")) != BSA_OK) return st;
     fmha_fwd_kernel<D, BK, NH><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
     if ((st = cuda_check(cudaGetLastError(), "fmha_fwd_kernel launch")) != BSA_OK) return st;
   }
@@ -525,6 +649,10 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+size_t forward_chunk_bytes(int Hq) {
+  return 256 + (((size_t)4 * kMaxFwdBatch * Hq + 255) & ~(size_t)255);
+}
 
 unsigned int read_and_clear_device_error() {
   unsigned int v = 0, zero = 0;

@@ -55,7 +55,10 @@ struct ForwardArgs {
   float scale;
   void* out;
   float* lse;
+  void* workspace;           // forward_chunk_bytes(Hq) per chunk of kMaxFwdBatch requests
 };
+// Workspace bytes per launch chunk: tile counter (256 B) + group order.
+size_t forward_chunk_bytes(int Hq);
 bsa_status launch_forward(const ForwardArgs& a, cudaStream_t stream);
 
 // Device error word of the current device (0xFFFFFFFF if it cannot be read);

@@ -119,7 +119,8 @@ BSA_API bsa_status bsa_select(const bsa_tensor* q, const bsa_tensor* k, int32_t 
                       void* workspace, size_t ws_bytes, bsa_stream_t stream);
 
 /* --------------------------------------------------------------- forward ---
- * Workspace bytes bsa_forward needs (the work-tile order list). */
+ * Workspace bytes bsa_forward needs: per launch chunk of up to 8 requests, a
+ * work-tile counter and the order of the (request, KV head) groups. */
 BSA_API size_t bsa_forward_workspace_size(int B, int Hq, int Sq, int block_q);
 
 /* Selected-block attention forward (PR 8335, Purpose: the adapter executes

@@ -169,6 +169,17 @@ def test_forward_rejects_bad_arguments(lib, case, status, needle):
     assert needle in err(lib), err(lib)
 
 
+def test_forward_workspace_required(lib):
+    q, k, v = T(H=4), T(H=2, S=768), T(H=2, S=768)
+    need = lib.bsa_forward_workspace_size(1, 4, 512, 256)
+    assert need == 256 + 256      # tile counter + group order (8 requests x 4 heads x 4 B, rounded)
+    assert lib.bsa_forward_workspace_size(9, 4, 512, 256) == 2 * need   # two launch chunks of 8
+    st = call_forward(lib, q, k, v, prefix=256)
+    assert st == 3 and "workspace is NULL" in err(lib)
+    st = call_forward(lib, q, k, v, prefix=256, ws=FAKE, ws_bytes=need - 1)
+    assert st == 3 and "smaller than" in err(lib)
+
+
 def test_forward_counts_required_with_indices(lib):
     q, k, v = T(H=4), T(H=2, S=768), T(H=2, S=768)
     st = lib.bsa_forward(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), FAKE, None, 256, None, 256, 128,
