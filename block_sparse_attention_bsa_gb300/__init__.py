@@ -14,6 +14,7 @@ from .api import (  # noqa: F401
     bsa_forward_workspace_size,
     bsa_get_last_error,
     bsa_select,
+    bsa_select_noalloc,
     bsa_select_workspace_size,
     bsa_validate_indices,
     bsa_version,

@@ -124,6 +124,30 @@ def bsa_select(q: torch.Tensor, k: torch.Tensor, prefix_len: int, seq_lens: Opti
     return indices, counts
 
 
+def bsa_select_noalloc(q: torch.Tensor, k: torch.Tensor, prefix_len: int, seq_lens: Optional[Sequence[int]],
+                       block_q: int, block_k: int, keep_ratio, *, indices: Optional[torch.Tensor] = None,
+                       counts: Optional[torch.Tensor] = None, stream=None):
+    """bsa_select without caller workspace: the block means go to the
+    library's static device scratch (for callers that cannot allocate device
+    memory).  Same results; calls that overlap on the GPU race on the scratch."""
+    qd, kd = _desc(q, "q"), _desc(k, "k")
+    B, Sq, Hq, d = q.shape
+    nQb, nKb = _cdiv(Sq, block_q), _cdiv(k.shape[1], block_k)
+    if isinstance(keep_ratio, (int, float)):
+        keep_ratio = [float(keep_ratio)]
+    keep = (ctypes.c_float * len(keep_ratio))(*[float(x) for x in keep_ratio])
+    if indices is None:
+        indices = torch.full((B, Hq, nQb, nKb), -1, dtype=torch.int32, device=q.device)
+    if counts is None:
+        counts = torch.empty((B, Hq, nQb), dtype=torch.int32, device=q.device)
+    st = _lib.load().bsa_select_noalloc(ctypes.byref(qd), ctypes.byref(kd), int(prefix_len),
+                                        _i32_array(seq_lens), int(block_q), int(block_k), keep,
+                                        len(keep_ratio), indices.data_ptr(), counts.data_ptr(),
+                                        _stream_ptr(stream))
+    _check(st)
+    return indices, counts
+
+
 def bsa_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, indices: Optional[torch.Tensor],
                 counts: Optional[torch.Tensor], prefix_len: int, seq_lens: Optional[Sequence[int]],
                 block_q: int, block_k: int, softmax_scale: float = 0.0, *,

@@ -12,6 +12,7 @@
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "bsa_internal.h"
 
@@ -276,3 +277,62 @@ bsa_status launch_select(const SelectArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace bsa
+
+// ------------------------------------------------------------------------
+// bsa_select_noalloc: the selector with its block means in a static device
+// array instead of caller workspace, for callers that cannot allocate device
+// memory.  The array is the only scratch the selector needs; its size is the
+// stated maximum and every device that loads the library keeps it for the
+// life of the process.
+namespace bsa {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[BSA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the host-side symbol is only a stand-in, never a device address).
+bsa_status noalloc_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  bsa_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != BSA_OK) return st;
+  if (dev < 0 || dev >= 64)
+    return set_error(BSA_ERR_UNSUPPORTED, "bsa_select_noalloc: device ordinal " + std::to_string(dev) +
+                                              " above the 64 devices it tracks");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    st = cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)");
+    if (st != BSA_OK) return st;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return BSA_OK;
+}
+
+}  // namespace
+}  // namespace bsa
+
+extern "C" bsa_status bsa_select_noalloc(const bsa_tensor* q, const bsa_tensor* k, int32_t prefix_len,
+                                         const int32_t* seq_lens, int32_t block_q, int32_t block_k,
+                                         const float* keep_ratio, int32_t n_keep, int32_t* indices,
+                                         int32_t* counts, bsa_stream_t stream) {
+  using namespace bsa;
+  clear_error();
+  if (q && k && q->B > 0 && q->H > 0 && k->H > 0 && q->S > 0 && k->S > 0 && q->D > 0 && block_q > 0 &&
+      block_k > 0) {
+    const size_t need = select_workspace_bytes((int)q->B, (int)q->H, (int)k->H, (int)q->S, (int)k->S,
+                                               (int)q->D, block_q, block_k);
+    if (need > BSA_NOALLOC_SCRATCH_BYTES)
+      return set_error(BSA_ERR_UNSUPPORTED,
+                       "bsa_select_noalloc: the block means need " + std::to_string(need) +
+                           " bytes, above the static scratch of " +
+                           std::to_string((size_t)BSA_NOALLOC_SCRATCH_BYTES) + " bytes; use bsa_select");
+  }
+  void* scratch = nullptr;
+  const bsa_status st = noalloc_scratch_address(&scratch);
+  if (st != BSA_OK) return st;
+  return bsa_select(q, k, prefix_len, seq_lens, block_q, block_k, keep_ratio, n_keep, indices, counts,
+                    scratch, BSA_NOALLOC_SCRATCH_BYTES, stream);
+}

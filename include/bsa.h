@@ -118,6 +118,34 @@ BSA_API bsa_status bsa_select(const bsa_tensor* q, const bsa_tensor* k, int32_t 
                       int32_t* indices, int32_t* counts,
                       void* workspace, size_t ws_bytes, bsa_stream_t stream);
 
+/* ------------------------------------------------- select, no allocation ---
+ * bsa_select for callers that cannot provide device scratch memory: for
+ * example a plugin inside a serving runtime that owns every device
+ * allocation and hands the plugin only its input and output buffers, or a
+ * deployment whose device memory budget is fixed up front.  The pages have
+ * no counterpart; this is a library convenience.
+ *
+ * Same contract and results as bsa_select, except that the block means live
+ * in a buffer of BSA_NOALLOC_SCRATCH_BYTES that the library declares as a
+ * static device array: every GPU that loads libbsa holds that much memory
+ * until the process exits.  Nothing is allocated by this call (no
+ * cudaMalloc, no allocating library routine).
+ *  - A problem whose block means need more than BSA_NOALLOC_SCRATCH_BYTES
+ *    (see bsa_select_workspace_size) returns BSA_ERR_UNSUPPORTED naming the
+ *    size and the limit.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before capturing any stream on the device.
+ *  - All calls share the one array and it keeps the last call's contents
+ *    (every value a call reads is written by that call first).  Calls whose
+ *    kernels overlap on the GPU -- on different streams, or from different
+ *    host threads -- race on it; serialise them. */
+#define BSA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+BSA_API bsa_status bsa_select_noalloc(const bsa_tensor* q, const bsa_tensor* k, int32_t prefix_len,
+                                      const int32_t* seq_lens, int32_t block_q, int32_t block_k,
+                                      const float* keep_ratio, int32_t n_keep,
+                                      int32_t* indices, int32_t* counts, bsa_stream_t stream);
+
 /* --------------------------------------------------------------- forward ---
  * Workspace bytes bsa_forward needs: per launch chunk of up to 8 requests, a
  * work-tile counter and the order of the (request, KV head) groups. */

@@ -31,6 +31,7 @@ def test_header_declares_the_expected_calls():
     assert declared_symbols() == sorted([
         "bsa_version", "bsa_get_last_error", "bsa_select_workspace_size", "bsa_select",
         "bsa_forward_workspace_size", "bsa_forward", "bsa_validate_indices", "bsa_device_status",
+        "bsa_select_noalloc",
     ])
 
 
