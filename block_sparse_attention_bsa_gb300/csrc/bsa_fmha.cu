@@ -36,6 +36,16 @@
 #include "bsa_internal.h"
 #include "bsa_ptx.cuh"
 
+#ifndef BSA_SOFTMAX_PACKED
+#define BSA_SOFTMAX_PACKED 1     // packed FFMA2/FADD2 in the softmax
+#endif
+#ifndef BSA_SOFTMAX_MAX3
+#define BSA_SOFTMAX_MAX3 1       // three-input max for the row max
+#endif
+#ifndef BSA_REG_CONTROL
+#define BSA_REG_CONTROL 0        // registers of the control warpgroup (0: no split; measured faster)
+#endif
+
 namespace bsa {
 
 namespace {
@@ -71,6 +81,14 @@ struct Cfg {
   static constexpr int kSmemBytes = kQBytes + kStages * kTileBytes + kBarBytes + kAlignSlack;
   static constexpr int kThreads = 128 + 128 * NH;
   static constexpr uint32_t kTmemCols = NH == 2 ? 512 : 256;
+  // Register split for NH == 2 (launched with 168 per thread x 384 threads
+  // = 64,512): control warpgroup 56, each softmax warpgroup 224
+  // (56*128 + 224*256 = 64,512).
+  static constexpr uint32_t kRegsLaunch = 168;
+  static constexpr uint32_t kRegsControl = BSA_REG_CONTROL;
+  static constexpr uint32_t kRegsSoftmax = ((kRegsLaunch * kThreads - BSA_REG_CONTROL * 128) / 256) / 8 * 8;
+  static_assert(NH != 2 || kRegsControl * 128 + kRegsSoftmax * 256 <= kRegsLaunch * kThreads,
+                "register split exceeds the launch budget");
   static constexpr uint32_t kOCol = NH * 128;             // O_h at kOCol + 128 h
   static_assert(kStages >= 2, "not enough shared memory for a K/V ring");
   static_assert(D == 64 || D == 128, "head dim");
@@ -202,6 +220,8 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < 4) {
+  if constexpr (NH == 2 && BSA_REG_CONTROL > 0) regs_dec<C::kRegsControl>();
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer ---
     Ring ring;
@@ -277,25 +297,38 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       uint32_t qi = 0;
       uint32_t pph[2] = {0u, 0u};
       bool ok = true;
+      // Shared-memory descriptors are computed once: a descriptor's start
+      // address field is (address >> 4) in its low 14 bits, so moving the
+      // operand by `off` bytes is a plain add of off >> 4 (shared addresses
+      // stay below 2^18, so the field never carries).  Each MMA then costs one
+      // 64-bit add; the issuing thread shares its SM sub-partition with two
+      // busy softmax warps, and its issue rate bounds the tensor pipe.
+      uint64_t qdesc[NH];
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) qdesc[hh] = sdesc_sw128(q_base + hh * C::kChunks * 16384, 16, 1024);
+      const uint64_t kdesc0 = sdesc_sw128(kv_base, 16, 1024);
+      const uint64_t vdesc0 = sdesc_sw128(kv_base, BK * 128, 1024);
       auto issue_s = [&](int hh, uint32_t stage) {
         const uint32_t d_t = tmem + hh * 128;
+        const uint64_t bs = kdesc0 + (uint64_t)(stage * (uint32_t)(C::kTileBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const int c = kk / 4;
-          const uint32_t off = (kk % 4) * 32;
-          const uint64_t a = sdesc_sw128(q_base + (hh * C::kChunks + c) * 16384 + off, 16, 1024);
-          const uint64_t b = sdesc_sw128(kv_base + stage * C::kTileBytes + c * (BK * 128) + off, 16, 1024);
-          mma_ss(d_t, a, b, idesc_s, kk > 0 ? 1u : 0u);
+          constexpr int kQChunk = 16384 >> 4, kKChunk = (BK * 128) >> 4;
+          const uint64_t a = qdesc[hh] + (uint64_t)((kk / 4) * kQChunk + (kk % 4) * 2);
+          const uint64_t b = bs + (uint64_t)((kk / 4) * kKChunk + (kk % 4) * 2);
+          if (kk == 0) mma_ss_acc<0>(d_t, a, b, idesc_s);
+          else mma_ss_acc<1>(d_t, a, b, idesc_s);
         }
       };
       auto issue_pv = [&](int hh, uint32_t stage, bool acc) {
         const uint32_t d_t = tmem + C::kOCol + hh * 128;
+        const uint64_t bs = vdesc0 + (uint64_t)(stage * (uint32_t)(C::kTileBytes >> 4));
+        const uint32_t a_t = tmem + hh * 128;
+        if (acc) mma_ts_acc<1>(d_t, a_t, bs, idesc_o);
+        else mma_ts_acc<0>(d_t, a_t, bs, idesc_o);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint32_t a_t = tmem + hh * 128 + kk * 8;
-          const uint64_t b = sdesc_sw128(kv_base + stage * C::kTileBytes + kk * 16 * 128, BK * 128, 1024);
-          mma_ts(d_t, a_t, b, idesc_o, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < BK / 16; ++kk)
+          mma_ts_acc<1>(d_t, a_t + kk * 8, bs + (uint64_t)(kk * ((16 * 128) >> 4)), idesc_o);
       };
       TileRing tr;
       while (ok) {
@@ -358,7 +391,9 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  }
+  } else {
+    if constexpr (NH == 2 && BSA_REG_CONTROL > 0) regs_inc<C::kRegsSoftmax>();
     // --------------------------------------------------- softmax + epilogue ---
     const int hh = (warp - 4) / 4;
     const int wq = warp % 4;
@@ -407,13 +442,21 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
           for (int c = 0; c < BK; ++c)
             if (c >= kvalid) s[c] = -INFINITY;
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // Row max: four independent chains of three-input max.
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int c = 4; c < BK; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int c = 0; c < BK; c += 8) {
+#if BSA_SOFTMAX_MAX3
+          mx0 = max3f(mx0, s[c], s[c + 1]);
+          mx1 = max3f(mx1, s[c + 2], s[c + 3]);
+          mx2 = max3f(mx2, s[c + 4], s[c + 5]);
+          mx3 = max3f(mx3, s[c + 6], s[c + 7]);
+#else
+          mx0 = fmaxf(fmaxf(mx0, s[c]), s[c + 1]);
+          mx1 = fmaxf(fmaxf(mx1, s[c + 2]), s[c + 3]);
+          mx2 = fmaxf(fmaxf(mx2, s[c + 4]), s[c + 5]);
+          mx3 = fmaxf(fmaxf(mx3, s[c + 6]), s[c + 7]);
+#endif
         }
         const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         const float m_new = fmaxf(m_ref, mx * p.scale_log2);
@@ -422,14 +465,35 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
         const float alpha = rescale_o ? ex2_approx(m_ref - m_new) : 1.f;
         if (grow) m_ref = m_new;
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        float ls0 = 0.f, ls1 = 0.f;
+        // p = 2^(s * scale * log2 e - m): packed FFMA2 for the argument, MUFU
+        // ex2 per element, packed FADD2 row sums in two chains.
+#if BSA_SOFTMAX_PACKED
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nm2 = make_float2(-m_use, -m_use);
+        float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < BK; c += 4) {
+          const float2 a = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
+          const float2 b = __ffma2_rn(make_float2(s[c + 2], s[c + 3]), sc2, nm2);
+          s[c] = ex2_approx(a.x);
+          s[c + 1] = ex2_approx(a.y);
+          s[c + 2] = ex2_approx(b.x);
+          s[c + 3] = ex2_approx(b.y);
+          ls0 = __fadd2_rn(ls0, make_float2(s[c], s[c + 1]));
+          ls1 = __fadd2_rn(ls1, make_float2(s[c + 2], s[c + 3]));
+        }
+        const float lsum = (ls0.x + ls0.y) + (ls1.x + ls1.y);
+#else
+        float l0 = 0.f, l1 = 0.f;
 #pragma unroll
         for (int c = 0; c < BK; c += 2) {
           s[c] = ex2_approx(fmaf(s[c], p.scale_log2, -m_use));
           s[c + 1] = ex2_approx(fmaf(s[c + 1], p.scale_log2, -m_use));
-          ls0 += s[c];
-          ls1 += s[c + 1];
+          l0 += s[c];
+          l1 += s[c + 1];
         }
+        const float lsum = l0 + l1;
+#endif
         // P (bf16 pairs) over the first BK/2 columns of S_h.
 #pragma unroll
         for (int c = 0; c < BK / 64; ++c) {
@@ -438,7 +502,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
           for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[c * 64 + 2 * i], s[c * 64 + 2 * i + 1]);
           tmem_st32(s_t + c * 32, pk);
         }
-        l = l * alpha + (ls0 + ls1);
+        l = l * alpha + lsum;
         // Lazy rescale of O (rare): after P is out of registers, before PV is issued.
         if (__any_sync(0xffffffffu, rescale_o)) {
 #pragma unroll 1
