@@ -58,6 +58,49 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one forward
+# launch, from an ncu capture of the build whose FMHA sources hash to `sha`.
+# When the sources change the figure no longer applies and traffic is null.
+FMHA_TRAFFIC = {
+    "sha": "5f4490e7be6b60a2",
+    "480p_75": 505897728 + 268969472,     # profiles/fmha_fwd_480p_75.md
+}
+
+
+def fmha_source_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_sparse_attention_bsa_gb300", "csrc")
+    for f in ("bsa_fmha.cu", "bsa_ptx.cuh", "bsa_internal.h"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def algorithmic_bytes(cfg, counts) -> float:
+    """Bytes the forward must move at least once: Q, K, V, O, LSE, index lists."""
+    B, Sq, Skv = cfg.B, cfg.Sq, cfg.Skv
+    return (2.0 * B * Sq * cfg.Hq * cfg.d * 2          # Q read + O written
+            + 2.0 * B * Skv * cfg.Hkv * cfg.d * 2      # K + V
+            + 4.0 * B * cfg.Hq * Sq                    # LSE
+            + 4.0 * float(counts.sum()))               # index lists
+
+
+def fmha_traffic(cfg, counts):
+    """(bytes per launch, how obtained) or (None, reason)."""
+    if fmha_source_sha() != FMHA_TRAFFIC["sha"]:
+        return None, "forward kernel changed since the last ncu capture"
+    if cfg.name in FMHA_TRAFFIC:
+        return float(FMHA_TRAFFIC[cfg.name]), f"ncu capture of {cfg.name}"
+    from bsa_inputs import CONFIGS
+    ref = CONFIGS["480p_75"]
+    import numpy as np
+    # scale the 480p capture by algorithmic bytes (traffic tracks Q/K/V/O sizes)
+    ref_counts = np.full(1, 4536 * 99)
+    ratio = FMHA_TRAFFIC["480p_75"] / algorithmic_bytes(ref, ref_counts)
+    return ratio * algorithmic_bytes(cfg, counts), (
+        f"480p_75 ncu capture scaled by algorithmic bytes (traffic/algorithmic = {ratio:.3f} there)")
+
+
 def tile_flops(counts, d, bq, bk) -> float:
     """4*d*block_q*block_k per selected (work tile, key block) pair."""
     return 4.0 * d * bq * bk * float(counts.sum())
@@ -79,6 +122,24 @@ def valid_pair_flops(counts_np, indices_np, seq_lens, prefix, d, bq, bk) -> floa
                 keys = (idx.size * bk) - int(max(0, (idx[-1] + 1) * bk - (prefix + L))) if c else 0
                 tot += rows * keys
     return 4.0 * d * tot
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank scalar over the process group (identity without one).
+    Timing only: nothing on the data path is exchanged between ranks."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Replicas: every rank runs the full step, so the job does world x the work
+    in the slowest rank's time."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
 
 
 class ClockSampler:
@@ -331,13 +392,11 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     sel_ms = [e[0].elapsed_time(e[1]) for e in evs]
     fwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_ms = max_over_ranks(total_ms, device="cuda")
     if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
         dist.barrier()
     ms_step = total_ms / args.steps
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops, world, ms_step)
     pk = peaks()
     fwd_mean = sum(fwd_ms) / len(fwd_ms)
     fwd_tflops = flops / (fwd_mean * 1e-3) / 1e12
@@ -345,6 +404,7 @@ def main():
     exact_flops = valid_pair_flops(cnt_np, idx_np, lens, P, d, bq, bk)
     dense_tiles = sum(-(-(P + L) // bk) * -(-L // bq) for L in lens) * Hq
     tile_sparsity = 1.0 - float(cnt_np.sum()) / dense_tiles
+    traffic, traffic_src = fmha_traffic(cfg, cnt_np)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -371,14 +431,10 @@ def main():
             e2e_step()
         b_.record(stream)
         torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b_) / n_e2e
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(a.elapsed_time(b_) / n_e2e, device="cuda")
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk_, hv))
         d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
-        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+        e2e = {"value": whole_job_tflops(flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
@@ -402,7 +458,10 @@ def main():
             "effective_tflop_per_step": flops / 1e12,
             "roofline": {"bound": "tensor", "kernel": "fmha_fwd_kernel<128,128,2>", "achieved": fwd_tflops,
                          "peak": pk["bf16"], "unit": "TFLOP/s", "frac": fwd_tflops / pk["bf16"],
-                         "peak_source": f"{pk['source']} bf16 burst", "traffic": None},
+                         "peak_source": f"{pk['source']} bf16 burst (of measured)",
+                         "traffic": traffic, "traffic_source": traffic_src,
+                         "algorithmic_bytes": algorithmic_bytes(cfg, cnt_np),
+                         "algorithmic_flops": flops},
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,
