@@ -42,6 +42,9 @@
 #ifndef BSA_SOFTMAX_MAX3
 #define BSA_SOFTMAX_MAX3 1       // three-input max for the row max
 #endif
+#ifndef BSA_KV_PAIR
+#define BSA_KV_PAIR 1            // K and V of one key block share one ring stage (measured +2.5%)
+#endif
 #ifndef BSA_REG_CONTROL
 #define BSA_REG_CONTROL 0        // registers of the control warpgroup (0: no split; measured faster)
 #endif
@@ -76,9 +79,10 @@ struct Cfg {
   static constexpr int kBarBytes = 256;
   static constexpr int kAlignSlack = 1024;
   static constexpr int kSmemMax = 232448;                 // 227 KB per CTA
-  static constexpr int kStagesFit = (kSmemMax - kQBytes - kBarBytes - kAlignSlack) / kTileBytes;
+  static constexpr int kStageBytes = (BSA_KV_PAIR ? 2 : 1) * kTileBytes;   // one ring stage
+  static constexpr int kStagesFit = (kSmemMax - kQBytes - kBarBytes - kAlignSlack) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-  static constexpr int kSmemBytes = kQBytes + kStages * kTileBytes + kBarBytes + kAlignSlack;
+  static constexpr int kSmemBytes = kQBytes + kStages * kStageBytes + kBarBytes + kAlignSlack;
   static constexpr int kThreads = 128 + 128 * NH;
   static constexpr uint32_t kTmemCols = NH == 2 ? 512 : 256;
   // Register split for NH == 2 (launched with 168 per thread x 384 threads
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* q_smem = smem;
   uint8_t* kv_smem = smem + C::kQBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(kv_smem + C::kStages * C::kTileBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(kv_smem + C::kStages * C::kStageBytes);
   // barrier slots
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
@@ -269,6 +273,21 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
           int kb = __shfl_sync(0xffffffffu, my_kb, jj);
           if (kb < 0 || kb >= p.nKb) kb = p.nKb;   // out of range: rows past the end read zeros
           if (lane == 0) {
+#if BSA_KV_PAIR
+            // K at the stage base, V right after it; one barrier for both.
+            ok = mbar_wait(smem_u32(kv_empty + ring.stage), ring.phase ^ 1u, abort_flag);
+            if (ok) {
+              const uint32_t fb = smem_u32(kv_full + ring.stage);
+              mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
+              for (int which = 0; which < 2; ++which) {
+                const CUtensorMap* tm = which == 0 ? &p.tk[ti.bl] : &p.tv[ti.bl];
+                for (int c = 0; c < C::kChunks; ++c)
+                  tma_load_3d(kv_base + ring.stage * C::kStageBytes + which * C::kTileBytes + c * (BK * 128),
+                              tm, fb, c * 64, kb * BK, ti.hk);
+              }
+              ring.next<C::kStages>();
+            }
+#else
             for (int which = 0; which < 2 && ok; ++which) {
               ok = mbar_wait(smem_u32(kv_empty + ring.stage), ring.phase ^ 1u, abort_flag);
               if (!ok) break;
@@ -280,6 +299,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
                             kb * BK, ti.hk);
               ring.next<C::kStages>();
             }
+#endif
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
@@ -308,9 +328,10 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       for (int hh = 0; hh < NH; ++hh) qdesc[hh] = sdesc_sw128(q_base + hh * C::kChunks * 16384, 16, 1024);
       const uint64_t kdesc0 = sdesc_sw128(kv_base, 16, 1024);
       const uint64_t vdesc0 = sdesc_sw128(kv_base, BK * 128, 1024);
-      auto issue_s = [&](int hh, uint32_t stage) {
+      // issue_s / issue_pv take the byte offset of the K or V tile in the ring.
+      auto issue_s = [&](int hh, uint32_t tile_off) {
         const uint32_t d_t = tmem + hh * 128;
-        const uint64_t bs = kdesc0 + (uint64_t)(stage * (uint32_t)(C::kTileBytes >> 4));
+        const uint64_t bs = kdesc0 + (uint64_t)(tile_off >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           constexpr int kQChunk = 16384 >> 4, kKChunk = (BK * 128) >> 4;
@@ -320,9 +341,9 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
           else mma_ss_acc<1>(d_t, a, b, idesc_s);
         }
       };
-      auto issue_pv = [&](int hh, uint32_t stage, bool acc) {
+      auto issue_pv = [&](int hh, uint32_t tile_off, bool acc) {
         const uint32_t d_t = tmem + C::kOCol + hh * 128;
-        const uint64_t bs = vdesc0 + (uint64_t)(stage * (uint32_t)(C::kTileBytes >> 4));
+        const uint64_t bs = vdesc0 + (uint64_t)(tile_off >> 4);
         const uint32_t a_t = tmem + hh * 128;
         if (acc) mma_ts_acc<1>(d_t, a_t, bs, idesc_o);
         else mma_ts_acc<0>(d_t, a_t, bs, idesc_o);
@@ -340,6 +361,50 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
         ok = mbar_wait(smem_u32(q_full), qi & 1u, abort_flag);
         ++qi;
         if (!ok) break;
+#if BSA_KV_PAIR
+        // K_j and V_j share stage sJ (K at +0, V at +kTileBytes).
+        uint32_t sJ = ring.stage;
+        ok = mbar_wait(smem_u32(kv_full + sJ), ring.phase, abort_flag);
+        ring.next<C::kStages>();
+        if (!ok) break;
+        tc_fence_after();
+        for (int hh = 0; hh < NH; ++hh) {
+          issue_s(hh, sJ * C::kStageBytes);
+          mma_commit(smem_u32(s_full + hh));
+        }
+        if (n == 1) mma_commit(smem_u32(q_empty));
+        for (int j = 0; j < n && ok; ++j) {
+          const bool has_next = j + 1 < n;
+          uint32_t sN = 0, sN_phase = 0;
+          if (has_next) {
+            sN = ring.stage;
+            sN_phase = ring.phase;
+            ring.next<C::kStages>();
+          }
+          for (int hh = 0; hh < NH && ok; ++hh) {
+            ok = mbar_wait(smem_u32(p_full + hh), pph[hh] & 1u, abort_flag);
+            ++pph[hh];
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(hh, sJ * C::kStageBytes + C::kTileBytes, j > 0);
+            if (j == n - 1) mma_commit(smem_u32(o_full + hh));
+            if (has_next) {
+              if (hh == 0) {
+                ok = mbar_wait(smem_u32(kv_full + sN), sN_phase, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              issue_s(hh, sN * C::kStageBytes);
+              mma_commit(smem_u32(s_full + hh));
+            }
+          }
+          if (!ok) break;
+          // both halves are done with stage sJ once PV_1(j) completes
+          mma_commit(smem_u32(kv_empty + sJ));
+          if (has_next && j + 2 == n) mma_commit(smem_u32(q_empty));
+          sJ = sN;
+        }
+#else
         // S_h(0) for every half
         uint32_t sK = ring.stage;
         ok = mbar_wait(smem_u32(kv_full + sK), ring.phase, abort_flag);
@@ -347,7 +412,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         for (int hh = 0; hh < NH; ++hh) {
-          issue_s(hh, sK);
+          issue_s(hh, sK * C::kTileBytes);
           mma_commit(smem_u32(s_full + hh));
         }
         mma_commit(smem_u32(kv_empty + sK));
@@ -369,7 +434,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
             ++pph[hh];
             if (!ok) break;
             tc_fence_after();
-            issue_pv(hh, sV, j > 0);
+            issue_pv(hh, sV * C::kTileBytes, j > 0);
             if (j == n - 1) mma_commit(smem_u32(o_full + hh));
             if (has_next) {
               if (hh == 0) {
@@ -377,7 +442,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
               }
-              issue_s(hh, sKn);
+              issue_s(hh, sKn * C::kTileBytes);
               mma_commit(smem_u32(s_full + hh));
             }
           }
@@ -388,6 +453,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
             if (j + 2 == n) mma_commit(smem_u32(q_empty));
           }
         }
+#endif
       }
     }
     __syncwarp();
