@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--schedule", choices=["cosmos3", "h3"], default=None,
+                    help="time the dense pass and the sparse step and report a dense->sparse schedule")
     return ap.parse_args()
 
 
@@ -252,6 +254,74 @@ def cpu_baseline(inp, idx, cnt, n_tiles_sample=400, budget_s=20.0):
     }
 
 
+# Dense -> sparse schedules from the pages (attention calls per generation):
+#  * "[Core] Add Cosmos3 attention strategy PoC", Test Result: Cosmos3-Nano,
+#    35 steps x 36 generation layers; "mixed" = 10 dense steps, then 28 of
+#    36 layers sparse; "all-sparse" = every layer sparse.  End-to-end
+#    speedups there (GH200): 1.22x mixed, 1.48x all-sparse.
+#  * "[Model] Add MiniMax H3 attention strategy PoC": 50 iterations, the
+#    first 20 dense, then every DiT layer sparse (48 here: the layer count
+#    does not change the ratio).  End-to-end: 1.28x.
+SCHEDULES = {
+    "cosmos3": dict(steps=35, layers=36, arms={
+        "dense": lambda s, l: True,
+        "mixed": lambda s, l: s < 10 or l >= 28,
+        "all_sparse": lambda s, l: False}, published={"mixed": 1.22, "all_sparse": 1.48}),
+    "h3": dict(steps=50, layers=48, arms={
+        "dense": lambda s, l: True,
+        "mixed": lambda s, l: s < 20}, published={"mixed": 1.28}),
+}
+
+
+def run_schedule(args):
+    """Attention time of a whole generation under a dense->sparse schedule,
+    from the measured dense-pass and sparse-step (select + forward) times of
+    one attention call on the workload (the kernel-level analogue of the
+    pages' end-to-end latencies, which also include everything else)."""
+    import torch
+    import block_sparse_attention_bsa_gb300 as bsa
+    from bsa_inputs import CONFIGS, make_inputs
+    bsa.build()
+    cfg = CONFIGS[args.config]
+    inp = make_inputs(cfg, "cuda", pad_fill=0.0)
+    q, k, v = inp["q"], inp["k"], inp["v"]
+    P, lens, bq, bk = cfg.prefix, inp["seq_lens"], cfg.block_q, cfg.block_k
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    def sparse():
+        idx, cnt = bsa.bsa_select(q, k, P, lens, bq, bk, inp["keep_ratio"])
+        bsa.bsa_forward(q, k, v, idx, cnt, P, lens, bq, bk, return_lse=False)
+
+    t_sparse = timed(sparse, max(3, args.steps))
+    t_dense = timed(lambda: bsa.bsa_forward(q, k, v, None, None, P, lens, bq, bk, return_lse=False),
+                    max(3, args.steps))
+    bsa.bsa_device_status()
+    sch = SCHEDULES[args.schedule]
+    totals = {}
+    for arm, is_dense in sch["arms"].items():
+        n_d = sum(1 for s in range(sch["steps"]) for l in range(sch["layers"]) if is_dense(s, l))
+        n_s = sch["steps"] * sch["layers"] - n_d
+        totals[arm] = dict(dense_calls=n_d, sparse_calls=n_s, attention_s=(n_d * t_dense + n_s * t_sparse) / 1e3)
+    base = totals["dense"]["attention_s"]
+    for arm in totals:
+        totals[arm]["speedup_vs_dense"] = base / totals[arm]["attention_s"]
+    print(json.dumps({"schedule": args.schedule, "workload": args.config, "dense_call_ms": t_dense,
+                      "sparse_call_ms": t_sparse, "per_call_speedup": t_dense / t_sparse, "arms": totals,
+                      "pages_end_to_end_speedups": sch["published"]}), flush=True)
+
+
 def run_reference(args, rank, world):
     """--impl reference: the fp64 oracle on the host cores, K timed steps of a
     bounded sample each; only rank 0 works."""
@@ -332,6 +402,10 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.schedule:
+        if rank == 0:
+            run_schedule(args)
         return
 
     import torch

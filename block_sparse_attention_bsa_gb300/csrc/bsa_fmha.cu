@@ -635,29 +635,27 @@ struct ScheduleParams {
 constexpr int kMaxGroups = kMaxFwdBatch * kMaxHeads;
 
 __global__ void __launch_bounds__(1024) schedule_kernel(const __grid_constant__ ScheduleParams p) {
-  __shared__ long long cost[kMaxGroups];
+  __shared__ unsigned long long cost[kMaxGroups];
   const int ng = p.Bn * p.Hkv;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  for (int gi = warp; gi < ng; gi += blockDim.x / 32) {
-    const int bl = gi / p.Hkv, hk = gi % p.Hkv;
-    const int b = p.b0 + bl;
+  for (int i = threadIdx.x; i < ng; i += blockDim.x) cost[i] = 0ull;
+  __syncthreads();
+  // every (group, query head of the group, query block) tile; query blocks
+  // fastest so the count reads are coalesced
+  const int per_group = p.G * p.nQb;
+  const int total = ng * per_group;
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int gi = i / per_group, w = i - gi * per_group;
+    const int g = w / p.nQb, qb = w - g * p.nQb;
+    const int bl = gi / p.Hkv, hk = gi - bl * p.Hkv;
     const int L = p.seq_lens[bl];
-    const int nkv = (p.prefix_len + L + p.block_k - 1) / p.block_k;
-    long long c = 0;
-    for (int w = lane; w < p.G * p.nQb; w += 32) {
-      const int g = w % p.G, qb = w / p.G;
-      const int rows = min(p.block_q, L - qb * p.block_q);
-      if (rows <= 0) continue;
-      int n = nkv;
-      if (p.counts) {
-        n = p.counts[((int64_t)b * p.Hq + hk * p.G + g) * p.nQb + qb];
-        n = n < 0 ? 0 : min(n, p.nKb);
-      }
-      c += (long long)rows * n;
+    const int rows = min(p.block_q, L - qb * p.block_q);
+    if (rows <= 0) continue;
+    int n = (p.prefix_len + L + p.block_k - 1) / p.block_k;
+    if (p.counts) {
+      n = p.counts[((int64_t)(p.b0 + bl) * p.Hq + hk * p.G + g) * p.nQb + qb];
+      n = n < 0 ? 0 : min(n, p.nKb);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    if (lane == 0) cost[gi] = c;
+    if (n > 0) atomicAdd(&cost[gi], (unsigned long long)rows * (unsigned long long)n);
   }
   __syncthreads();
   for (int i = threadIdx.x; i < ng; i += blockDim.x) {

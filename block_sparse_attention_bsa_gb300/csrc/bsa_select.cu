@@ -88,14 +88,18 @@ __global__ void __launch_bounds__(kPoolCols* kPoolGroups)
 }
 
 // ---------------------------------------------------- score + top-k -------
-// One CTA per (batch element, query head, kRows query blocks); one warp per
-// query block (row).  Candidate block means are staged 32 at a time in
-// shared memory; each lane scores one candidate (fp32 dot product of the
-// two means).  Selection: the kh-th largest score key is found bit by bit
-// (32 counting passes), then one pass in ascending block order writes the
-// blocks above it plus the lowest-index blocks equal to it.
+// One CTA per (batch element, query head, kRows query blocks).
+// Scores: every thread takes candidate key blocks in turn and computes their
+// fp32 dot products with the kRows query-block means at once (the key-block
+// mean streams from L2 as float4s; the query means sit transposed in shared
+// memory and are read as broadcast float4s), so each key mean is read once
+// per CTA and each multiply-add needs a fraction of a shared-memory load.
+// Selection: one warp per row; the kh-th largest score key is found bit by
+// bit (32 counting passes), then one pass in ascending block order writes
+// the blocks above it plus the lowest-index blocks equal to it.
 
-constexpr int kRows = 8;
+constexpr int kRows = 16;
+constexpr int kTopkThreads = 256;
 
 struct TopkParams {
   const float* qbar;   // [B, Hq, nQb, D]
@@ -121,12 +125,12 @@ __device__ __forceinline__ int keep_count_dev(float r, int n) {
   return v >= (double)n ? n : (int)v;
 }
 
-__global__ void __launch_bounds__(kRows * 32) score_topk_kernel(const __grid_constant__ TopkParams p) {
+__global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const __grid_constant__ TopkParams p) {
   extern __shared__ float sm[];
   const int D = p.D;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int b = blockIdx.z, h = blockIdx.y;
-  const int qb = blockIdx.x * kRows + warp;
+  const int qb0 = blockIdx.x * kRows;
   const int L = p.seq_lens[b];
   const int valid_kv = p.prefix_len + L;
   const int nkv = (valid_kv + p.block_k - 1) / p.block_k;
@@ -135,93 +139,94 @@ __global__ void __launch_bounds__(kRows * 32) score_topk_kernel(const __grid_con
   const int kh = keep_count_dev(p.keep[h], N);
   const int nqv = (L + p.block_q - 1) / p.block_q;
   const int hk = h / (p.Hq / p.Hkv);
-  const bool row_on = qb < p.nQb;
-  const bool row_valid = qb < nqv;
+  const int rows_here = min(kRows, p.nQb - qb0);
+  const int rows_valid = max(0, min(kRows, nqv - qb0));
 
-  float* qs = sm;                       // [kRows][D]
-  float* ks = qs + kRows * D;           // [32][D + 1]
-  uint32_t* keys = reinterpret_cast<uint32_t*>(ks + 32 * (D + 1));   // [kRows][nKb]
-  uint32_t* my_keys = keys + (size_t)warp * p.nKb;
+  float* qT = sm;                                                    // [D][kRows]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(qT + D * kRows);      // [kRows][nKb]
 
-  const bool need_scores = row_valid && kh > 0 && kh < N;
-  // Every warp of the CTA takes part in staging, so the CTA-wide decision
-  // is whether any row needs scores.
-  const int cta_rows_valid = min(kRows, max(0, nqv - (int)blockIdx.x * kRows));
-  const bool cta_scores = cta_rows_valid > 0 && kh > 0 && kh < N;
-
-  if (cta_scores) {
-    for (int i = threadIdx.x; i < kRows * D; i += blockDim.x) {
-      const int r = i / D, e = i % D;
-      const int qbr = blockIdx.x * kRows + r;
-      qs[i] = (qbr < nqv) ? p.qbar[(((int64_t)b * p.Hq + h) * p.nQb + qbr) * D + e] : 0.f;
+  if (rows_valid > 0 && kh > 0 && kh < N) {
+    for (int i = threadIdx.x; i < D * kRows; i += blockDim.x) {
+      const int e = i / kRows, r = i % kRows;
+      qT[i] = (r < rows_valid) ? p.qbar[(((int64_t)b * p.Hq + h) * p.nQb + qb0 + r) * D + e] : 0.f;
     }
+    __syncthreads();
     const float* kb_base = p.kbar + ((int64_t)b * p.Hkv + hk) * p.nKb * D;
-    for (int kb0 = npb; kb0 < nkv; kb0 += 32) {
-      __syncthreads();
-      for (int i = threadIdx.x; i < 32 * D; i += blockDim.x) {
-        const int r = i / D, e = i % D;
-        ks[r * (D + 1) + e] = (kb0 + r < nkv) ? kb_base[(int64_t)(kb0 + r) * D + e] : 0.f;
-      }
-      __syncthreads();
-      if (need_scores && kb0 + lane < nkv) {
-        const float* qr = qs + warp * D;
-        const float* kr = ks + lane * (D + 1);
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        for (int e = 0; e < D; e += 4) {
-          s0 = fmaf(qr[e], kr[e], s0);
-          s1 = fmaf(qr[e + 1], kr[e + 1], s1);
-          s2 = fmaf(qr[e + 2], kr[e + 2], s2);
-          s3 = fmaf(qr[e + 3], kr[e + 3], s3);
+    for (int c = threadIdx.x; c < N; c += blockDim.x) {
+      const float4* krow = reinterpret_cast<const float4*>(kb_base + (int64_t)(npb + c) * D);
+      float acc[kRows];
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) acc[r] = 0.f;
+#pragma unroll 4
+      for (int e4 = 0; e4 < D / 4; ++e4) {
+        const float4 kv = __ldg(krow + e4);
+        const float ke[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float4* qr = reinterpret_cast<const float4*>(qT + (e4 * 4 + u) * kRows);
+#pragma unroll
+          for (int r4 = 0; r4 < kRows / 4; ++r4) {
+            const float4 q4 = qr[r4];
+            acc[4 * r4 + 0] = fmaf(q4.x, ke[u], acc[4 * r4 + 0]);
+            acc[4 * r4 + 1] = fmaf(q4.y, ke[u], acc[4 * r4 + 1]);
+            acc[4 * r4 + 2] = fmaf(q4.z, ke[u], acc[4 * r4 + 2]);
+            acc[4 * r4 + 3] = fmaf(q4.w, ke[u], acc[4 * r4 + 3]);
+          }
         }
-        const float s = ((s0 + s1) + (s2 + s3)) + 0.f;   // -0 -> +0
-        my_keys[kb0 + lane - npb] = order_key(s);
       }
+#pragma unroll
+      for (int r = 0; r < kRows; ++r)
+        if (r < rows_valid) keys[r * p.nKb + c] = order_key(acc[r] + 0.f);   // -0 -> +0
     }
-    __syncwarp();
+    __syncthreads();
   }
-  if (!row_on) return;
-  const int64_t row_id = ((int64_t)b * p.Hq + h) * p.nQb + qb;
-  int32_t* out_idx = p.indices + row_id * p.nKb;
-  if (!row_valid) {
-    if (lane == 0) p.counts[row_id] = 0;
-    return;
-  }
-  for (int i = lane; i < npb; i += 32) out_idx[i] = i;
-  if (lane == 0) p.counts[row_id] = npb + kh;
-  if (kh == 0) return;
-  if (kh >= N) {
-    for (int i = lane; i < N; i += 32) out_idx[npb + i] = npb + i;
-    return;
-  }
-  // Threshold T = largest key with count(key >= T) >= kh, i.e. the kh-th key.
-  uint32_t T = 0;
-  for (int bit = 31; bit >= 0; --bit) {
-    const uint32_t cand = T | (1u << bit);
-    int cnt = 0;
-    for (int i = lane; i < N; i += 32) cnt += (my_keys[i] >= cand) ? 1 : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if (cnt >= kh) T = cand;
-  }
-  int c_gt = 0;
-  for (int i = lane; i < N; i += 32) c_gt += (my_keys[i] > T) ? 1 : 0;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) c_gt += __shfl_xor_sync(0xffffffffu, c_gt, o);
-  const int need_eq = kh - c_gt;
+
   const uint32_t lt_mask = (1u << lane) - 1u;
-  int written = 0, eq_seen = 0;
-  for (int i0 = 0; i0 < N; i0 += 32) {
-    const int i = i0 + lane;
-    const uint32_t key = (i < N) ? my_keys[i] : 0u;
-    const bool gt = (i < N) && key > T;
-    const bool eq = (i < N) && key == T;
-    const uint32_t eq_ball = __ballot_sync(0xffffffffu, eq);
-    const int eq_rank = eq_seen + __popc(eq_ball & lt_mask);
-    const bool sel = gt || (eq && eq_rank < need_eq);
-    const uint32_t sel_ball = __ballot_sync(0xffffffffu, sel);
-    if (sel) out_idx[npb + written + __popc(sel_ball & lt_mask)] = npb + i;
-    written += __popc(sel_ball);
-    eq_seen += __popc(eq_ball);
+  for (int r = warp; r < rows_here; r += kTopkThreads / 32) {
+    const int qb = qb0 + r;
+    const int64_t row_id = ((int64_t)b * p.Hq + h) * p.nQb + qb;
+    int32_t* out_idx = p.indices + row_id * p.nKb;
+    if (qb >= nqv) {
+      if (lane == 0) p.counts[row_id] = 0;
+      continue;
+    }
+    for (int i = lane; i < npb; i += 32) out_idx[i] = i;
+    if (lane == 0) p.counts[row_id] = npb + kh;
+    if (kh == 0) continue;
+    if (kh >= N) {
+      for (int i = lane; i < N; i += 32) out_idx[npb + i] = npb + i;
+      continue;
+    }
+    const uint32_t* my_keys = keys + r * p.nKb;
+    // Threshold T = largest key with count(key >= T) >= kh, i.e. the kh-th key.
+    uint32_t T = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t cand = T | (1u << bit);
+      int cnt = 0;
+      for (int i = lane; i < N; i += 32) cnt += (my_keys[i] >= cand) ? 1 : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      if (cnt >= kh) T = cand;
+    }
+    int c_gt = 0;
+    for (int i = lane; i < N; i += 32) c_gt += (my_keys[i] > T) ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c_gt += __shfl_xor_sync(0xffffffffu, c_gt, o);
+    const int need_eq = kh - c_gt;
+    int written = 0, eq_seen = 0;
+    for (int i0 = 0; i0 < N; i0 += 32) {
+      const int i = i0 + lane;
+      const uint32_t key = (i < N) ? my_keys[i] : 0u;
+      const bool gt = (i < N) && key > T;
+      const bool eq = (i < N) && key == T;
+      const uint32_t eq_ball = __ballot_sync(0xffffffffu, eq);
+      const int eq_rank = eq_seen + __popc(eq_ball & lt_mask);
+      const bool sel = gt || (eq && eq_rank < need_eq);
+      const uint32_t sel_ball = __ballot_sync(0xffffffffu, sel);
+      if (sel) out_idx[npb + written + __popc(sel_ball & lt_mask)] = npb + i;
+      written += __popc(sel_ball);
+      eq_seen += __popc(eq_ball);
+    }
   }
 }
 
@@ -260,8 +265,7 @@ bsa_status launch_select(const SelectArgs& a, cudaStream_t stream) {
     for (int b = 0; b < a.B; ++b) p.seq_lens[b] = a.seq_lens ? a.seq_lens[b] : a.Sq;
     for (int h = 0; h < a.Hq; ++h) p.keep[h] = a.keep[h];
     p.indices = a.indices; p.counts = a.counts;
-    const size_t smem = sizeof(float) * ((size_t)kRows * a.d + 32 * (a.d + 1)) +
-                        sizeof(uint32_t) * (size_t)kRows * a.nKb;
+    const size_t smem = sizeof(float) * (size_t)kRows * a.d + sizeof(uint32_t) * (size_t)kRows * a.nKb;
     if (smem > 227 * 1024)
       return set_error(BSA_ERR_UNSUPPORTED, "bsa_select: too many key blocks (nKb=" +
                                                 std::to_string(a.nKb) + ") for one CTA's shared memory");
@@ -270,7 +274,7 @@ bsa_status launch_select(const SelectArgs& a, cudaStream_t stream) {
                          "cudaFuncSetAttribute(score_topk_kernel)")) != BSA_OK)
       return st;
     dim3 grid((a.nQb + kRows - 1) / kRows, a.Hq, a.B);
-    score_topk_kernel<<<grid, kRows * 32, smem, stream>>>(p);
+    score_topk_kernel<<<grid, kTopkThreads, smem, stream>>>(p);
     if ((st = cuda_check(cudaGetLastError(), "score_topk_kernel launch")) != BSA_OK) return st;
   }
   return BSA_OK;
