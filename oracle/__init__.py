@@ -11,6 +11,7 @@ from .bsa_oracle import (  # noqa: F401
     attention,
     attention_rows,
     attention_tile,
+    causal_prefix_attention,
     boundary_gap,
     cdiv,
     default_scale,

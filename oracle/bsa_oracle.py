@@ -320,3 +320,38 @@ def attention(q, k, v, indices, counts, prefix_len: int, seq_lens: Sequence[int]
         out[b, r0:r0 + o.shape[0], h, :] = o
         lse[b, h, r0:r0 + o.shape[0]] = l
     return out, lse
+
+
+# ---------------------------------------------------------------------------
+# Understanding stream: causal self-attention over the prefix
+# ---------------------------------------------------------------------------
+
+def causal_prefix_attention(q_und, k, v, prefix_len: int, scale: Optional[float] = None):
+    """Causal self-attention of the understanding (prefix) stream.
+
+    cosmos_parallel.py, ``cosmos3_cp_attention``: the understanding pathway
+    self-attends causally over the full understanding sequence (``is_causal``
+    with equal query and key lengths).  Query row i of ``q_und`` ``[B, P, Hq, d]``
+    attends key positions ``0..i`` of ``k``/``v`` (``[B, >=P, Hkv, d]``; only the
+    first P rows are understanding keys), reading KV head h // (Hq/Hkv).
+
+    Returns out ``[B, P, Hq, d]`` and lse ``[B, Hq, P]`` (float64).
+    """
+    q_und = np.asarray(q_und)
+    B, P, Hq, d = q_und.shape
+    Hkv = np.asarray(k).shape[2]
+    G = Hq // Hkv
+    if scale is None or scale <= 0:
+        scale = default_scale(d)
+    out = np.zeros((B, P, Hq, np.asarray(v).shape[3]))
+    lse = np.full((B, Hq, P), -np.inf)
+    for b in range(B):
+        for h in range(Hq):
+            qq = np.asarray(q_und[b, :, h, :], dtype=np.float64)
+            kk = np.asarray(k[b, :P, h // G, :], dtype=np.float64)
+            vv = np.asarray(v[b, :P, h // G, :], dtype=np.float64)
+            for i in range(P):
+                o, l = attention_rows(qq[i:i + 1], kk[:i + 1], vv[:i + 1], scale)
+                out[b, i, h] = o[0]
+                lse[b, h, i] = l[0]
+    return out, lse

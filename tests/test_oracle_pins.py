@@ -433,3 +433,40 @@ def test_planted_dropped_prefix_is_caught(monkeypatch):
                           e["seq_lens"], e["block_q"], e["block_k"], [np.float32(0.5)])
     c = sel["counts"][0, 0, 0]
     assert c != 3 or not np.array_equal(sel["indices"][0, 0, :, :3], e["expect_indices"][0][0])
+
+
+# ------------------------------------------------ causal understanding pass ---
+
+def test_causal_prefix_matches_torch_sdpa_is_causal():
+    rng = np.random.default_rng(11)
+    B, P, Hq, Hkv, d = 2, 37, 4, 2, 16
+    q = rng.standard_normal((B, P, Hq, d))
+    k = rng.standard_normal((B, P + 9, Hkv, d))     # rows past P are generation keys: never read
+    v = rng.standard_normal((B, P + 9, Hkv, d))
+    out, lse = O.causal_prefix_attention(q, k, v, P)
+    for b in range(B):
+        qt = torch.from_numpy(q[b]).permute(1, 0, 2)
+        kt = torch.from_numpy(k[b, :P]).permute(1, 0, 2).repeat_interleave(2, 0)
+        vt = torch.from_numpy(v[b, :P]).permute(1, 0, 2).repeat_interleave(2, 0)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True)
+        np.testing.assert_allclose(out[b], ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+        z = (qt @ kt.transpose(1, 2)) / math.sqrt(d)
+        z = z.masked_fill(torch.ones(P, P, dtype=torch.bool).triu(1), float("-inf"))
+        np.testing.assert_allclose(lse[b], torch.logsumexp(z, -1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_causal_prefix_first_row_and_generation_keys_ignored():
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((1, 5, 1, 4))
+    k = rng.standard_normal((1, 8, 1, 4))
+    v = rng.standard_normal((1, 8, 1, 4))
+    out, lse = O.causal_prefix_attention(q, k, v, 5, scale=0.5)
+    # row 0 sees only key 0: output = v[0], lse = its logit
+    np.testing.assert_allclose(out[0, 0, 0], v[0, 0, 0], rtol=1e-14)
+    np.testing.assert_allclose(lse[0, 0, 0], 0.5 * q[0, 0, 0] @ k[0, 0, 0], rtol=1e-14)
+    k2, v2 = k.copy(), v.copy()
+    k2[0, 5:] = 1e6
+    v2[0, 5:] = np.nan
+    out2, lse2 = O.causal_prefix_attention(q, k2, v2, 5, scale=0.5)
+    np.testing.assert_array_equal(out, out2)
+    np.testing.assert_array_equal(lse, lse2)
