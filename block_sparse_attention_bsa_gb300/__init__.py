@@ -11,6 +11,7 @@ from .api import (  # noqa: F401
     BsaError,
     bsa_device_status,
     bsa_forward,
+    bsa_forward_causal,
     bsa_forward_workspace_size,
     bsa_get_last_error,
     bsa_select,

@@ -186,6 +186,32 @@ def bsa_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, indices: Opti
     return out, lse
 
 
+def bsa_forward_causal(q_und: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_q: int, block_k: int,
+                       softmax_scale: float = 0.0, *, out: Optional[torch.Tensor] = None,
+                       lse: Optional[torch.Tensor] = None, return_lse: bool = True,
+                       workspace: Optional[torch.Tensor] = None, stream=None):
+    """Causal self-attention of the understanding stream: row i of ``q_und``
+    ``[B, P, Hq, d]`` attends key rows 0..i of ``k``/``v`` (only their first P
+    rows are read).  Returns ``(out [B, P, Hq, d], lse [B, Hq, P] or None)``."""
+    qd, kd, vd = _desc(q_und, "q_und"), _desc(k, "k"), _desc(v, "v")
+    B, P, Hq, d = q_und.shape
+    if out is None:
+        out = torch.empty((B, P, Hq, d), dtype=torch.bfloat16, device=q_und.device)
+    if tuple(out.shape) != (B, P, Hq, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor [B, P, Hq, d]")
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, P), dtype=torch.float32, device=q_und.device)
+    need = bsa_forward_workspace_size(B, Hq, P, block_q)
+    ws = _workspace(need, q_und.device, workspace)
+    st = _lib.load().bsa_forward_causal(ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), int(block_q),
+                                        int(block_k), float(softmax_scale), out.data_ptr(),
+                                        lse.data_ptr() if lse is not None else None,
+                                        ws.data_ptr() if ws is not None else None,
+                                        ws.numel() if ws is not None else 0, _stream_ptr(stream))
+    _check(st)
+    return out, lse
+
+
 def bsa_validate_indices(indices: torch.Tensor, counts: torch.Tensor, B: int, Hq: int, Sq: int, Skv: int,
                          prefix_len: int, seq_lens: Optional[Sequence[int]], block_q: int, block_k: int,
                          require_prefix: bool = True, stream=None) -> int:

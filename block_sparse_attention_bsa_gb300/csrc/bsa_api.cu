@@ -251,6 +251,42 @@ bsa_status bsa_forward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tenso
   return launch_forward(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+bsa_status bsa_forward_causal(const bsa_tensor* q_und, const bsa_tensor* k, const bsa_tensor* v,
+                              int32_t block_q, int32_t block_k, float softmax_scale, void* out, float* lse,
+                              void* workspace, size_t ws_bytes, bsa_stream_t stream) {
+  clear_error();
+  const char* fn = "bsa_forward_causal";
+  // The understanding stream: queries are q_und's rows, keys the first P rows of k/v.
+  bsa_status st = check_common(fn, q_und, k, 0, nullptr, block_q, block_k, 1 << 20);
+  if (st != BSA_OK) return st;
+  if ((st = check_tensor(v, fn, "v")) != BSA_OK) return st;
+  if (v->B != k->B || v->S != k->S || v->H != k->H || v->D != k->D)
+    return set_error(BSA_ERR_INVALID_ARG, "bsa_forward_causal: v shape differs from k shape");
+  if (!out) return set_error(BSA_ERR_INVALID_ARG, "bsa_forward_causal: out is NULL");
+  if (reinterpret_cast<uintptr_t>(out) & 15u)
+    return set_error(BSA_ERR_INVALID_ARG, "bsa_forward_causal: out is not 16-byte aligned");
+  if (!(std::isfinite(softmax_scale)))
+    return set_error(BSA_ERR_INVALID_ARG, "bsa_forward_causal: softmax_scale is not finite");
+  if ((st = check_workspace(fn, workspace, ws_bytes,
+                            bsa_forward_workspace_size((int)q_und->B, (int)q_und->H, (int)q_und->S, block_q))) != BSA_OK)
+    return st;
+  ForwardArgs a{};
+  a.q = q_und->ptr; a.q_sb = q_und->stride_b; a.q_ss = q_und->stride_s; a.q_sh = q_und->stride_h;
+  a.k = k->ptr; a.k_sb = k->stride_b; a.k_ss = k->stride_s; a.k_sh = k->stride_h;
+  a.v = v->ptr; a.v_sb = v->stride_b; a.v_ss = v->stride_s; a.v_sh = v->stride_h;
+  a.B = (int)q_und->B; a.Hq = (int)q_und->H; a.Hkv = (int)k->H; a.Sq = (int)q_und->S; a.Skv = (int)k->S;
+  a.d = (int)q_und->D;
+  a.block_q = block_q; a.block_k = block_k;
+  a.prefix_len = 0;                    // every understanding row is a query; keys are rows [0, P)
+  a.nQb = (int)cdiv64(q_und->S, block_q); a.nKb = (int)cdiv64(k->S, block_k);
+  a.seq_lens = nullptr;                // L_b = P for every request
+  a.indices = nullptr; a.counts = nullptr;
+  a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)q_und->D);
+  a.out = out; a.lse = lse; a.workspace = workspace;
+  a.causal = true;
+  return launch_forward(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 bsa_status bsa_validate_indices(const int32_t* indices, const int32_t* counts, int32_t B, int32_t Hq, int32_t Sq,
                                 int32_t Skv, int32_t prefix_len, const int32_t* seq_lens, int32_t block_q,
                                 int32_t block_k, int32_t require_prefix, int32_t* bad_rows, bsa_stream_t stream) {

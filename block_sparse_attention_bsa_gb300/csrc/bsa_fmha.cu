@@ -61,6 +61,7 @@ struct FmhaParams {   // CUtensorMap members make it 128-byte aligned
   int b0;           // first request of this launch
   int Bn;           // requests in this launch
   int Hq, Hkv, G, Sq, nQb, nKb, block_q, prefix_len, n_tiles;
+  int causal;              // 1: query row i sees key positions 0..i only (dense pass)
   const int32_t* indices;  // NULL = dense pass
   const int32_t* counts;
   int* counter;            // next work tile (zeroed by the schedule kernel)
@@ -128,7 +129,9 @@ __device__ __forceinline__ TileInfo decode_tile(const FmhaParams& p, int t, int 
   if (ti.qb * p.block_q >= ti.L) {
     ti.n = 0;
   } else if (p.indices == nullptr) {
-    ti.n = (ti.valid_kv + BK - 1) / BK;
+    // dense pass; a causal pass stops at the block holding the block's last row
+    const int kv_end = p.causal ? min(ti.valid_kv, min((ti.qb + 1) * p.block_q, ti.L)) : ti.valid_kv;
+    ti.n = (kv_end + BK - 1) / BK;
   } else {
     const int c = p.counts[row];
     ti.n = c < 0 ? 0 : (c > p.nKb ? p.nKb : c);
@@ -502,7 +505,10 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < BK / 32; ++c) tmem_ld32f(s_t + c * 32, s + c * 32);
         tmem_wait_ld();
-        const int kvalid = ti.valid_kv - kb * BK;
+        // keys of this block this row may see: the real keys, and in a causal
+        // pass only positions <= the row
+        const int kv_end = p.causal ? min(ti.valid_kv, row + 1) : ti.valid_kv;
+        const int kvalid = kv_end - kb * BK;
         if (kvalid < BK) {
 #pragma unroll
           for (int c = 0; c < BK; ++c)
@@ -626,6 +632,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
 // counter reset for the forward launch that follows on the same stream.
 struct ScheduleParams {
   const int32_t* counts;   // NULL = dense pass
+  int causal;
   int b0, Bn, Hq, Hkv, G, nQb, nKb, block_q, block_k, prefix_len;
   int seq_lens[kMaxFwdBatch];
   int* counter;
@@ -650,7 +657,8 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const __grid_constant__ 
     const int L = p.seq_lens[bl];
     const int rows = min(p.block_q, L - qb * p.block_q);
     if (rows <= 0) continue;
-    int n = (p.prefix_len + L + p.block_k - 1) / p.block_k;
+    const int kv_end = p.causal ? min(p.prefix_len + L, min((qb + 1) * p.block_q, L)) : p.prefix_len + L;
+    int n = (kv_end + p.block_k - 1) / p.block_k;
     if (p.counts) {
       n = p.counts[((int64_t)(p.b0 + bl) * p.Hq + hk * p.G + g) * p.nQb + qb];
       n = n < 0 ? 0 : min(n, p.nKb);
@@ -753,6 +761,7 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
     p.n_tiles = Bn * a.nQb * a.Hq;
     p.indices = a.indices;
     p.counts = a.counts;
+    p.causal = a.causal ? 1 : 0;
     char* cws = static_cast<char*>(a.workspace) + (size_t)(b0 / kMaxFwdBatch) * forward_chunk_bytes(a.Hq);
     p.counter = reinterpret_cast<int*>(cws);
     p.group_order = reinterpret_cast<const int*>(cws + 256);
@@ -763,6 +772,7 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
     if (grid <= 0) continue;
     ScheduleParams sp{};
     sp.counts = a.indices ? a.counts : nullptr;
+    sp.causal = a.causal ? 1 : 0;
     sp.b0 = b0; sp.Bn = Bn; sp.Hq = a.Hq; sp.Hkv = a.Hkv; sp.G = a.Hq / a.Hkv;
     sp.nQb = a.nQb; sp.nKb = a.nKb; sp.block_q = a.block_q; sp.block_k = BK; sp.prefix_len = a.prefix_len;
     for (int i = 0; i < Bn; ++i) sp.seq_lens[i] = p.seq_lens[i];

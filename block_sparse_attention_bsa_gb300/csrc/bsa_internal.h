@@ -56,6 +56,7 @@ struct ForwardArgs {
   void* out;
   float* lse;
   void* workspace;           // forward_chunk_bytes(Hq) per chunk of kMaxFwdBatch requests
+  bool causal;               // key position <= query row (dense pass over the prefix only)
 };
 // Workspace bytes per launch chunk: tile counter (256 B) + group order.
 size_t forward_chunk_bytes(int Hq);

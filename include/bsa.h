@@ -178,6 +178,25 @@ BSA_API bsa_status bsa_forward(const bsa_tensor* q, const bsa_tensor* k, const b
                        void* out, float* lse,
                        void* workspace, size_t ws_bytes, bsa_stream_t stream);
 
+/* ------------------------------------------ understanding stream, causal ---
+ * Causal self-attention of the understanding (prefix) stream
+ * (cosmos_parallel.py, cosmos3_cp_attention: the understanding pathway
+ * self-attends causally over the whole understanding sequence), through the
+ * same kernel as bsa_forward's dense pass.
+ *
+ * q_und: [B, P, Hq, d] bf16, P = q_und->S = the understanding length.
+ * k, v: [B, Skv, Hkv, d] with Skv >= P; only rows [0, P) (the prefix) are
+ *   read.  Row i of q_und attends key positions 0..i of KV head h/(Hq/Hkv):
+ *   out_i = softmax((q_i . k_j) * scale)_j v_j over j <= i; lse_i = ln-sum-exp.
+ * out: bf16 [B, P, Hq, d] contiguous; lse: fp32 [B, Hq, P] contiguous or NULL.
+ * block_q/block_k: any supported geometry (the key blocks up to the one that
+ *   holds a query block's last row are visited; the diagonal is masked per
+ *   row).  workspace: bsa_forward_workspace_size(B, Hq, P, block_q) bytes. */
+BSA_API bsa_status bsa_forward_causal(const bsa_tensor* q_und, const bsa_tensor* k, const bsa_tensor* v,
+                                      int32_t block_q, int32_t block_k, float softmax_scale,
+                                      void* out, float* lse, void* workspace, size_t ws_bytes,
+                                      bsa_stream_t stream);
+
 /* ------------------------------------------------------------ validation ---
  * Debug check of index lists (PR 8335, Purpose: provider failures propagate
  * as errors).  Counts the rows (b, h, qb) whose list is malformed: count

@@ -31,7 +31,7 @@ def test_header_declares_the_expected_calls():
     assert declared_symbols() == sorted([
         "bsa_version", "bsa_get_last_error", "bsa_select_workspace_size", "bsa_select",
         "bsa_forward_workspace_size", "bsa_forward", "bsa_validate_indices", "bsa_device_status",
-        "bsa_select_noalloc",
+        "bsa_select_noalloc", "bsa_forward_causal",
     ])
 
 
@@ -203,3 +203,14 @@ def test_python_binding_refuses_cpu_tensors():
         bsa.bsa_select(q, q, 0, None, 64, 64, 0.5)
     with pytest.raises(ValueError, match="CUDA tensor"):
         bsa.bsa_forward(q, q, q, None, None, 0, None, 64, 64)
+
+
+def test_causal_rejects_bad_arguments(lib):
+    q, k, v = T(H=4, S=512), T(H=2, S=400), T(H=2, S=400)
+    st = lib.bsa_forward_causal(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 256, 128, 0.0, FAKE, None,
+                                None, 0, None)
+    assert st == 1 and "exceeds Skv" in err(lib)          # understanding keys must cover P rows
+    k, v = T(H=2, S=512), T(H=2, S=512)
+    st = lib.bsa_forward_causal(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 256, 128, 0.0, FAKE, None,
+                                None, 0, None)
+    assert st == 3 and "workspace is NULL" in err(lib)

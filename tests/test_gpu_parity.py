@@ -226,6 +226,43 @@ def test_out_of_range_indices_are_clamped_not_read():
     run_forward(inp, bad, cnt_big)
 
 
+# ------------------------------------------- causal understanding stream ---
+
+@pytest.mark.parametrize("P,Hq,Hkv,d,bq,bk", [
+    (700, 4, 2, 128, 256, 128),      # ragged last query and key blocks
+    (1024, 8, 2, 128, 256, 128),     # the 720p workload's prefix length
+    (333, 3, 1, 64, 64, 64),         # MQA, 64x64 geometry
+    (512, 2, 2, 128, 128, 64),
+])
+def test_causal_prefix_parity(P, Hq, Hkv, d, bq, bk):
+    g = torch.Generator(device="cpu").manual_seed(P * 7 + Hq)
+    q = torch.randn(2, P, Hq, d, generator=g).bfloat16()
+    k = torch.randn(2, P + 300, Hkv, d, generator=g).bfloat16()     # generation rows after P
+    v = torch.randn(2, P + 300, Hkv, d, generator=g).bfloat16()
+    k[:, P:] = float("nan")                                         # never read
+    v[:, P:] = float("nan")
+    out, lse = bsa.bsa_forward_causal(q.cuda(), k.cuda(), v.cuda(), bq, bk)
+    bsa.bsa_device_status()
+    o_ref, l_ref = O.causal_prefix_attention(q.float().numpy(), k.float().numpy(), v.float().numpy(), P)
+    stats = compare_attention(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, [P, P])
+    print("causal", P, Hq, Hkv, d, bq, bk, stats)
+
+
+def test_causal_equals_dense_on_last_row():
+    """The last understanding row sees every prefix key: it must equal a dense
+    pass of that row over the prefix (a selected-block forward with P keys)."""
+    g = torch.Generator(device="cpu").manual_seed(5)
+    P, Hq, Hkv, d = 512, 2, 1, 128
+    q = torch.randn(1, P, Hq, d, generator=g).bfloat16().cuda()
+    k = torch.randn(1, P, Hkv, d, generator=g).bfloat16().cuda()
+    v = torch.randn(1, P, Hkv, d, generator=g).bfloat16().cuda()
+    out, lse = bsa.bsa_forward_causal(q, k, v, 256, 128)
+    dense, dl = bsa.bsa_forward(q, k, v, None, None, 0, None, 256, 128)
+    bsa.bsa_device_status()
+    assert (out[0, -1].float() - dense[0, -1].float()).abs().max().item() <= 2 ** -8
+    assert abs(lse[0, 0, -1].item() - dl[0, 0, -1].item()) <= 1e-5
+
+
 # ----------------------------------------------------------- full size ---
 
 def full_inputs(name):
