@@ -8,6 +8,7 @@ invariants and a hand-worked example); none is "parity unpinned".
 
 from .bsa_oracle import (  # noqa: F401
     NEAR_TIE_REL,
+    apply_rope,
     attention,
     attention_rows,
     attention_tile,
@@ -20,6 +21,9 @@ from .bsa_oracle import (  # noqa: F401
     keep_count,
     kv_geometry,
     pool_means,
+    rope_then_select,
+    rotate_half,
+    round_to_bf16,
     select_blocks,
     tile_keys,
     topk_lowest_index,

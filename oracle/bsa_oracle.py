@@ -355,3 +355,55 @@ def causal_prefix_attention(q_und, k, v, prefix_len: int, scale: Optional[float]
                 out[b, i, h] = o[0]
                 lse[b, h, i] = l[0]
     return out, lse
+
+
+# ---------------------------------------------------------------------------
+# Rotary prologue (applied before selection and attention)
+# ---------------------------------------------------------------------------
+
+def round_to_bf16(x) -> np.ndarray:
+    """float64/float32 -> nearest bf16 value (ties to even), returned as float64.
+
+    IEEE round-to-nearest-even on the float32 bit pattern: add 0x7FFF plus the
+    lowest kept bit, clear the 16 dropped bits.  NaN stays NaN."""
+    f = np.asarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) & 0xFFFF0000).astype(np.uint32).view(np.float32)
+    r = np.where(np.isnan(f), np.float32(np.nan), r)
+    return r.astype(np.float64)
+
+
+def rotate_half(x: np.ndarray) -> np.ndarray:
+    """Half-split rotation of the last axis: (x1, x2) -> (-x2, x1).
+
+    cosmos_parallel.py imports ``_rotate_half`` from the Cosmos 3 transformer
+    without printing it; this is the conventional half-split form that name
+    denotes (first half paired with the second half)."""
+    d = x.shape[-1]
+    return np.concatenate([-x[..., d // 2:], x[..., : d // 2]], axis=-1)
+
+
+def apply_rope(x, cos, sin) -> np.ndarray:
+    """``x * cos + rotate_half(x) * sin`` (cosmos_parallel.py,
+    ``_project_qkv_with_rope``), in float64.
+
+    ``x``: ``[B, S, H, d]``; ``cos``/``sin``: ``[S, d]`` per position, shared by
+    every head (the ``unsqueeze(1)`` over heads) and every request."""
+    x = np.asarray(x, dtype=np.float64)
+    c = np.asarray(cos, dtype=np.float64)[None, :, None, :]
+    s = np.asarray(sin, dtype=np.float64)[None, :, None, :]
+    return x * c + rotate_half(x) * s
+
+
+def rope_then_select(q, k, cos_q, sin_q, cos_k, sin_k, prefix_len, seq_lens, block_q, block_k,
+                     keep_ratio) -> dict:
+    """The selector run on rotated Q and K: RoPE in float64, rounded to bf16
+    (the precision the attention reads), then ``select_blocks``.  Returns the
+    selection dict plus ``q_rot`` and ``k_rot`` (the rounded tensors)."""
+    q_rot = round_to_bf16(apply_rope(q, cos_q, sin_q))
+    k_rot = round_to_bf16(apply_rope(k, cos_k, sin_k))
+    sel = select_blocks(q_rot, k_rot, prefix_len, seq_lens, block_q, block_k, keep_ratio)
+    sel["q_rot"] = q_rot
+    sel["k_rot"] = k_rot
+    return sel

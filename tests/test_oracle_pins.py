@@ -470,3 +470,66 @@ def test_causal_prefix_first_row_and_generation_keys_ignored():
     out2, lse2 = O.causal_prefix_attention(q, k2, v2, 5, scale=0.5)
     np.testing.assert_array_equal(out, out2)
     np.testing.assert_array_equal(lse, lse2)
+
+
+# ------------------------------------------------------------ RoPE prologue ---
+
+def _rope_tables(S, d, base=10000.0, offset=0):
+    inv = base ** (-np.arange(0, d // 2) * 2.0 / d)
+    ang = np.outer(np.arange(offset, offset + S), inv)             # [S, d/2]
+    ang = np.concatenate([ang, ang], axis=1)                       # half-split layout
+    return np.cos(ang), np.sin(ang)
+
+
+def test_round_to_bf16_matches_torch():
+    rng = np.random.default_rng(13)
+    x = np.concatenate([rng.standard_normal(20000) * 10 ** rng.uniform(-6, 6, 20000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.0078125, 3.0e38, np.inf, -np.inf]])
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(O.round_to_bf16(x), want)
+    assert np.isnan(O.round_to_bf16(np.array([np.nan]))).all()
+
+
+def test_rope_identity_at_angle_zero():
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal((2, 9, 3, 16))
+    np.testing.assert_array_equal(O.apply_rope(x, np.ones((9, 16)), np.zeros((9, 16))), x)
+
+
+def test_rope_preserves_pair_norms():
+    rng = np.random.default_rng(15)
+    x = rng.standard_normal((1, 11, 2, 32))
+    c, s = _rope_tables(11, 32)
+    y = O.apply_rope(x, c, s)
+    n_x = x[..., :16] ** 2 + x[..., 16:] ** 2
+    n_y = y[..., :16] ** 2 + y[..., 16:] ** 2
+    np.testing.assert_allclose(n_y, n_x, rtol=1e-12)
+    # quarter turn on every pair: (x1, x2) -> (-x2, x1)
+    np.testing.assert_allclose(O.apply_rope(x, np.zeros((11, 32)), np.ones((11, 32))), O.rotate_half(x), rtol=0)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    rng = np.random.default_rng(16)
+    d = 64
+    qv, kv = rng.standard_normal(d), rng.standard_normal(d)
+    c, s = _rope_tables(40, d)
+    q = np.tile(qv, (1, 40, 1, 1)).reshape(1, 40, 1, d)
+    k = np.tile(kv, (1, 40, 1, 1)).reshape(1, 40, 1, d)
+    qr, kr = O.apply_rope(q, c, s)[0, :, 0], O.apply_rope(k, c, s)[0, :, 0]
+    for m, n in [(5, 2), (25, 22), (39, 36)]:                     # all offset 3
+        np.testing.assert_allclose(qr[m] @ kr[n], qr[5] @ kr[2], rtol=1e-10)
+
+
+def test_rope_then_select_uses_rounded_rotated_inputs():
+    inp = make_inputs(CONFIGS["small_mqa_d64"], "cpu", pad_fill=0.0)
+    c = inp["cfg"]
+    q, k = f64(inp["q"]), f64(inp["k"])
+    cq, sq = _rope_tables(c.Sq, c.d)
+    ck, sk = _rope_tables(c.Skv, c.d)
+    sel = O.rope_then_select(q, k, cq, sq, ck, sk, c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    ref = O.select_blocks(O.round_to_bf16(O.apply_rope(q, cq, sq)), O.round_to_bf16(O.apply_rope(k, ck, sk)),
+                          c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    np.testing.assert_array_equal(sel["indices"], ref["indices"])
+    # rotation changes the selection (the prologue matters)
+    plain = O.select_blocks(q, k, c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    assert not np.array_equal(plain["indices"], sel["indices"])
