@@ -16,6 +16,7 @@ from .api import (  # noqa: F401
     bsa_get_last_error,
     bsa_select,
     bsa_select_noalloc,
+    bsa_select_rope,
     bsa_select_workspace_size,
     bsa_validate_indices,
     bsa_version,

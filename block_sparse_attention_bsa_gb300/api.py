@@ -124,6 +124,42 @@ def bsa_select(q: torch.Tensor, k: torch.Tensor, prefix_len: int, seq_lens: Opti
     return indices, counts
 
 
+def bsa_select_rope(q: torch.Tensor, k: torch.Tensor, cos_q: torch.Tensor, sin_q: torch.Tensor,
+                    cos_k: torch.Tensor, sin_k: torch.Tensor, prefix_len: int, seq_lens: Optional[Sequence[int]],
+                    block_q: int, block_k: int, keep_ratio, *, q_out: Optional[torch.Tensor] = None,
+                    k_out: Optional[torch.Tensor] = None, indices: Optional[torch.Tensor] = None,
+                    counts: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Rotary prologue fused with the selector: returns ``(q_out, k_out,
+    indices, counts)``; q_out/k_out are the rotated bf16 tensors (contiguous)
+    to pass to bsa_forward.  cos/sin: fp32 CUDA tensors [S, d]."""
+    qd, kd = _desc(q, "q"), _desc(k, "k")
+    B, Sq, Hq, d = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    nQb, nKb = _cdiv(Sq, block_q), _cdiv(Skv, block_k)
+    for name, t, rows in (("cos_q", cos_q, Sq), ("sin_q", sin_q, Sq), ("cos_k", cos_k, Skv), ("sin_k", sin_k, Skv)):
+        if t.dtype != torch.float32 or tuple(t.shape) != (rows, d) or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous fp32 tensor [{rows}, {d}] on {q.device}")
+    if isinstance(keep_ratio, (int, float)):
+        keep_ratio = [float(keep_ratio)]
+    keep = (ctypes.c_float * len(keep_ratio))(*[float(x) for x in keep_ratio])
+    q_out = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device=q.device) if q_out is None else q_out
+    k_out = torch.empty((B, Skv, Hkv, d), dtype=torch.bfloat16, device=q.device) if k_out is None else k_out
+    if indices is None:
+        indices = torch.full((B, Hq, nQb, nKb), -1, dtype=torch.int32, device=q.device)
+    if counts is None:
+        counts = torch.empty((B, Hq, nQb), dtype=torch.int32, device=q.device)
+    need = bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, block_q, block_k)
+    ws = _workspace(need, q.device, workspace)
+    st = _lib.load().bsa_select_rope(ctypes.byref(qd), ctypes.byref(kd), cos_q.data_ptr(), sin_q.data_ptr(),
+                                     cos_k.data_ptr(), sin_k.data_ptr(), int(prefix_len), _i32_array(seq_lens),
+                                     int(block_q), int(block_k), keep, len(keep_ratio), q_out.data_ptr(),
+                                     k_out.data_ptr(), indices.data_ptr(), counts.data_ptr(),
+                                     ws.data_ptr() if ws is not None else None,
+                                     ws.numel() if ws is not None else 0, _stream_ptr(stream))
+    _check(st)
+    return q_out, k_out, indices, counts
+
+
 def bsa_select_noalloc(q: torch.Tensor, k: torch.Tensor, prefix_len: int, seq_lens: Optional[Sequence[int]],
                        block_q: int, block_k: int, keep_ratio, *, indices: Optional[torch.Tensor] = None,
                        counts: Optional[torch.Tensor] = None, stream=None):

@@ -174,28 +174,31 @@ size_t bsa_select_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int d,
   return select_workspace_bytes(B, Hq, Hkv, Sq, Skv, d, block_q, block_k);
 }
 
-bsa_status bsa_select(const bsa_tensor* q, const bsa_tensor* k, int32_t prefix_len, const int32_t* seq_lens,
-                      int32_t block_q, int32_t block_k, const float* keep_ratio, int32_t n_keep,
-                      int32_t* indices, int32_t* counts, void* workspace, size_t ws_bytes,
-                      bsa_stream_t stream) {
-  clear_error();
-  const char* fn = "bsa_select";
+}  // extern "C"
+
+namespace {
+// Shared body of bsa_select and bsa_select_rope (`rope` carries the tables and
+// rotated outputs, or is NULL).
+bsa_status select_impl(const char* fn, const bsa_tensor* q, const bsa_tensor* k, int32_t prefix_len,
+                       const int32_t* seq_lens, int32_t block_q, int32_t block_k, const float* keep_ratio,
+                       int32_t n_keep, int32_t* indices, int32_t* counts, void* workspace, size_t ws_bytes,
+                       bsa_stream_t stream, const SelectArgs* rope) {
   bsa_status st = check_common(fn, q, k, prefix_len, seq_lens, block_q, block_k, kMaxSelectBatch);
   if (st != BSA_OK) return st;
-  if (!keep_ratio) return set_error(BSA_ERR_INVALID_ARG, "bsa_select: keep_ratio is NULL");
+  if (!keep_ratio) return set_error(BSA_ERR_INVALID_ARG, std::string(fn) + ": keep_ratio is NULL");
   if (n_keep != 1 && n_keep != q->H)
-    return set_error(BSA_ERR_INVALID_ARG, "bsa_select: n_keep = " + std::to_string(n_keep) + " must be 1 or Hq = " +
+    return set_error(BSA_ERR_INVALID_ARG, std::string(fn) + ": n_keep = " + std::to_string(n_keep) + " must be 1 or Hq = " +
                                               std::to_string(q->H));
   float keep[kMaxHeads];
   for (int h = 0; h < q->H; ++h) {
     const float r = keep_ratio[n_keep == 1 ? 0 : h];
     if (!(r >= 0.f && r <= 1.f))
-      return set_error(BSA_ERR_INVALID_ARG, "bsa_select: keep_ratio[" + std::to_string(n_keep == 1 ? 0 : h) +
+      return set_error(BSA_ERR_INVALID_ARG, std::string(fn) + ": keep_ratio[" + std::to_string(n_keep == 1 ? 0 : h) +
                                                 "] = " + std::to_string(r) + " outside [0, 1]");
     keep[h] = r;
   }
-  if (!indices) return set_error(BSA_ERR_INVALID_ARG, "bsa_select: indices is NULL");
-  if (!counts) return set_error(BSA_ERR_INVALID_ARG, "bsa_select: counts is NULL");
+  if (!indices) return set_error(BSA_ERR_INVALID_ARG, std::string(fn) + ": indices is NULL");
+  if (!counts) return set_error(BSA_ERR_INVALID_ARG, std::string(fn) + ": counts is NULL");
   const size_t need = select_workspace_bytes((int)q->B, (int)q->H, (int)k->H, (int)q->S, (int)k->S, (int)q->D,
                                              block_q, block_k);
   if ((st = check_workspace(fn, workspace, ws_bytes, need)) != BSA_OK) return st;
@@ -208,9 +211,45 @@ bsa_status bsa_select(const bsa_tensor* q, const bsa_tensor* k, int32_t prefix_l
   a.seq_lens = seq_lens; a.keep = keep;
   a.indices = indices; a.counts = counts;
   const size_t qbar_bytes = ((size_t)a.B * a.Hq * a.nQb * a.d * sizeof(float) + 255) & ~(size_t)255;
+  if (rope) {
+    a.rope = true;
+    a.cos_q = rope->cos_q; a.sin_q = rope->sin_q; a.cos_k = rope->cos_k; a.sin_k = rope->sin_k;
+    a.q_out = rope->q_out; a.k_out = rope->k_out;
+  }
   a.qbar = static_cast<float*>(workspace);
   a.kbar = reinterpret_cast<float*>(static_cast<char*>(workspace) + qbar_bytes);
   return launch_select(a, reinterpret_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+extern "C" {
+
+bsa_status bsa_select(const bsa_tensor* q, const bsa_tensor* k, int32_t prefix_len, const int32_t* seq_lens,
+                      int32_t block_q, int32_t block_k, const float* keep_ratio, int32_t n_keep,
+                      int32_t* indices, int32_t* counts, void* workspace, size_t ws_bytes,
+                      bsa_stream_t stream) {
+  clear_error();
+  return select_impl("bsa_select", q, k, prefix_len, seq_lens, block_q, block_k, keep_ratio, n_keep, indices,
+                     counts, workspace, ws_bytes, stream, nullptr);
+}
+
+bsa_status bsa_select_rope(const bsa_tensor* q, const bsa_tensor* k, const float* cos_q, const float* sin_q,
+                           const float* cos_k, const float* sin_k, int32_t prefix_len, const int32_t* seq_lens,
+                           int32_t block_q, int32_t block_k, const float* keep_ratio, int32_t n_keep,
+                           void* q_out, void* k_out, int32_t* indices, int32_t* counts, void* workspace,
+                           size_t ws_bytes, bsa_stream_t stream) {
+  clear_error();
+  const void* ptrs[6] = {cos_q, sin_q, cos_k, sin_k, q_out, k_out};
+  const char* names[6] = {"cos_q", "sin_q", "cos_k", "sin_k", "q_out", "k_out"};
+  for (int i = 0; i < 6; ++i) {
+    if (!ptrs[i]) return set_error(BSA_ERR_INVALID_ARG, std::string("bsa_select_rope: ") + names[i] + " is NULL");
+    if (reinterpret_cast<uintptr_t>(ptrs[i]) & 15u)
+      return set_error(BSA_ERR_INVALID_ARG, std::string("bsa_select_rope: ") + names[i] + " is not 16-byte aligned");
+  }
+  SelectArgs r{};
+  r.cos_q = cos_q; r.sin_q = sin_q; r.cos_k = cos_k; r.sin_k = sin_k; r.q_out = q_out; r.k_out = k_out;
+  return select_impl("bsa_select_rope", q, k, prefix_len, seq_lens, block_q, block_k, keep_ratio, n_keep,
+                     indices, counts, workspace, ws_bytes, stream, &r);
 }
 
 size_t bsa_forward_workspace_size(int B, int Hq, int Sq, int block_q) {

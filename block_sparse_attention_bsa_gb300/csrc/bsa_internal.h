@@ -39,6 +39,11 @@ struct SelectArgs {
   int32_t* counts;
   float* qbar;               // workspace [B,Hq,nQb,d]
   float* kbar;               // workspace [B,Hkv,nKb,d]
+  // rotary prologue (bsa_select_rope): tables [S, d] fp32, rotated outputs
+  bool rope = false;
+  const float* cos_q = nullptr; const float* sin_q = nullptr;
+  const float* cos_k = nullptr; const float* sin_k = nullptr;
+  void* q_out = nullptr; void* k_out = nullptr;
 };
 bsa_status launch_select(const SelectArgs& a, cudaStream_t stream);
 

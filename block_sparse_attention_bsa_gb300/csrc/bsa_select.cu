@@ -87,6 +87,124 @@ __global__ void __launch_bounds__(kPoolCols* kPoolGroups)
   }
 }
 
+// ------------------------------------------------- rotary + pooling -------
+// Fused prologue: x' = x * cos + rotate_half(x) * sin per row (tables [S, d]
+// shared by every head and request), written back as bf16, and the block
+// means of the written (rounded) values.  A thread owns channels
+// [8j, 8j+8) and their partners [8j+d/2, 8j+d/2+8) of one head, so it holds
+// both halves of every rotated pair; rows are summed in the same order as
+// pool_kernel, so the means equal pooling the rotated tensor afterwards.
+
+struct RopePoolParams {
+  const __nv_bfloat16* x;
+  int64_t sb, ss, sh;              // input strides (elements)
+  __nv_bfloat16* y;                // output [B, S, H, D] contiguous
+  const float* cos_t;              // [S, D]
+  const float* sin_t;              // [S, D]
+  int H, D, S, block, nb, cols;    // cols = H * D / 16
+  int valid[kMaxSelectBatch];
+  float* out;                      // means [B, H, nb, D]
+};
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
+  const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(v2[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
+  uint4 u;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 t = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&t);
+  }
+  return u;
+}
+
+__global__ void __launch_bounds__(kPoolCols* kPoolGroups)
+    rope_pool_kernel(const __grid_constant__ RopePoolParams p) {
+  const int blk = blockIdx.x;
+  const int b = blockIdx.y;
+  const int tc = threadIdx.x % kPoolCols;
+  const int g = threadIdx.x / kPoolCols;
+  const int c = blockIdx.z * kPoolCols + tc;
+  const int r0 = blk * p.block;
+  const int r_end = min(r0 + p.block, p.S);
+  const int r_valid = min(r0 + p.block, p.valid[b]);
+  const int jc = p.D / 16, half = p.D / 2;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  int h = 0, lo = 0;
+  if (c < p.cols) {
+    h = c / jc;
+    lo = (c % jc) * 8;
+    const __nv_bfloat16* xb = p.x + (int64_t)b * p.sb + (int64_t)h * p.sh;
+    __nv_bfloat16* yb = p.y + (((int64_t)b * p.S) * p.H + h) * p.D;
+    for (int r = r0 + g; r < r_end; r += kPoolGroups) {
+      float xl[8], xh[8], cl[8], ch[8], sl[8], sh[8], yl[8], yh[8];
+      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(xb + (int64_t)r * p.ss + lo)), xl);
+      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(xb + (int64_t)r * p.ss + lo + half)), xh);
+      const float4* ct = reinterpret_cast<const float4*>(p.cos_t + (int64_t)r * p.D);
+      const float4* st = reinterpret_cast<const float4*>(p.sin_t + (int64_t)r * p.D);
+      *reinterpret_cast<float4*>(cl) = __ldg(ct + lo / 4);
+      *reinterpret_cast<float4*>(cl + 4) = __ldg(ct + lo / 4 + 1);
+      *reinterpret_cast<float4*>(ch) = __ldg(ct + (lo + half) / 4);
+      *reinterpret_cast<float4*>(ch + 4) = __ldg(ct + (lo + half) / 4 + 1);
+      *reinterpret_cast<float4*>(sl) = __ldg(st + lo / 4);
+      *reinterpret_cast<float4*>(sl + 4) = __ldg(st + lo / 4 + 1);
+      *reinterpret_cast<float4*>(sh) = __ldg(st + (lo + half) / 4);
+      *reinterpret_cast<float4*>(sh + 4) = __ldg(st + (lo + half) / 4 + 1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        yl[i] = fmaf(xl[i], cl[i], -xh[i] * sl[i]);   // first half: rotate_half gives -x2
+        yh[i] = fmaf(xh[i], ch[i], xl[i] * sh[i]);    // second half: rotate_half gives x1
+      }
+      const uint4 ul = f32_to_bf16x8(yl), uh = f32_to_bf16x8(yh);
+      __nv_bfloat16* yr = yb + (int64_t)r * p.H * p.D;
+      *reinterpret_cast<uint4*>(yr + lo) = ul;
+      *reinterpret_cast<uint4*>(yr + lo + half) = uh;
+      if (r < r_valid) {
+        float rl[8], rh[8];
+        bf16x8_to_f32(ul, rl);
+        bf16x8_to_f32(uh, rh);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc[i] += rl[i];
+          acc[8 + i] += rh[i];
+        }
+      }
+    }
+  }
+  __shared__ float red[kPoolGroups][kPoolCols][17];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) red[g][tc][i] = acc[i];
+  __syncthreads();
+  if (g == 0 && c < p.cols) {
+    const int n = max(r_valid - r0, 0);
+    const float inv = n > 0 ? 1.f / (float)n : 0.f;
+    float m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float s = red[0][tc][i];
+#pragma unroll
+      for (int gg = 1; gg < kPoolGroups; ++gg) s += red[gg][tc][i];
+      m[i] = s * inv;
+    }
+    float* o = p.out + (((int64_t)b * p.H + h) * p.nb + blk) * p.D;
+    reinterpret_cast<float4*>(o + lo)[0] = make_float4(m[0], m[1], m[2], m[3]);
+    reinterpret_cast<float4*>(o + lo)[1] = make_float4(m[4], m[5], m[6], m[7]);
+    reinterpret_cast<float4*>(o + lo + half)[0] = make_float4(m[8], m[9], m[10], m[11]);
+    reinterpret_cast<float4*>(o + lo + half)[1] = make_float4(m[12], m[13], m[14], m[15]);
+  }
+}
+
 // ---------------------------------------------------- score + top-k -------
 // One CTA per (batch element, query head, kRows query blocks).
 // Scores: every thread takes candidate key blocks in turn and computes their
@@ -232,8 +350,32 @@ __global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const __grid_c
 
 }  // namespace
 
+static bsa_status launch_topk(const SelectArgs& a, cudaStream_t stream);
+
 bsa_status launch_select(const SelectArgs& a, cudaStream_t stream) {
   bsa_status st;
+  if (a.rope) {
+    // RoPE on Q and K fused with their block means.
+    for (int which = 0; which < 2; ++which) {
+      RopePoolParams p{};
+      const bool isq = which == 0;
+      p.x = static_cast<const __nv_bfloat16*>(isq ? a.q : a.k);
+      p.sb = isq ? a.q_sb : a.k_sb; p.ss = isq ? a.q_ss : a.k_ss; p.sh = isq ? a.q_sh : a.k_sh;
+      p.y = static_cast<__nv_bfloat16*>(isq ? a.q_out : a.k_out);
+      p.cos_t = isq ? a.cos_q : a.cos_k; p.sin_t = isq ? a.sin_q : a.sin_k;
+      p.H = isq ? a.Hq : a.Hkv; p.D = a.d; p.S = isq ? a.Sq : a.Skv;
+      p.block = isq ? a.block_q : a.block_k; p.nb = isq ? a.nQb : a.nKb; p.cols = p.H * a.d / 16;
+      for (int b = 0; b < a.B; ++b) {
+        const int L = a.seq_lens ? a.seq_lens[b] : a.Sq;
+        p.valid[b] = isq ? L : a.prefix_len + L;
+      }
+      p.out = isq ? a.qbar : a.kbar;
+      dim3 grid(p.nb, a.B, (p.cols + kPoolCols - 1) / kPoolCols);
+      rope_pool_kernel<<<grid, kPoolCols * kPoolGroups, 0, stream>>>(p);
+      if ((st = cuda_check(cudaGetLastError(), "rope_pool_kernel launch")) != BSA_OK) return st;
+    }
+    return launch_topk(a, stream);
+  }
   // Pool Q over real query rows and K over real keys of every block.
   {
     PoolParams p{};
@@ -257,6 +399,11 @@ bsa_status launch_select(const SelectArgs& a, cudaStream_t stream) {
     pool_kernel<<<grid, kPoolCols * kPoolGroups, 0, stream>>>(p);
     if ((st = cuda_check(cudaGetLastError(), "pool_kernel(K) launch")) != BSA_OK) return st;
   }
+  return launch_topk(a, stream);
+}
+
+static bsa_status launch_topk(const SelectArgs& a, cudaStream_t stream) {
+  bsa_status st;
   {
     TopkParams p{};
     p.qbar = a.qbar; p.kbar = a.kbar;

@@ -118,6 +118,33 @@ BSA_API bsa_status bsa_select(const bsa_tensor* q, const bsa_tensor* k, int32_t 
                       int32_t* indices, int32_t* counts,
                       void* workspace, size_t ws_bytes, bsa_stream_t stream);
 
+/* ------------------------------------------------ select with RoPE fused ---
+ * The rotary prologue of cosmos_parallel.py (_project_qkv_with_rope:
+ * x' = x * cos + rotate_half(x) * sin per position, cos/sin shared by every
+ * head) fused with the selector's block pooling: Q and K are read once,
+ * rotated in fp32, written as bf16 to q_out / k_out (what bsa_forward then
+ * reads), and the block means are taken of the written bf16 values, so the
+ * result equals rotating first and calling bsa_select on q_out / k_out.
+ * rotate_half pairs channel i with channel i + d/2: (x1, x2) -> (-x2, x1).
+ *
+ * cos_q, sin_q: device fp32 [Sq, d] (positions of the generation queries);
+ * cos_k, sin_k: device fp32 [Skv, d] (understanding positions for key rows
+ *   < prefix_len, then generation positions).  All 16-byte aligned.
+ * q_out: device bf16 [B, Sq, Hq, d] contiguous; k_out: [B, Skv, Hkv, d]
+ *   contiguous.  Every row is rotated (padding rows too); q_out may be q's
+ *   own storage when q is contiguous (each element is read before it is
+ *   written by the same thread), likewise k_out.
+ * Everything else as bsa_select (same workspace size). */
+BSA_API bsa_status bsa_select_rope(const bsa_tensor* q, const bsa_tensor* k,
+                                   const float* cos_q, const float* sin_q,
+                                   const float* cos_k, const float* sin_k,
+                                   int32_t prefix_len, const int32_t* seq_lens,
+                                   int32_t block_q, int32_t block_k,
+                                   const float* keep_ratio, int32_t n_keep,
+                                   void* q_out, void* k_out,
+                                   int32_t* indices, int32_t* counts,
+                                   void* workspace, size_t ws_bytes, bsa_stream_t stream);
+
 /* ------------------------------------------------- select, no allocation ---
  * bsa_select for callers that cannot provide device scratch memory: for
  * example a plugin inside a serving runtime that owns every device

@@ -31,7 +31,7 @@ def test_header_declares_the_expected_calls():
     assert declared_symbols() == sorted([
         "bsa_version", "bsa_get_last_error", "bsa_select_workspace_size", "bsa_select",
         "bsa_forward_workspace_size", "bsa_forward", "bsa_validate_indices", "bsa_device_status",
-        "bsa_select_noalloc", "bsa_forward_causal",
+        "bsa_select_noalloc", "bsa_forward_causal", "bsa_select_rope",
     ])
 
 
@@ -214,3 +214,17 @@ def test_causal_rejects_bad_arguments(lib):
     st = lib.bsa_forward_causal(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 256, 128, 0.0, FAKE, None,
                                 None, 0, None)
     assert st == 3 and "workspace is NULL" in err(lib)
+
+
+def test_select_rope_rejects_missing_tables(lib):
+    q, k = T(H=4), T(H=2, S=768)
+    keep = (ctypes.c_float * 1)(0.25)
+    st = lib.bsa_select_rope(ctypes.byref(q), ctypes.byref(k), None, FAKE, FAKE, FAKE, 256, None, 256, 128, keep, 1,
+                             FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert st == 1 and "cos_q is NULL" in err(lib)
+    st = lib.bsa_select_rope(ctypes.byref(q), ctypes.byref(k), FAKE, FAKE, FAKE + 4, FAKE, 256, None, 256, 128, keep, 1,
+                             FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert st == 1 and "cos_k is not 16-byte aligned" in err(lib)
+    st = lib.bsa_select_rope(ctypes.byref(q), ctypes.byref(k), FAKE, FAKE, FAKE, FAKE, 256, None, 96, 128, keep, 1,
+                             FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert st == 2 and "block geometry" in err(lib)

@@ -263,6 +263,65 @@ def test_causal_equals_dense_on_last_row():
     assert abs(lse[0, 0, -1].item() - dl[0, 0, -1].item()) <= 1e-5
 
 
+# ------------------------------------------------- rotary prologue fused ---
+
+def _tables(S, d, offset=0, base=10000.0):
+    inv = base ** (-torch.arange(0, d // 2, dtype=torch.float64) * 2.0 / d)
+    ang = torch.outer(torch.arange(offset, offset + S, dtype=torch.float64), inv)
+    ang = torch.cat([ang, ang], dim=1)
+    return ang.cos().float(), ang.sin().float()
+
+
+@pytest.mark.parametrize("name", ["small_gqa", "small_mqa_d64", "small_mha_perhead"])
+def test_select_rope_parity(name):
+    inp = cuda_inputs(name, pad_fill=0.0)
+    c = inp["cfg"]
+    # understanding positions 0..P-1 for the prefix keys, generation positions after
+    cq, sq = _tables(c.Sq, c.d, offset=c.prefix)
+    ck, sk = _tables(c.Skv, c.d)
+    q_out, k_out, idx, cnt = bsa.bsa_select_rope(inp["q"], inp["k"], cq.cuda(), sq.cuda(), ck.cuda(), sk.cuda(),
+                                                 c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    bsa.bsa_device_status()
+    ref = O.rope_then_select(to_f32_np(inp["q"]), to_f32_np(inp["k"]), cq.numpy(), sq.numpy(), ck.numpy(),
+                             sk.numpy(), c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    # rotated tensors: the fp32 rotation differs from the fp64 one by fp32
+    # rounding of the two products (absolute, ~1e-7 of the terms, which
+    # matters where they cancel); after rounding both to bf16 they are at most
+    # one bf16 ulp plus that apart, and almost always identical
+    for got, want, x, cs, sn in ((q_out, ref["q_rot"], inp["q"], cq, sq), (k_out, ref["k_rot"], inp["k"], ck, sk)):
+        g = got.float().cpu().numpy().astype(np.float64)
+        xf = to_f32_np(x).astype(np.float64)
+        terms = np.abs(xf) * np.abs(cs.numpy())[None, :, None, :] + \
+            np.abs(O.rotate_half(xf)) * np.abs(sn.numpy())[None, :, None, :]
+        tol = np.abs(want) * 2.0 ** -7 + terms * 2.0 ** -22
+        assert (np.abs(g - want) <= tol).all(), float(np.max(np.abs(g - want) - tol))
+        assert (g == want).mean() > 0.999
+    stats = compare_selection(idx.cpu().numpy(), cnt.cpu().numpy(), ref)
+    # fused == rotate first, then select on the rotated tensors (bit for bit)
+    idx2, cnt2 = bsa.bsa_select(q_out, k_out, c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    assert torch.equal(cnt, cnt2)
+    for b in range(c.B):
+        for h in range(c.Hq):
+            for qb in range(cnt.shape[2]):
+                n = int(cnt[b, h, qb])
+                assert torch.equal(idx[b, h, qb, :n], idx2[b, h, qb, :n])
+    print(name, stats)
+
+
+def test_select_rope_in_place():
+    inp = cuda_inputs("small_gqa", pad_fill=0.0)
+    c = inp["cfg"]
+    cq, sq = _tables(c.Sq, c.d, offset=c.prefix)
+    ck, sk = _tables(c.Skv, c.d)
+    q1, k1, i1, n1 = bsa.bsa_select_rope(inp["q"], inp["k"], cq.cuda(), sq.cuda(), ck.cuda(), sk.cuda(), c.prefix,
+                                         inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    q, k = inp["q"].clone(), inp["k"].clone()
+    q2, k2, i2, n2 = bsa.bsa_select_rope(q, k, cq.cuda(), sq.cuda(), ck.cuda(), sk.cuda(), c.prefix, inp["seq_lens"],
+                                         c.block_q, c.block_k, inp["keep_ratio"], q_out=q, k_out=k)
+    bsa.bsa_device_status()
+    assert torch.equal(q1, q) and torch.equal(k1, k) and torch.equal(n1, n2)
+
+
 # ----------------------------------------------------------- full size ---
 
 def full_inputs(name):
