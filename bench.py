@@ -64,8 +64,9 @@ def peaks():
 # launch, from an ncu capture of the build whose FMHA sources hash to `sha`.
 # When the sources change the figure no longer applies and traffic is null.
 FMHA_TRAFFIC = {
-    "sha": "5f4490e7be6b60a2",
-    "480p_75": 505897728 + 268969472,     # profiles/fmha_fwd_480p_75.md
+    "sha": "f68df8a7ab548f42",
+    "720p_75": 14.24e9 + 1.78e9,          # profiles/launches_720p_75.md (1-pass capture)
+    "480p_75": 504364544 + 267939072,     # profiles/fmha_fwd_480p_75.md
 }
 
 

@@ -646,24 +646,32 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const __grid_constant__ 
   const int ng = p.Bn * p.Hkv;
   for (int i = threadIdx.x; i < ng; i += blockDim.x) cost[i] = 0ull;
   __syncthreads();
-  // every (group, query head of the group, query block) tile; query blocks
-  // fastest so the count reads are coalesced
+  // Warps split the groups' tiles (query blocks fastest, so count reads are
+  // coalesced); each warp reduces its slice and adds it with one atomic.
   const int per_group = p.G * p.nQb;
-  const int total = ng * per_group;
-  for (int i = threadIdx.x; i < total; i += blockDim.x) {
-    const int gi = i / per_group, w = i - gi * per_group;
-    const int g = w / p.nQb, qb = w - g * p.nQb;
+  const int nwarps = blockDim.x / 32;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int wpg = max(1, nwarps / ng);            // warps per group
+  for (int task = warp; task < ng * wpg; task += nwarps) {
+    const int gi = task / wpg, part = task - gi * wpg;
     const int bl = gi / p.Hkv, hk = gi - bl * p.Hkv;
     const int L = p.seq_lens[bl];
-    const int rows = min(p.block_q, L - qb * p.block_q);
-    if (rows <= 0) continue;
-    const int kv_end = p.causal ? min(p.prefix_len + L, min((qb + 1) * p.block_q, L)) : p.prefix_len + L;
-    int n = (kv_end + p.block_k - 1) / p.block_k;
-    if (p.counts) {
-      n = p.counts[((int64_t)(p.b0 + bl) * p.Hq + hk * p.G + g) * p.nQb + qb];
-      n = n < 0 ? 0 : min(n, p.nKb);
+    unsigned long long c = 0;
+    for (int w = part * 32 + lane; w < per_group; w += 32 * wpg) {
+      const int g = w / p.nQb, qb = w - g * p.nQb;
+      const int rows = min(p.block_q, L - qb * p.block_q);
+      if (rows <= 0) continue;
+      const int kv_end = p.causal ? min(p.prefix_len + L, min((qb + 1) * p.block_q, L)) : p.prefix_len + L;
+      int n = (kv_end + p.block_k - 1) / p.block_k;
+      if (p.counts) {
+        n = p.counts[((int64_t)(p.b0 + bl) * p.Hq + hk * p.G + g) * p.nQb + qb];
+        n = n < 0 ? 0 : min(n, p.nKb);
+      }
+      c += (unsigned long long)rows * (unsigned long long)n;
     }
-    if (n > 0) atomicAdd(&cost[gi], (unsigned long long)rows * (unsigned long long)n);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (lane == 0 && c) atomicAdd(&cost[gi], c);
   }
   __syncthreads();
   for (int i = threadIdx.x; i < ng; i += blockDim.x) {
