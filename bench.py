@@ -428,7 +428,7 @@ def main():
     idx = torch.empty((B, Hq, nQb, nKb), dtype=torch.int32, device="cuda")
     cnt = torch.empty((B, Hq, nQb), dtype=torch.int32, device="cuda")
     ws = torch.empty(bsa.bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, bq, bk), dtype=torch.uint8, device="cuda")
-    fws = torch.empty(max(256, bsa.bsa_forward_workspace_size(B, Hq, Sq, bq)), dtype=torch.uint8, device="cuda")
+    fws = torch.empty(max(256, bsa.bsa_forward_workspace_size(B, Hq, Sq, Skv, bq, bk)), dtype=torch.uint8, device="cuda")
     out = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()

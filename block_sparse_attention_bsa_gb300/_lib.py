@@ -49,7 +49,7 @@ SIGNATURES = {
     "bsa_select_rope": (_I, [_TP, _TP, _P, _P, _P, _P, _I32, _P, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P,
                              _SZ, _P]),
     "bsa_select_noalloc": (_I, [_TP, _TP, _I32, _P, _I32, _I32, _P, _I32, _P, _P, _P]),
-    "bsa_forward_workspace_size": (_SZ, [_I, _I, _I, _I]),
+    "bsa_forward_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "bsa_forward": (_I, [_TP, _TP, _TP, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P, _P,
                          _P, _SZ, _P]),
     "bsa_forward_causal": (_I, [_TP, _TP, _TP, _I32, _I32, ctypes.c_float, _P, _P, _P, _SZ, _P]),

@@ -76,8 +76,8 @@ def bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, block_q, block_k) -> int:
     return int(_lib.load().bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, block_q, block_k))
 
 
-def bsa_forward_workspace_size(B, Hq, Sq, block_q) -> int:
-    return int(_lib.load().bsa_forward_workspace_size(B, Hq, Sq, block_q))
+def bsa_forward_workspace_size(B, Hq, Sq, Skv, block_q, block_k) -> int:
+    return int(_lib.load().bsa_forward_workspace_size(B, Hq, Sq, Skv, block_q, block_k))
 
 
 def _workspace(nbytes: int, device, given: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
@@ -207,7 +207,7 @@ def bsa_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, indices: Opti
     for name, t in (("indices", indices), ("counts", counts)):
         if t is not None and (t.dtype != torch.int32 or not t.is_contiguous() or t.device != q.device):
             raise ValueError(f"{name} must be a contiguous int32 tensor on {q.device}")
-    need = bsa_forward_workspace_size(B, Hq, Sq, block_q)
+    need = bsa_forward_workspace_size(B, Hq, Sq, k.shape[1], block_q, block_k)
     ws = _workspace(need, q.device, workspace)
     lib = _lib.load()
     st = lib.bsa_forward(ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd),
@@ -237,7 +237,7 @@ def bsa_forward_causal(q_und: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bl
         raise ValueError("out must be a contiguous bf16 tensor [B, P, Hq, d]")
     if lse is None and return_lse:
         lse = torch.empty((B, Hq, P), dtype=torch.float32, device=q_und.device)
-    need = bsa_forward_workspace_size(B, Hq, P, block_q)
+    need = bsa_forward_workspace_size(B, Hq, P, k.shape[1], block_q, block_k)
     ws = _workspace(need, q_und.device, workspace)
     st = _lib.load().bsa_forward_causal(ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), int(block_q),
                                         int(block_k), float(softmax_scale), out.data_ptr(),

@@ -252,10 +252,10 @@ bsa_status bsa_select_rope(const bsa_tensor* q, const bsa_tensor* k, const float
                      indices, counts, workspace, ws_bytes, stream, &r);
 }
 
-size_t bsa_forward_workspace_size(int B, int Hq, int Sq, int block_q) {
-  (void)Sq; (void)block_q;
-  if (B <= 0 || Hq <= 0) return 0;
-  return (size_t)cdiv64(B, kMaxFwdBatch) * forward_chunk_bytes(Hq);
+size_t bsa_forward_workspace_size(int B, int Hq, int Sq, int Skv, int block_q, int block_k) {
+  if (B <= 0 || Hq <= 0 || Sq <= 0 || Skv <= 0 || block_q <= 0 || block_k <= 0) return 0;
+  return (size_t)cdiv64(B, kMaxFwdBatch) * forward_chunk_bytes(Hq) +
+         merged_list_bytes(B, Hq, Sq, Skv, block_q, block_k);
 }
 
 bsa_status bsa_forward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tensor* v, const int32_t* indices,
@@ -275,7 +275,7 @@ bsa_status bsa_forward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tenso
     return set_error(BSA_ERR_INVALID_ARG, "bsa_forward: out is not 16-byte aligned");
   if (!(std::isfinite(softmax_scale)))
     return set_error(BSA_ERR_INVALID_ARG, "bsa_forward: softmax_scale is not finite");
-  if ((st = check_workspace(fn, workspace, ws_bytes, bsa_forward_workspace_size((int)q->B, (int)q->H, (int)q->S, block_q))) != BSA_OK)
+  if ((st = check_workspace(fn, workspace, ws_bytes, bsa_forward_workspace_size((int)q->B, (int)q->H, (int)q->S, (int)k->S, block_q, block_k))) != BSA_OK)
     return st;
   ForwardArgs a{};
   a.q = q->ptr; a.q_sb = q->stride_b; a.q_ss = q->stride_s; a.q_sh = q->stride_h;
@@ -307,7 +307,7 @@ bsa_status bsa_forward_causal(const bsa_tensor* q_und, const bsa_tensor* k, cons
   if (!(std::isfinite(softmax_scale)))
     return set_error(BSA_ERR_INVALID_ARG, "bsa_forward_causal: softmax_scale is not finite");
   if ((st = check_workspace(fn, workspace, ws_bytes,
-                            bsa_forward_workspace_size((int)q_und->B, (int)q_und->H, (int)q_und->S, block_q))) != BSA_OK)
+                            bsa_forward_workspace_size((int)q_und->B, (int)q_und->H, (int)q_und->S, (int)k->S, block_q, block_k))) != BSA_OK)
     return st;
   ForwardArgs a{};
   a.q = q_und->ptr; a.q_sb = q_und->stride_b; a.q_ss = q_und->stride_s; a.q_sh = q_und->stride_h;

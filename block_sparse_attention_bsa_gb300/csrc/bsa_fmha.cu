@@ -62,6 +62,8 @@ struct FmhaParams {   // CUtensorMap members make it 128-byte aligned
   int Bn;           // requests in this launch
   int Hq, Hkv, G, Sq, nQb, nKb, block_q, prefix_len, n_tiles;
   int causal;              // 1: query row i sees key positions 0..i only (dense pass)
+  int group_rows;          // merged lists: rows per original query block (64 or 128)
+  int masked;              // 1: list entries are kb | membership << 24 (merged lists)
   const int32_t* indices;  // NULL = dense pass
   const int32_t* counts;
   int* counter;            // next work tile (zeroed by the schedule kernel)
@@ -99,6 +101,11 @@ struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(BK == 64 || BK == 128, "key block");
 };
+
+// Merged-list entries: key block in the low 24 bits, one membership bit per
+// original query block of the 256-row super-block from bit 24.
+constexpr int kEntryBlockMask = (1 << 24) - 1;
+constexpr int kEntryGroupShift = 24;
 
 struct TileInfo {
   int bl, b, qb, h, hk, L, valid_kv, n;
@@ -270,7 +277,8 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       ++qi;
       for (int j0 = 0; j0 < ti.n && ok; j0 += 32) {
-        const int my_kb = ti.idx ? (j0 + lane < ti.n ? __ldg(ti.idx + j0 + lane) : 0) : j0 + lane;
+        int my_kb = ti.idx ? (j0 + lane < ti.n ? __ldg(ti.idx + j0 + lane) : 0) : j0 + lane;
+        if (p.masked) my_kb &= kEntryBlockMask;
         const int m = min(32, ti.n - j0);
         for (int jj = 0; jj < m && ok; ++jj) {
           int kb = __shfl_sync(0xffffffffu, my_kb, jj);
@@ -495,8 +503,12 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       float m_ref = -INFINITY;
       float l = 0.f;
       for (int j = 0; j < ti.n; ++j) {
-        int kb = ti.idx ? __ldg(ti.idx + j) : j;
+        const int entry = ti.idx ? __ldg(ti.idx + j) : j;
+        int kb = (ti.idx && p.masked) ? (entry & kEntryBlockMask) : entry;
         if (kb < 0 || kb >= p.nKb) kb = p.nKb;     // same clamp as the producer: fully masked
+        // merged lists: a key block that this row's own query block did not
+        // select is masked whole (it contributes exact zeros)
+        if (p.masked && !((entry >> (kEntryGroupShift + row_in_blk / p.group_rows)) & 1)) kb = p.nKb;
         ok = mbar_wait(smem_u32(s_full + hh), sph & 1u, abort_flag);
         ++sph;
         if (!ok) break;
@@ -770,6 +782,8 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
     p.indices = a.indices;
     p.counts = a.counts;
     p.causal = a.causal ? 1 : 0;
+    p.masked = a.masked ? 1 : 0;
+    p.group_rows = a.group_rows > 0 ? a.group_rows : a.block_q;
     char* cws = static_cast<char*>(a.workspace) + (size_t)(b0 / kMaxFwdBatch) * forward_chunk_bytes(a.Hq);
     p.counter = reinterpret_cast<int*>(cws);
     p.group_order = reinterpret_cast<const int*>(cws + 256);
@@ -807,12 +821,106 @@ unsigned int read_and_clear_device_error() {
   return v;
 }
 
-bsa_status launch_forward(const ForwardArgs& a, cudaStream_t stream) {
-  const int nh = a.block_q > 128 ? 2 : 1;
-  if (a.d == 128 && a.block_k == 128) return nh == 2 ? launch_t<128, 128, 2>(a, stream) : launch_t<128, 128, 1>(a, stream);
-  if (a.d == 128 && a.block_k == 64) return nh == 2 ? launch_t<128, 64, 2>(a, stream) : launch_t<128, 64, 1>(a, stream);
-  if (a.d == 64 && a.block_k == 128) return nh == 2 ? launch_t<64, 128, 2>(a, stream) : launch_t<64, 128, 1>(a, stream);
-  if (a.d == 64 && a.block_k == 64) return nh == 2 ? launch_t<64, 64, 2>(a, stream) : launch_t<64, 64, 1>(a, stream);
+// ------------------------------------------------------ merged lists ---
+// For query blocks of 64 or 128 rows, the 256/block_q query blocks of each
+// 256-row super-block are attended together: one warp ORs their key-block
+// lists into bitmaps and writes the ascending union with one membership bit
+// per query block (kb | bits << 24).  The forward then runs its 256-row,
+// two-half ping-pong path over the union and masks, per row, the key blocks
+// the row's own query block did not select -- the same result as attending
+// each query block's list alone, with K/V tiles reused by 256 rows.
+struct MergeParams {
+  const int32_t* indices;   // [B, Hq, nQb, nKb]
+  const int32_t* counts;    // [B, Hq, nQb]
+  int32_t* uindices;        // [B, Hq, nSb, nKb]
+  int32_t* ucounts;         // [B, Hq, nSb]
+  int Hq, nQb, nKb, nSb, ratio, words;
+};
+
+__global__ void __launch_bounds__(32) merge_lists_kernel(const __grid_constant__ MergeParams p) {
+  extern __shared__ uint32_t bm[];   // [ratio][words]
+  const int lane = threadIdx.x;
+  const int sb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  for (int i = lane; i < p.ratio * p.words; i += 32) bm[i] = 0u;
+  __syncwarp();
+  for (int g = 0; g < p.ratio; ++g) {
+    const int qb = sb * p.ratio + g;
+    if (qb >= p.nQb) break;
+    const int64_t row = ((int64_t)b * p.Hq + h) * p.nQb + qb;
+    const int c = min(max(p.counts[row], 0), p.nKb);
+    const int32_t* lst = p.indices + row * p.nKb;
+    for (int i = lane; i < c; i += 32) {
+      const int kb = lst[i];
+      if (kb >= 0 && kb < p.nKb) atomicOr(&bm[g * p.words + (kb >> 5)], 1u << (kb & 31));
+    }
+  }
+  __syncwarp();
+  const int64_t srow = ((int64_t)b * p.Hq + h) * p.nSb + sb;
+  int32_t* out = p.uindices + srow * p.nKb;
+  int running = 0;
+  for (int w0 = 0; w0 < p.words; w0 += 32) {
+    const int w = w0 + lane;
+    uint32_t m[4] = {0u, 0u, 0u, 0u};
+    uint32_t u = 0u;
+    if (w < p.words)
+      for (int g = 0; g < p.ratio; ++g) { m[g] = bm[g * p.words + w]; u |= m[g]; }
+    const int cnt = __popc(u);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int pos = running + incl - cnt;
+    while (u) {
+      const int bit = __ffs(u) - 1;
+      u &= u - 1;
+      int mask = 0;
+      for (int g = 0; g < p.ratio; ++g) mask |= (int)((m[g] >> bit) & 1u) << g;
+      out[pos++] = (w * 32 + bit) | (mask << kEntryGroupShift);
+    }
+    running += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) p.ucounts[srow] = running;
+}
+
+size_t merged_list_bytes(int B, int Hq, int Sq, int Skv, int block_q, int block_k) {
+  if (block_q >= 256) return 0;
+  const size_t nSb = (size_t)cdiv64(Sq, 256), nKb = (size_t)cdiv64(Skv, block_k);
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  return al((size_t)B * Hq * nSb * nKb * 4) + al((size_t)B * Hq * nSb * 4);
+}
+
+bsa_status launch_forward(const ForwardArgs& a_in, cudaStream_t stream) {
+  ForwardArgs a = a_in;
+  if (a.block_q < 256) {
+    // 64- and 128-row query blocks run as 256-row super-blocks (see above).
+    const int ratio = 256 / a.block_q;
+    const int nSb = (int)cdiv64(a.Sq, 256);
+    if (a.indices) {
+      char* mws = static_cast<char*>(a.workspace) + forward_chunk_bytes(a.Hq) * (size_t)cdiv64(a.B, kMaxFwdBatch);
+      const size_t ul_bytes = ((size_t)a.B * a.Hq * nSb * a.nKb * 4 + 255) & ~(size_t)255;
+      MergeParams mp{};
+      mp.indices = a.indices; mp.counts = a.counts;
+      mp.uindices = reinterpret_cast<int32_t*>(mws);
+      mp.ucounts = reinterpret_cast<int32_t*>(mws + ul_bytes);
+      mp.Hq = a.Hq; mp.nQb = a.nQb; mp.nKb = a.nKb; mp.nSb = nSb; mp.ratio = ratio;
+      mp.words = (a.nKb + 31) / 32;
+      merge_lists_kernel<<<dim3(nSb, a.Hq, a.B), 32, sizeof(uint32_t) * ratio * mp.words, stream>>>(mp);
+      bsa_status st = cuda_check(cudaGetLastError(), "merge_lists_kernel launch");
+      if (st != BSA_OK) return st;
+      a.indices = mp.uindices;
+      a.counts = mp.ucounts;
+      a.masked = true;
+    }
+    a.group_rows = a.block_q;
+    a.block_q = 256;
+    a.nQb = nSb;
+  }
+  if (a.d == 128 && a.block_k == 128) return launch_t<128, 128, 2>(a, stream);
+  if (a.d == 128 && a.block_k == 64) return launch_t<128, 64, 2>(a, stream);
+  if (a.d == 64 && a.block_k == 128) return launch_t<64, 128, 2>(a, stream);
+  if (a.d == 64 && a.block_k == 64) return launch_t<64, 64, 2>(a, stream);
   return set_error(BSA_ERR_UNSUPPORTED, "bsa_forward: unsupported (d, block_k)");
 }
 

@@ -62,7 +62,11 @@ struct ForwardArgs {
   float* lse;
   void* workspace;           // forward_chunk_bytes(Hq) per chunk of kMaxFwdBatch requests
   bool causal;               // key position <= query row (dense pass over the prefix only)
+  bool masked = false;       // internal: merged lists with membership bits
+  int group_rows = 0;        // internal: rows per original query block of merged lists
 };
+// Workspace bytes of the merged lists used when block_q < 256 (0 otherwise).
+size_t merged_list_bytes(int B, int Hq, int Sq, int Skv, int block_q, int block_k);
 // Workspace bytes per launch chunk: tile counter (256 B) + group order.
 size_t forward_chunk_bytes(int Hq);
 bsa_status launch_forward(const ForwardArgs& a, cudaStream_t stream);

@@ -105,6 +105,10 @@ CONFIGS = {
         lens=(176640, 150000), block_q=256, block_k=128,
         keep=("uniform", 0.10, 0.50), recipe="block", grid=(48, 46, 80),
         seed=1005, description="1280x736 latent (48x46x80), 2 ragged requests, per-head keep"),
+    "480p_75_64x64": Config(
+        "480p_75_64x64", B=1, Hq=24, Hkv=8, d=128, prefix=512, lens=(48360,),
+        block_q=64, block_k=64, keep=0.25, recipe="block", grid=(31, 30, 52),
+        seed=1006, description="480p latent, Hopper 64x64 geometry at d128, keep 25%"),
     # --- small parity cases (oracle in seconds; several tiles + ragged tails) ---
     "small_gqa": Config(
         "small_gqa", B=2, Hq=4, Hkv=2, d=128, prefix=256, lens=(1900, 1333),

@@ -174,9 +174,13 @@ BSA_API bsa_status bsa_select_noalloc(const bsa_tensor* q, const bsa_tensor* k, 
                                       int32_t* indices, int32_t* counts, bsa_stream_t stream);
 
 /* --------------------------------------------------------------- forward ---
- * Workspace bytes bsa_forward needs: per launch chunk of up to 8 requests, a
- * work-tile counter and the order of the (request, KV head) groups. */
-BSA_API size_t bsa_forward_workspace_size(int B, int Hq, int Sq, int block_q);
+ * Workspace bytes bsa_forward (and bsa_forward_causal) need: per launch chunk
+ * of up to 8 requests, a work-tile counter and the order of the (request, KV
+ * head) groups; with block_q of 64 or 128, also the merged key-block lists of
+ * each 256-row super-block (int32 [B, Hq, ceil(Sq/256), nKb] plus counts):
+ * those query blocks are attended 256 rows at a time over the union of their
+ * lists, each row masking the blocks its own query block did not select. */
+BSA_API size_t bsa_forward_workspace_size(int B, int Hq, int Sq, int Skv, int block_q, int block_k);
 
 /* Selected-block attention forward (PR 8335, Purpose: the adapter executes
  * the selection; cosmos_parallel.py cosmos3_cp_attention: non-causal
@@ -192,7 +196,9 @@ BSA_API size_t bsa_forward_workspace_size(int B, int Hq, int Sq, int block_q);
  * indices/counts: device int32 as written by bsa_select, or indices == NULL
  *   for the dense pass (every valid key block; counts is then ignored and may
  *   be NULL).  A count above nKb is clamped to nKb; indices are not checked
- *   here (see bsa_validate_indices); an out-of-range index reads zeros.
+ *   here (see bsa_validate_indices); an out-of-range index reads zeros.  Each
+ *   list must be strictly ascending (as bsa_select writes it): with block_q
+ *   below 256 the lists are merged and a repeated block is attended once.
  * softmax_scale <= 0 selects head_dim^-1/2.
  * out: device bf16 [B, Sq, Hq, d] contiguous.  lse: device fp32 [B, Hq, Sq]
  *   contiguous, or NULL.
@@ -218,7 +224,7 @@ BSA_API bsa_status bsa_forward(const bsa_tensor* q, const bsa_tensor* k, const b
  * out: bf16 [B, P, Hq, d] contiguous; lse: fp32 [B, Hq, P] contiguous or NULL.
  * block_q/block_k: any supported geometry (the key blocks up to the one that
  *   holds a query block's last row are visited; the diagonal is masked per
- *   row).  workspace: bsa_forward_workspace_size(B, Hq, P, block_q) bytes. */
+ *   row).  workspace: bsa_forward_workspace_size(B, Hq, P, Skv, block_q, block_k) bytes. */
 BSA_API bsa_status bsa_forward_causal(const bsa_tensor* q_und, const bsa_tensor* k, const bsa_tensor* v,
                                       int32_t block_q, int32_t block_k, float softmax_scale,
                                       void* out, float* lse, void* workspace, size_t ws_bytes,

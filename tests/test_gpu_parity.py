@@ -187,6 +187,29 @@ def test_strided_views_match_contiguous():
     assert torch.equal(lse, lse2)
 
 
+@pytest.mark.parametrize("name", ["tiny", "small_64x64_d128", "small_mha_perhead"])
+def test_merged_small_query_blocks_match_per_block_lists(name):
+    """64/128-row query blocks run 256 rows at a time over merged lists; each
+    row must see exactly its own query block's list: compare against the
+    oracle and against feeding one query block's list at a time (the other
+    blocks' counts set to 0)."""
+    inp = cuda_inputs(name, pad_fill=0.0)
+    c = inp["cfg"]
+    idx, cnt = run_select(inp)
+    out, lse = run_forward(inp, idx, cnt)
+    ratio = 256 // c.block_q
+    for g in range(ratio):
+        cnt_g = cnt.clone()
+        keep = torch.zeros_like(cnt_g, dtype=torch.bool)
+        keep[:, :, g::ratio] = True
+        cnt_g[~keep] = 0
+        out_g, lse_g = run_forward(inp, idx, cnt_g)
+        for qb in range(g, cnt.shape[2], ratio):
+            r0, r1 = qb * c.block_q, min((qb + 1) * c.block_q, c.Sq)
+            assert torch.equal(out[:, r0:r1], out_g[:, r0:r1])
+            assert torch.equal(lse[:, :, r0:r1], lse_g[:, :, r0:r1])
+
+
 def test_keep_zero_without_prefix_gives_empty_rows():
     inp = cuda_inputs("small_mha_perhead")
     idx, cnt = run_select(inp, keep=[0.0])
@@ -329,7 +352,7 @@ def full_inputs(name):
     return make_inputs(cfg, "cuda", pad_fill=float("nan"))
 
 
-@pytest.mark.parametrize("name", WORKLOAD_CONFIGS)
+@pytest.mark.parametrize("name", list(WORKLOAD_CONFIGS) + ["480p_75_64x64"])
 def test_workload_config_parity(name):
     inp = full_inputs(name)
     c = inp["cfg"]
