@@ -10,6 +10,7 @@ from .bsa_oracle import (  # noqa: F401
     NEAR_TIE_REL,
     apply_rope,
     attention,
+    attention_backward,
     attention_rows,
     attention_tile,
     causal_prefix_attention,

@@ -407,3 +407,61 @@ def rope_then_select(q, k, cos_q, sin_q, cos_k, sin_k, prefix_len, seq_lens, blo
     sel["q_rot"] = q_rot
     sel["k_rot"] = k_rot
     return sel
+
+
+# ---------------------------------------------------------------------------
+# Backward pass of the selected-block attention
+# ---------------------------------------------------------------------------
+
+def attention_backward(q, k, v, out, dout, lse, indices, counts, prefix_len: int,
+                       seq_lens: Sequence[int], block_q: int, block_k: int,
+                       scale: Optional[float] = None):
+    """Gradients of the selected-block attention forward with respect to Q, K, V.
+
+    For every real query row i of tile (b, h, qb) and every key position j it
+    attends (the listed blocks' real keys, KV head h // G), with the stored
+    LSE of the forward:
+        P_ij = exp(scale * q_i.k_j - lse_i),   D_i = sum_c dO_ic O_ic,
+        dV_j += P_ij dO_i,   dS_ij = P_ij (dO_i.v_j - D_i),
+        dQ_i += scale * dS_ij k_j,   dK_j += scale * dS_ij q_i.
+    dK/dV of a KV head sum over every query head of its group and every query
+    block that listed the key's block; keys nobody listed, padded keys and
+    padded query rows get zero gradients.  Returns dq [B, Sq, Hq, d],
+    dk, dv [B, Skv, Hkv, d] (float64).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    out = np.asarray(out, dtype=np.float64)
+    dout = np.asarray(dout, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    B, Sq, Hq, d = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    if scale is None or scale <= 0:
+        scale = default_scale(d)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    nQb = cdiv(Sq, block_q)
+    for b in range(B):
+        L = int(seq_lens[b])
+        for h in range(Hq):
+            hk = h // G
+            for qb in range(nQb):
+                r0, r1 = qb * block_q, min((qb + 1) * block_q, L)
+                if r1 <= r0:
+                    continue
+                c = int(counts[b, h, qb])
+                pos = tile_keys(indices[b, h, qb, :c], prefix_len + L, block_k)
+                if pos.size == 0:
+                    continue
+                qq, oo, gg = q[b, r0:r1, h], out[b, r0:r1, h], dout[b, r0:r1, h]
+                kk, vv = k[b, pos, hk], v[b, pos, hk]
+                p_ = np.exp((qq @ kk.T) * scale - lse[b, h, r0:r1, None])
+                D = (gg * oo).sum(axis=1, keepdims=True)
+                dv[b, pos, hk] += p_.T @ gg
+                ds = p_ * (gg @ vv.T - D)
+                dq[b, r0:r1, h] += scale * ds @ kk
+                dk[b, pos, hk] += scale * ds.T @ qq
+    return dq, dk, dv

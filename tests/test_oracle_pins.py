@@ -533,3 +533,78 @@ def test_rope_then_select_uses_rounded_rotated_inputs():
     # rotation changes the selection (the prologue matters)
     plain = O.select_blocks(q, k, c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
     assert not np.array_equal(plain["indices"], sel["indices"])
+
+
+# ----------------------------------------------------------------- backward ---
+
+def _torch_selected_attention(q, k, v, idx, cnt, P, lens, bq, bk, scale):
+    """Autograd-able fp64 torch version (dense matmuls with a boolean mask of
+    the listed blocks) for the gradient pin."""
+    B, Sq, Hq, d = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    outs = []
+    for b in range(B):
+        L = lens[b]
+        allow = torch.zeros(Hq, Sq, Skv, dtype=torch.bool)
+        for h in range(Hq):
+            for qb in range(O.cdiv(Sq, bq)):
+                r0, r1 = qb * bq, min((qb + 1) * bq, L)
+                for kb in idx[b, h, qb, :cnt[b, h, qb]]:
+                    allow[h, r0:r1, kb * bk:(kb + 1) * bk] = True
+        allow[:, :, P + L:] = False
+        kr = k[b].repeat_interleave(G, dim=1).permute(1, 0, 2)
+        vr = v[b].repeat_interleave(G, dim=1).permute(1, 0, 2)
+        z = (q[b].permute(1, 0, 2) @ kr.transpose(1, 2)) * scale
+        z = z.masked_fill(~allow, float("-inf"))
+        p_ = torch.softmax(z, dim=-1).nan_to_num(0.0)
+        outs.append((p_ @ vr).permute(1, 0, 2))
+    return torch.stack(outs)
+
+
+@pytest.mark.parametrize("cfg", ["small_gqa", "small_mqa_d64"])
+def test_backward_matches_torch_autograd(cfg):
+    inp, q, k, v = _tiny(cfg)
+    c = inp["cfg"]
+    q, k, v = (np.nan_to_num(x) for x in (q, k, v))
+    sel = O.select_blocks(q, k, c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    out, lse = O.attention(q, k, v, sel["indices"], sel["counts"], c.prefix, inp["seq_lens"], c.block_q, c.block_k)
+    rng = np.random.default_rng(21)
+    dout = rng.standard_normal(out.shape)
+    for b, L in enumerate(inp["seq_lens"]):
+        dout[b, L:] = 0.0          # padded rows carry no gradient
+    scale = 1 / math.sqrt(c.d)
+    dq, dk, dv = O.attention_backward(q, k, v, out, dout, lse, sel["indices"], sel["counts"], c.prefix,
+                                      inp["seq_lens"], c.block_q, c.block_k)
+    qt, kt, vt = (torch.from_numpy(x).requires_grad_(True) for x in (q, k, v))
+    ot = _torch_selected_attention(qt, kt, vt, sel["indices"], sel["counts"], c.prefix, inp["seq_lens"],
+                                   c.block_q, c.block_k, scale)
+    np.testing.assert_allclose(ot.detach().numpy()[~np.isnan(out)], out[~np.isnan(out)], rtol=0, atol=1e-12)
+    ot.backward(torch.from_numpy(dout))
+    np.testing.assert_allclose(dq, qt.grad.numpy(), rtol=0, atol=1e-10)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), rtol=0, atol=1e-10)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), rtol=0, atol=1e-10)
+
+
+def test_backward_finite_difference_tiny():
+    rng = np.random.default_rng(22)
+    B, Sq, Hq, Hkv, d, P, bq, bk = 1, 8, 2, 1, 4, 4, 4, 4
+    q, k, v = rng.standard_normal((B, Sq, Hq, d)), rng.standard_normal((B, P + Sq, Hkv, d)), rng.standard_normal((B, P + Sq, Hkv, d))
+    idx = np.array([[[[0, 2, -1], [0, 1, 2]], [[1, -1, -1], [0, 2, -1]]]])
+    cnt = np.array([[[2, 3], [1, 2]]])
+    w = rng.standard_normal((B, Sq, Hq, d))          # loss = sum(w * out)
+    out, lse = O.attention(q, k, v, idx, cnt, P, [Sq], bq, bk)
+    dq, dk, dv = O.attention_backward(q, k, v, out, w, lse, idx, cnt, P, [Sq], bq, bk)
+    eps = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for _ in range(12):
+            i = tuple(rng.integers(0, s) for s in x.shape)
+            xp, xm = x.copy(), x.copy()
+            xp[i] += eps
+            xm[i] -= eps
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xp
+            lp = (w * O.attention(args["q"], args["k"], args["v"], idx, cnt, P, [Sq], bq, bk)[0]).sum()
+            args[name] = xm
+            lm = (w * O.attention(args["q"], args["k"], args["v"], idx, cnt, P, [Sq], bq, bk)[0]).sum()
+            assert abs((lp - lm) / (2 * eps) - g[i]) < 1e-6, (name, i)
