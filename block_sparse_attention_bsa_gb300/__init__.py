@@ -9,6 +9,8 @@ from .api import (  # noqa: F401
     BLOCK_K_SUPPORTED,
     BLOCK_Q_SUPPORTED,
     BsaError,
+    bsa_backward,
+    bsa_backward_workspace_size,
     bsa_device_status,
     bsa_forward,
     bsa_forward_causal,

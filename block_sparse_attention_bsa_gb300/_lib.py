@@ -53,6 +53,9 @@ SIGNATURES = {
     "bsa_forward": (_I, [_TP, _TP, _TP, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P, _P,
                          _P, _SZ, _P]),
     "bsa_forward_causal": (_I, [_TP, _TP, _TP, _I32, _I32, ctypes.c_float, _P, _P, _P, _SZ, _P]),
+    "bsa_backward_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "bsa_backward": (_I, [_TP, _TP, _TP, _TP, _TP, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float,
+                          _P, _P, _P, _P, _SZ, _P]),
     "bsa_validate_indices": (_I, [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
     "bsa_device_status": (_I, [_P]),
 }

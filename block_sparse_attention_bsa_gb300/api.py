@@ -248,6 +248,50 @@ def bsa_forward_causal(q_und: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bl
     return out, lse
 
 
+def bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, block_q, block_k) -> int:
+    return int(_lib.load().bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, block_q, block_k))
+
+
+def bsa_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, dout: torch.Tensor,
+                 lse: torch.Tensor, indices: torch.Tensor, counts: torch.Tensor, prefix_len: int,
+                 seq_lens: Optional[Sequence[int]], block_q: int, block_k: int, softmax_scale: float = 0.0, *,
+                 dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+                 dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Gradients of ``bsa_forward`` with respect to q, k and v, given the
+    forward's ``out`` and ``lse`` and the upstream gradient ``dout``.
+
+    Returns ``(dq [B, Sq, Hq, d], dk [B, Skv, Hkv, d], dv [B, Skv, Hkv, d])``, bf16.
+    """
+    qd, kd, vd = _desc(q, "q"), _desc(k, "k"), _desc(v, "v")
+    od, dod = _desc(out, "out"), _desc(dout, "dout")
+    B, Sq, Hq, d = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    if dq is None:
+        dq = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device=q.device)
+    if dk is None:
+        dk = torch.empty((B, Skv, Hkv, d), dtype=torch.bfloat16, device=q.device)
+    if dv is None:
+        dv = torch.empty((B, Skv, Hkv, d), dtype=torch.bfloat16, device=q.device)
+    for name, t, shape in (("dq", dq, (B, Sq, Hq, d)), ("dk", dk, (B, Skv, Hkv, d)), ("dv", dv, (B, Skv, Hkv, d))):
+        if tuple(t.shape) != shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor {list(shape)}")
+    if tuple(lse.shape) != (B, Hq, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, Sq]")
+    for name, t in (("indices", indices), ("counts", counts)):
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous int32 tensor on {q.device}")
+    need = bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, block_q, block_k)
+    ws = _workspace(need, q.device, workspace)
+    st = _lib.load().bsa_backward(ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), ctypes.byref(od),
+                                  ctypes.byref(dod), lse.data_ptr(), indices.data_ptr(), counts.data_ptr(),
+                                  int(prefix_len), _i32_array(seq_lens), int(block_q), int(block_k),
+                                  float(softmax_scale), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                  ws.data_ptr() if ws is not None else None,
+                                  ws.numel() if ws is not None else 0, _stream_ptr(stream))
+    _check(st)
+    return dq, dk, dv
+
+
 def bsa_validate_indices(indices: torch.Tensor, counts: torch.Tensor, B: int, Hq: int, Sq: int, Skv: int,
                          prefix_len: int, seq_lens: Optional[Sequence[int]], block_q: int, block_k: int,
                          require_prefix: bool = True, stream=None) -> int:

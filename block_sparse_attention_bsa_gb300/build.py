@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbsa.so")
-SOURCES = ("bsa_api.cu", "bsa_select.cu", "bsa_fmha.cu")
+SOURCES = ("bsa_api.cu", "bsa_select.cu", "bsa_fmha.cu", "bsa_bwd.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -326,6 +326,58 @@ bsa_status bsa_forward_causal(const bsa_tensor* q_und, const bsa_tensor* k, cons
   return launch_forward(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t bsa_backward_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int block_q, int block_k) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Sq <= 0 || Skv <= 0 || !supported_geometry(block_q, block_k)) return 0;
+  return backward_workspace_bytes(B, Hq, Hkv, Sq, Skv, block_q, block_k);
+}
+
+bsa_status bsa_backward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tensor* v, const bsa_tensor* out,
+                        const bsa_tensor* dout, const float* lse, const int32_t* indices, const int32_t* counts,
+                        int32_t prefix_len, const int32_t* seq_lens, int32_t block_q, int32_t block_k,
+                        float softmax_scale, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                        bsa_stream_t stream) {
+  clear_error();
+  const char* fn = "bsa_backward";
+  bsa_status st = check_common(fn, q, k, prefix_len, seq_lens, block_q, block_k, kMaxSelectBatch);
+  if (st != BSA_OK) return st;
+  if ((st = check_tensor(v, fn, "v")) != BSA_OK) return st;
+  if ((st = check_tensor(out, fn, "out")) != BSA_OK) return st;
+  if ((st = check_tensor(dout, fn, "dout")) != BSA_OK) return st;
+  if (v->B != k->B || v->S != k->S || v->H != k->H || v->D != k->D)
+    return set_error(BSA_ERR_INVALID_ARG, "bsa_backward: v shape differs from k shape");
+  for (const bsa_tensor* t : {out, dout})
+    if (t->B != q->B || t->S != q->S || t->H != q->H || t->D != q->D)
+      return set_error(BSA_ERR_INVALID_ARG, std::string("bsa_backward: ") + (t == out ? "out" : "dout") +
+                                                " shape differs from q shape");
+  if (q->D != 128 || block_k != 128 || (block_q != 128 && block_q != 256))
+    return set_error(BSA_ERR_UNSUPPORTED, "bsa_backward: supports head dim 128, block_k 128 and block_q 128 or 256; got d=" +
+                                              s(q->D) + ", block_q=" + s(block_q) + ", block_k=" + s(block_k));
+  if (!indices || !counts) return set_error(BSA_ERR_INVALID_ARG, "bsa_backward: indices and counts are required");
+  if (!lse) return set_error(BSA_ERR_INVALID_ARG, "bsa_backward: lse is NULL");
+  if (!dq || !dk || !dv) return set_error(BSA_ERR_INVALID_ARG, "bsa_backward: dq, dk and dv must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15u)
+    return set_error(BSA_ERR_INVALID_ARG, "bsa_backward: dq, dk and dv must be 16-byte aligned");
+  if (!(std::isfinite(softmax_scale)))
+    return set_error(BSA_ERR_INVALID_ARG, "bsa_backward: softmax_scale is not finite");
+  if ((st = check_workspace(fn, workspace, ws_bytes,
+                            backward_workspace_bytes((int)q->B, (int)q->H, (int)k->H, (int)q->S, (int)k->S, block_q,
+                                                     block_k))) != BSA_OK)
+    return st;
+  BackwardArgs a{};
+  a.q = q->ptr; a.q_sb = q->stride_b; a.q_ss = q->stride_s; a.q_sh = q->stride_h;
+  a.k = k->ptr; a.k_sb = k->stride_b; a.k_ss = k->stride_s; a.k_sh = k->stride_h;
+  a.v = v->ptr; a.v_sb = v->stride_b; a.v_ss = v->stride_s; a.v_sh = v->stride_h;
+  a.o = out->ptr; a.o_sb = out->stride_b; a.o_ss = out->stride_s; a.o_sh = out->stride_h;
+  a.dout = dout->ptr; a.d_sb = dout->stride_b; a.d_ss = dout->stride_s; a.d_sh = dout->stride_h;
+  a.lse = lse;
+  a.B = (int)q->B; a.Hq = (int)q->H; a.Hkv = (int)k->H; a.Sq = (int)q->S; a.Skv = (int)k->S;
+  a.block_q = block_q; a.block_k = block_k; a.prefix_len = prefix_len;
+  a.seq_lens = seq_lens; a.indices = indices; a.counts = counts;
+  a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)q->D);
+  a.dq = dq; a.dk = dk; a.dv = dv; a.workspace = workspace;
+  return launch_backward(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 bsa_status bsa_validate_indices(const int32_t* indices, const int32_t* counts, int32_t B, int32_t Hq, int32_t Sq,
                                 int32_t Skv, int32_t prefix_len, const int32_t* seq_lens, int32_t block_q,
                                 int32_t block_k, int32_t require_prefix, int32_t* bad_rows, bsa_stream_t stream) {

@@ -71,6 +71,25 @@ size_t merged_list_bytes(int B, int Hq, int Sq, int Skv, int block_q, int block_
 size_t forward_chunk_bytes(int Hq);
 bsa_status launch_forward(const ForwardArgs& a, cudaStream_t stream);
 
+// ---- backward (bsa_bwd.cu) ----
+struct BackwardArgs {
+  const void* q; int64_t q_sb, q_ss, q_sh;
+  const void* k; int64_t k_sb, k_ss, k_sh;
+  const void* v; int64_t v_sb, v_ss, v_sh;
+  const void* o; int64_t o_sb, o_ss, o_sh;
+  const void* dout; int64_t d_sb, d_ss, d_sh;
+  const float* lse;          // [B, Hq, Sq]
+  int B, Hq, Hkv, Sq, Skv, block_q, block_k, prefix_len;
+  const int32_t* seq_lens;   // host, B values
+  const int32_t* indices;
+  const int32_t* counts;
+  float scale;
+  void* dq; void* dk; void* dv;
+  void* workspace;
+};
+size_t backward_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int block_q, int block_k);
+bsa_status launch_backward(const BackwardArgs& a, cudaStream_t stream);
+
 // Device error word of the current device (0xFFFFFFFF if it cannot be read);
 // cleared after reading.
 unsigned int read_and_clear_device_error();

@@ -79,6 +79,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait that ignores the abort flag, for the way out of a kernel: a
+// producer lets its own TMA copies land (and the MMA thread its own MMAs
+// finish) before the CTA frees TMEM and exits.  Returns immediately when the
+// phase already completed, as it has in every run that did not abort.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      atomicOr(&g_bsa_error, kErrTimeout);
+      return;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ TMA ---
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {

@@ -230,6 +230,38 @@ BSA_API bsa_status bsa_forward_causal(const bsa_tensor* q_und, const bsa_tensor*
                                       void* out, float* lse, void* workspace, size_t ws_bytes,
                                       bsa_stream_t stream);
 
+/* -------------------------------------------------------------- backward ---
+ * Gradients of bsa_forward's output (the pages run inference only; this is
+ * the plain derivative of the attention that PR 8335, Purpose, and
+ * cosmos_parallel.py cosmos3_cp_attention define, over the same lists).
+ * With z_ij = scale q_i.k_j over the keys row i attends, P = softmax(z),
+ * D_i = sum_c dO_ic O_ic and dS_ij = P_ij (dO_i.v_j - D_i):
+ *   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i,
+ *   dV_j = sum_i P_ij dO_i,
+ * where dK_j/dV_j sum over every query head of j's KV group and every query
+ * row whose list holds j's block.  P is recomputed from `lse`, so q, k, v,
+ * indices, counts and lse must be the ones the forward used, and out its
+ * output.  Results do not depend on scheduling: no atomics touch dQ/dK/dV.
+ *
+ * Supported: head dim 128, block_k 128, block_q 128 or 256 (others return
+ *   BSA_ERR_UNSUPPORTED); indices/counts are required (dense lists come from
+ *   bsa_select with keep_ratio 1).
+ * q, k, v, out, dout: bf16 descriptors as in bsa_forward; out and dout have
+ *   q's shape.  lse: device fp32 [B, Hq, Sq] contiguous from bsa_forward.
+ * dq: device bf16 [B, Sq, Hq, d]; dk, dv: device bf16 [B, Skv, Hkv, d]; all
+ *   contiguous and fully written (padded rows and keys no query reads get 0).
+ * workspace: device, >= bsa_backward_workspace_size(...) bytes, 256-B
+ *   aligned; it holds D, the key-block -> query-block lists and their bitmaps.
+ * Gradient buffers may not alias any input. */
+BSA_API size_t bsa_backward_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int block_q, int block_k);
+BSA_API bsa_status bsa_backward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tensor* v,
+                                const bsa_tensor* out, const bsa_tensor* dout, const float* lse,
+                                const int32_t* indices, const int32_t* counts,
+                                int32_t prefix_len, const int32_t* seq_lens,
+                                int32_t block_q, int32_t block_k, float softmax_scale,
+                                void* dq, void* dk, void* dv,
+                                void* workspace, size_t ws_bytes, bsa_stream_t stream);
+
 /* ------------------------------------------------------------ validation ---
  * Debug check of index lists (PR 8335, Purpose: provider failures propagate
  * as errors).  Counts the rows (b, h, qb) whose list is malformed: count

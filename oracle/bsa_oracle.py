@@ -415,7 +415,7 @@ def rope_then_select(q, k, cos_q, sin_q, cos_k, sin_k, prefix_len, seq_lens, blo
 
 def attention_backward(q, k, v, out, dout, lse, indices, counts, prefix_len: int,
                        seq_lens: Sequence[int], block_q: int, block_k: int,
-                       scale: Optional[float] = None):
+                       scale: Optional[float] = None, tiles: Optional[Iterable[tuple]] = None):
     """Gradients of the selected-block attention forward with respect to Q, K, V.
 
     For every real query row i of tile (b, h, qb) and every key position j it
@@ -427,7 +427,9 @@ def attention_backward(q, k, v, out, dout, lse, indices, counts, prefix_len: int
     dK/dV of a KV head sum over every query head of its group and every query
     block that listed the key's block; keys nobody listed, padded keys and
     padded query rows get zero gradients.  Returns dq [B, Sq, Hq, d],
-    dk, dv [B, Skv, Hkv, d] (float64).
+    dk, dv [B, Skv, Hkv, d] (float64).  ``tiles``: iterable of (b, h, qb) to
+    process (default all); dQ of those tiles is then complete, while dK/dV
+    hold only their contributions.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -444,24 +446,24 @@ def attention_backward(q, k, v, out, dout, lse, indices, counts, prefix_len: int
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     nQb = cdiv(Sq, block_q)
-    for b in range(B):
+    if tiles is None:
+        tiles = [(b, h, qb) for b in range(B) for h in range(Hq) for qb in range(nQb)]
+    for (b, h, qb) in tiles:
         L = int(seq_lens[b])
-        for h in range(Hq):
-            hk = h // G
-            for qb in range(nQb):
-                r0, r1 = qb * block_q, min((qb + 1) * block_q, L)
-                if r1 <= r0:
-                    continue
-                c = int(counts[b, h, qb])
-                pos = tile_keys(indices[b, h, qb, :c], prefix_len + L, block_k)
-                if pos.size == 0:
-                    continue
-                qq, oo, gg = q[b, r0:r1, h], out[b, r0:r1, h], dout[b, r0:r1, h]
-                kk, vv = k[b, pos, hk], v[b, pos, hk]
-                p_ = np.exp((qq @ kk.T) * scale - lse[b, h, r0:r1, None])
-                D = (gg * oo).sum(axis=1, keepdims=True)
-                dv[b, pos, hk] += p_.T @ gg
-                ds = p_ * (gg @ vv.T - D)
-                dq[b, r0:r1, h] += scale * ds @ kk
-                dk[b, pos, hk] += scale * ds.T @ qq
+        hk = h // G
+        r0, r1 = qb * block_q, min((qb + 1) * block_q, L)
+        if r1 <= r0:
+            continue
+        c = int(counts[b, h, qb])
+        pos = tile_keys(indices[b, h, qb, :c], prefix_len + L, block_k)
+        if pos.size == 0:
+            continue
+        qq, oo, gg = q[b, r0:r1, h], out[b, r0:r1, h], dout[b, r0:r1, h]
+        kk, vv = k[b, pos, hk], v[b, pos, hk]
+        p_ = np.exp((qq @ kk.T) * scale - lse[b, h, r0:r1, None])
+        D = (gg * oo).sum(axis=1, keepdims=True)
+        dv[b, pos, hk] += p_.T @ gg
+        ds = p_ * (gg @ vv.T - D)
+        dq[b, r0:r1, h] += scale * ds @ kk
+        dk[b, pos, hk] += scale * ds.T @ qq
     return dq, dk, dv

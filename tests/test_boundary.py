@@ -32,6 +32,7 @@ def test_header_declares_the_expected_calls():
         "bsa_version", "bsa_get_last_error", "bsa_select_workspace_size", "bsa_select",
         "bsa_forward_workspace_size", "bsa_forward", "bsa_validate_indices", "bsa_device_status",
         "bsa_select_noalloc", "bsa_forward_causal", "bsa_select_rope",
+        "bsa_backward_workspace_size", "bsa_backward",
     ])
 
 
@@ -231,3 +232,66 @@ def test_select_rope_rejects_missing_tables(lib):
     st = lib.bsa_select_rope(ctypes.byref(q), ctypes.byref(k), FAKE, FAKE, FAKE, FAKE, 256, None, 96, 128, keep, 1,
                              FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
     assert st == 2 and "block geometry" in err(lib)
+
+
+def call_backward(lib, q, k, v, o=None, do=None, lse=FAKE, ind=FAKE, cnt=FAKE, prefix=0, lens=None, bq=256,
+                  bk=128, scale=0.0, dq=FAKE, dk=FAKE, dv=FAKE, ws=FAKE, ws_bytes=1 << 40):
+    o = q if o is None else o
+    do = q if do is None else do
+    lens_arr = (ctypes.c_int32 * len(lens))(*lens) if lens is not None else None
+    return lib.bsa_backward(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(o), ctypes.byref(do),
+                            lse, ind, cnt, prefix, lens_arr, bq, bk, scale, dq, dk, dv, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("case,status,needle", [
+    ("head_dim64", 2, "head dim 128"),
+    ("block_q64", 2, "block_q 128 or 256"),
+    ("block_k64", 2, "block_k 128"),
+    ("dout_shape", 1, "dout shape"),
+    ("out_shape", 1, "out shape"),
+    ("no_indices", 1, "indices and counts are required"),
+    ("no_lse", 1, "lse is NULL"),
+    ("dq_null", 1, "must be non-NULL"),
+    ("dk_align", 1, "16-byte aligned"),
+    ("scale_inf", 1, "softmax_scale"),
+    ("workspace_small", 3, "smaller than"),
+])
+def test_backward_rejects_bad_arguments(lib, case, status, needle):
+    q, k, v = T(H=4), T(H=2, S=768), T(H=2, S=768)
+    kw = dict(prefix=256)
+    if case == "head_dim64":
+        q, k, v = T(H=4, D=64), T(H=2, S=768, D=64), T(H=2, S=768, D=64)
+    elif case == "block_q64":
+        kw["bq"] = 64
+    elif case == "block_k64":
+        kw["bk"] = 64
+    elif case == "dout_shape":
+        kw["do"] = T(H=4, S=256)
+    elif case == "out_shape":
+        kw["o"] = T(H=2)
+    elif case == "no_indices":
+        kw["ind"] = None
+    elif case == "no_lse":
+        kw["lse"] = None
+    elif case == "dq_null":
+        kw["dq"] = None
+    elif case == "dk_align":
+        kw["dk"] = FAKE + 4
+    elif case == "scale_inf":
+        kw["scale"] = float("inf")
+    elif case == "workspace_small":
+        kw["ws_bytes"] = 1024
+    st = call_backward(lib, q, k, v, **kw)
+    assert st == status, (case, st, err(lib))
+    assert needle in err(lib), err(lib)
+
+
+def test_backward_workspace_size_formula(lib):
+    # D [B,Hq,Sq] fp32, bitmaps [B,Hkv,G*nQb,ceil(nKb/32)] u32, inverse counts [B,Hkv,nKb] and
+    # lists [B,Hkv,nKb,G*nQb] int32, each rounded up to 256 B
+    B, Hq, Hkv, Sq, Skv, bq, bk = 1, 32, 8, 172800, 173824, 256, 128
+    r = lambda x: ((x + 255) // 256) * 256
+    nQb, nKb, G = 675, 1358, 4
+    want = r(B * Hq * Sq * 4) + r(B * Hkv * G * nQb * 43 * 4) + r(B * Hkv * nKb * 4) + r(B * Hkv * nKb * G * nQb * 4)
+    assert lib.bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, bq, bk) == want
+    assert lib.bsa_backward_workspace_size(B, Hq, 5, Sq, Skv, bq, bk) == 0
