@@ -16,8 +16,11 @@
 //    (an inverse list built from bitmaps, ordered by query tile) and
 //    accumulates dK and dV in TMEM (S^T = K Q^T, dP^T = V dO^T,
 //    dV += P^T dO, dK += dS^T Q).
-// Both use TMA tile loads, one MMA-issuing thread and one 128-thread
-// warpgroup for the elementwise part; every wait is bounded.
+// Each 128 x 128 score tile is computed as two 64-wide halves in separate
+// TMEM buffers, handled by two elementwise warpgroups, so that one half's
+// exponentials overlap the other half's MMAs (the issue order is
+// SS(h0), TS(prev h1), SS(h1), TS(h0), ...).  TMA tile loads, one
+// MMA-issuing thread, every wait bounded.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -36,7 +39,9 @@ constexpr int kBKb = 128;               // key block
 constexpr int kT = 128;                 // query tile rows
 constexpr int kChunk = 128 * 128;       // 128 rows x 64 bf16 (one 128-byte column chunk)
 constexpr int kTile = 2 * kChunk;       // 128 rows x 128 bf16 = 32 KB
-constexpr int kThreads = 256;           // warp 0 TMA, warp 1 MMA, warps 4..7 elementwise
+constexpr int kHalfRows = 64 * 128;     // byte offset of row 64 inside a chunk
+constexpr int kRowStat = 2 * kT * 4;    // per query tile: -lse * log2(e) [128], -D [128]
+constexpr int kThreads = 384;           // warp 0 TMA, warp 1 MMA, warps 4..7 / 8..11 elementwise halves
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdParams {
@@ -48,8 +53,8 @@ struct BwdParams {
   int b0, Bn, Hq, Hkv, G, Sq, Skv, nQb, nKb, nQt, block_q, prefix_len, n_items;
   const int32_t* indices;     // [B, Hq, nQb, nKb]
   const int32_t* counts;      // [B, Hq, nQb]
-  const float* lse;           // [B, Hq, Sq]
-  const float* Dd;            // [B, Hq, Sq]
+  const float* rowstat;       // [B, Hq, nQt, 2, 128]: -lse * log2(e) (-inf on padded rows), -D
+  int* counter;               // next dK/dV item (zeroed before the launch)
   const int32_t* inv_cnt;     // [B, Hkv, nKb]
   const int32_t* inv_list;    // [B, Hkv, nKb, G * nQb]: listing rows g * nQb + qb, ascending
   float scale, scale_log2;
@@ -65,9 +70,23 @@ struct Ring2 {
   }
 };
 
+// Two-slot ring through which the producer hands the item ids it takes from
+// the global counter to the other roles (-1 ends the loop).
+struct ItemRing {
+  Ring2 r;
+  __device__ __forceinline__ int take(uint64_t* full, uint64_t* empty, volatile int* ids, volatile int* abort,
+                                      bool& ok) {
+    ok = mbar_wait(smem_u32(full + r.stage), r.phase, abort);
+    const int t = ok ? ids[r.stage] : -1;
+    if (ok) mbar_arrive(smem_u32(empty + r.stage));
+    r.next();
+    return t;
+  }
+};
+
 // Descriptor helpers for the 128 x 128 bf16 tiles (two 128-byte swizzled
 // column chunks of 16 KB): K-major use (rows are M or N, channels are K) and
-// MN-major use (channels are N, rows are K).
+// MN-major use (channels are N, rows are K, 16 rows per K step).
 __device__ __forceinline__ uint64_t kmaj(uint32_t tile, int kk) {
   return sdesc_sw128(tile + (kk / 4) * kChunk + (kk % 4) * 32, 16, 1024);
 }
@@ -75,7 +94,26 @@ __device__ __forceinline__ uint64_t mnmaj(uint32_t tile, int kk) {
   return sdesc_sw128(tile + kk * 16 * 128, kChunk, 1024);
 }
 
+// 128 bf16 of a row written as zeros.
+__device__ __forceinline__ void zero_row(__nv_bfloat16* row, int c0, int n) {
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = c0 / 8; i < (c0 + n) / 8; ++i) reinterpret_cast<uint4*>(row)[i] = z;
+}
+
+// 32 fp32 accumulator columns -> 32 bf16 at dst (times mul), or zeros.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* o, float mul, bool keep) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = keep ? pack_bf16x2(o[2 * i] * mul, o[2 * i + 1] * mul) : 0u;
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+
 // ---------------------------------------------------------------- dQ ---
+// TMEM: half h of the key block in columns [128 h, 128 h + 128): S in the
+// first 64 (dS bf16 over its first 32 once computed), dP in the next 64;
+// dQ accumulates in [256, 384).
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -86,24 +124,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + 2 * 2 * kTile);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* s_full = bars + 2;
-  uint64_t* ds_full = bars + 3;
-  uint64_t* dq_full = bars + 4;
-  uint64_t* kv_full = bars + 5;           // [2]
-  uint64_t* kv_empty = bars + 7;          // [2]
-  uint64_t* mma_done = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* s_full = bars + 2;            // [2] per half
+  uint64_t* ds_full = bars + 4;           // [2]
+  uint64_t* dq_full = bars + 6;
+  uint64_t* acc_empty = bars + 7;
+  uint64_t* kv_full = bars + 8;           // [2]
+  uint64_t* kv_empty = bars + 10;         // [2]
+  uint64_t* mma_done = bars + 12;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
     mbar_init(smem_u32(q_empty), 1);
-    mbar_init(smem_u32(s_full), 1);
-    mbar_init(smem_u32(ds_full), 128);
     mbar_init(smem_u32(dq_full), 1);
+    mbar_init(smem_u32(acc_empty), 256);
     mbar_init(smem_u32(mma_done), 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(s_full + i), 1);
+      mbar_init(smem_u32(ds_full + i), 128);
       mbar_init(smem_u32(kv_full + i), 1);
       mbar_init(smem_u32(kv_empty + i), 1);
     }
@@ -117,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;       // S cols [0,128), dP [128,256), dQ [256,384)
+  const uint32_t tmem = *tmem_slot;
 
   // item -> (request, KV head, query tile, query head of the group)
   auto decode = [&](int t, int& bl, int& h, int& qt, int& qb, int& n, int& L) {
@@ -184,44 +224,71 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA ---
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false);
       constexpr uint32_t idesc_mn = idesc_bf16_f32(128, 128, true);
       Ring2 ring;
-      uint32_t qi = 0, di = 0;
+      uint32_t qi = 0, ai = 0, dc[2] = {0u, 0u};
       bool ok = true;
       const uint32_t qa = smem_u32(q_s), da = smem_u32(do_s), kva = smem_u32(kv_s);
+      // S_h = Q K_h^T, dP_h = dO V_h^T over the 64 keys of half h
+      auto issue_ss = [&](uint32_t kt, int h) {
+        const uint32_t vt = kt + kTile;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + h * 128, kmaj(qa, kk), kmaj(kt + h * kHalfRows, kk), idesc_s, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + h * 128 + 64, kmaj(da, kk), kmaj(vt + h * kHalfRows, kk), idesc_s, kk > 0);
+        mma_commit(smem_u32(s_full + h));
+      };
+      // dQ += dS_h K_h  (dS bf16 in TMEM, K rows of half h as the MN-major B)
+      auto issue_ts = [&](uint32_t kt, int h, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + 256, tmem + h * 128 + kk * 8, mnmaj(kt, h * 4 + kk), idesc_mn,
+                 (first && kk == 0) ? 0u : 1u);
+      };
+      auto wait_ds = [&](int h) {
+        const bool r = mbar_wait(smem_u32(ds_full + h), dc[h] & 1u, abort_flag);
+        ++dc[h];
+        if (r) tc_fence_after();
+        return r;
+      };
       for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
         int bl, h, qt, qb, n, L;
         decode(t, bl, h, qt, qb, n, L);
         if (n == 0) continue;
-        ok = mbar_wait(smem_u32(q_full), qi & 1u, abort_flag);
+        ok = mbar_wait(smem_u32(acc_empty), (ai & 1u) ^ 1u, abort_flag);    // last epilogue read dQ
+        ++ai;
+        if (ok) ok = mbar_wait(smem_u32(q_full), qi & 1u, abort_flag);
         ++qi;
         if (!ok) break;
+        uint32_t prev_kt = 0, prev_st = 0;
         for (int j = 0; j < n && ok; ++j) {
           const uint32_t st = ring.stage;
           ok = mbar_wait(smem_u32(kv_full + st), ring.phase, abort_flag);
           ring.next();
           if (!ok) break;
           tc_fence_after();
-          const uint32_t kt = kva + st * 2 * kTile, vt = kt + kTile;
-          // S = Q K^T, dP = dO V^T
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem, kmaj(qa, kk), kmaj(kt, kk), idesc_s, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem + 128, kmaj(da, kk), kmaj(vt, kk), idesc_s, kk > 0);
-          mma_commit(smem_u32(s_full));
+          const uint32_t kt = kva + st * 2 * kTile;
+          issue_ss(kt, 0);
+          if (j > 0) {
+            if (!(ok = wait_ds(1))) break;
+            issue_ts(prev_kt, 1, false);
+            mma_commit(smem_u32(kv_empty + prev_st));
+          }
+          issue_ss(kt, 1);
           if (j == n - 1) mma_commit(smem_u32(q_empty));
-          ok = mbar_wait(smem_u32(ds_full), di & 1u, abort_flag);
-          ++di;
-          if (!ok) break;
-          tc_fence_after();
-          // dQ += dS K  (dS bf16 in TMEM over S's first 64 columns; K as MN-major B)
-#pragma unroll
-          for (int kk = 0; kk < kBKb / 16; ++kk)
-            mma_ts(tmem + 256, tmem + kk * 8, mnmaj(kt, kk), idesc_mn, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(smem_u32(kv_empty + st));
-          if (j == n - 1) mma_commit(smem_u32(dq_full));
+          if (!(ok = wait_ds(0))) break;
+          issue_ts(kt, 0, j == 0);
+          prev_kt = kt;
+          prev_st = st;
         }
+        if (!ok) break;
+        if (!(ok = wait_ds(1))) break;
+        issue_ts(prev_kt, 1, false);
+        mma_commit(smem_u32(kv_empty + prev_st));
+        mma_commit(smem_u32(dq_full));
       }
       mma_commit(smem_u32(mma_done));        // every MMA issued above has finished
       mbar_drain(smem_u32(mma_done), 0);
@@ -229,9 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     __syncwarp();
   } else if (warp >= 4) {
     // ----------------------------------------------------- elementwise ---
+    const int half = (warp - 4) / 4;        // 0: keys 0..63 of a block, 1: keys 64..127
     const int wq = warp % 4;
     const int r = wq * 32 + lane;
-    const uint32_t lb = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tb = tmem + (static_cast<uint32_t>(wq * 32) << 16) + half * 128;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(wq * 32) << 16) + 256;
     uint32_t si = 0, oi = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
@@ -243,47 +312,51 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       const bool row_ok = row < L;
       __nv_bfloat16* drow = p.dq + (((int64_t)b * p.Sq + row) * p.Hq + h) * kD;
       if (n == 0) {
-        if (row_exists) {
-          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int i = 0; i < kD / 8; ++i) reinterpret_cast<uint4*>(drow)[i] = z;
-        }
+        if (row_exists) zero_row(drow, half * 64, 64);
         continue;
       }
-      const int64_t li = ((int64_t)b * p.Hq + h) * p.Sq + row;
-      const float lse2 = row_ok ? __ldg(p.lse + li) * kLog2e : 0.f;
-      const float Dr = row_ok ? __ldg(p.Dd + li) : 0.f;
+      const float* rs = p.rowstat + (((int64_t)b * p.Hq + h) * p.nQt + qt) * (2 * kT);
+      const float nl = __ldg(rs + r);         // -lse log2(e); -inf on padded rows: P = 0
+      const float nD = __ldg(rs + kT + r);
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nl2 = make_float2(nl, nl);
+      const float2 nD2 = make_float2(nD, nD);
       const int valid_kv = p.prefix_len + L;
       const int32_t* lst = p.indices + (((int64_t)b * p.Hq + h) * p.nQb + qb) * p.nKb;
       for (int j = 0; j < n; ++j) {
         int kb = __ldg(lst + j);
         if (kb < 0 || kb >= p.nKb) kb = p.nKb;
-        const int kvalid = row_ok ? valid_kv - kb * kBKb : 0;
-        ok = mbar_wait(smem_u32(s_full), si & 1u, abort_flag);
+        const int kvalid = valid_kv - kb * kBKb - half * 64;    // keys of this half below the end
+        ok = mbar_wait(smem_u32(s_full + half), si & 1u, abort_flag);
         ++si;
         if (!ok) break;
         tc_fence_after();
+        // dS = P (dP - D), P = 2^(S scale log2(e) - lse log2(e)); keys past
+        // the end of the sequence (only in a block holding it) get P = 0
+        const bool all_valid = kvalid >= 64;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          float s[64], dp[64];
-          tmem_ld32f(tmem + lb + h2 * 64, s);
-          tmem_ld32f(tmem + lb + h2 * 64 + 32, s + 32);
-          tmem_ld32f(tmem + lb + 128 + h2 * 64, dp);
-          tmem_ld32f(tmem + lb + 128 + h2 * 64 + 32, dp + 32);
+        for (int c = 0; c < 2; ++c) {
+          float s[32], dp[32];
+          tmem_ld32f(tb + c * 32, s);
+          tmem_ld32f(tb + 64 + c * 32, dp);
           tmem_wait_ld();
-          uint32_t pk[32];
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c0 = h2 * 64 + 2 * i;
-            const float p0 = (c0 < kvalid) ? ex2_approx(fmaf(s[2 * i], p.scale_log2, -lse2)) : 0.f;
-            const float p1 = (c0 + 1 < kvalid) ? ex2_approx(fmaf(s[2 * i + 1], p.scale_log2, -lse2)) : 0.f;
-            pk[i] = pack_bf16x2(p0 * (dp[2 * i] - Dr), p1 * (dp[2 * i + 1] - Dr));
+          for (int i = 0; i < 16; ++i) {
+            const float2 t = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), sc2, nl2);
+            float2 pr = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            if (!all_valid) {
+              const int c0 = c * 32 + 2 * i;
+              pr.x = c0 < kvalid ? pr.x : 0.f;
+              pr.y = c0 + 1 < kvalid ? pr.y : 0.f;
+            }
+            const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(dp[2 * i], dp[2 * i + 1]), nD2));
+            pk[i] = pack_bf16x2(ds.x, ds.y);
           }
-          tmem_st32(tmem + lb + h2 * 32, pk);
+          tmem_st16(tb + c * 16, pk);
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(ds_full));
+        mbar_arrive(smem_u32(ds_full + half));
       }
       if (!ok) break;
       ok = mbar_wait(smem_u32(dq_full), oi & 1u, abort_flag);
@@ -291,21 +364,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float o[32];
-        tmem_ld32f(tmem + lb + 256 + c * 32, o);
+        tmem_ld32f(tq + half * 64 + c * 32, o);
         tmem_wait_ld();
-        if (row_exists) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = row_ok ? pack_bf16x2(o[2 * i] * p.scale, o[2 * i + 1] * p.scale) : 0u;
-          uint4* dst = reinterpret_cast<uint4*>(drow + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+        if (row_exists) store_row32(drow + half * 64 + c * 32, o, p.scale, row_ok);
       }
       tc_fence_before();
+      mbar_arrive(smem_u32(acc_empty));
     }
   }
   tc_fence_before();
@@ -317,39 +383,48 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 }
 
 // ------------------------------------------------------------- dK, dV ---
+// TMEM: half h of the query tile (rows 64 h .. 64 h + 63) in columns
+// [128 h, 128 h + 128): S^T in the first 64 (P^T bf16 over its first 32
+// once computed), dP^T in the next 64 (dS^T bf16 over its first 32);
+// dV accumulates in [256, 384), dK in [384, 512).
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  constexpr int kStage = 2 * kTile + kRowStat;   // Q tile, dO tile, lse/D of its rows
   uint8_t* k_s = smem;                    // K tile of the key block
   uint8_t* v_s = smem + kTile;            // V tile
-  uint8_t* qdo_s = smem + 2 * kTile;      // 2 stages of (Q tile, dO tile)
-  float* rowv = reinterpret_cast<float*>(qdo_s + 2 * 2 * kTile);   // [2][2][128]: lse*log2e, D
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rowv + 2 * 2 * kT);
+  uint8_t* qdo_s = smem + 2 * kTile;      // 2 stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qdo_s + 2 * kStage);
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
-  uint64_t* s_full = bars + 2;
-  uint64_t* p_full = bars + 3;
-  uint64_t* acc_full = bars + 4;
-  uint64_t* qdo_full = bars + 5;          // [2]
-  uint64_t* qdo_empty = bars + 7;         // [2]
-  uint64_t* row_ready = bars + 9;         // [2]: lse/D of a step staged in smem
-  uint64_t* mma_done = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* s_full = bars + 2;            // [2] per half
+  uint64_t* p_full = bars + 4;            // [2]
+  uint64_t* acc_full = bars + 6;
+  uint64_t* acc_empty = bars + 7;
+  uint64_t* qdo_full = bars + 8;          // [2]
+  uint64_t* qdo_empty = bars + 10;        // [2]
+  uint64_t* mma_done = bars + 12;
+  uint64_t* item_full = bars + 13;        // [2] item-id ring
+  uint64_t* item_empty = bars + 15;       // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* item_ids = reinterpret_cast<volatile int*>(tmem_slot + 2);   // [2]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(kv_full), 1);
     mbar_init(smem_u32(kv_empty), 1);
-    mbar_init(smem_u32(s_full), 1);
-    mbar_init(smem_u32(p_full), 128);
     mbar_init(smem_u32(acc_full), 1);
+    mbar_init(smem_u32(acc_empty), 256);
     mbar_init(smem_u32(mma_done), 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(s_full + i), 1);
+      mbar_init(smem_u32(p_full + i), 128);
       mbar_init(smem_u32(qdo_full + i), 1);
       mbar_init(smem_u32(qdo_empty + i), 1);
-      mbar_init(smem_u32(row_ready + i), 128);
+      mbar_init(smem_u32(item_full + i), 1);
+      mbar_init(smem_u32(item_empty + i), 1 + 256);    // MMA thread + elementwise threads
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -361,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;       // S^T [0,128), dP^T [128,256), dV [256,384), dK [384,512)
+  const uint32_t tmem = *tmem_slot;
   const int tiles_per_block = p.block_q / kT;
 
   // item -> (request, KV head, key block); steps = listed query blocks x tiles per block
@@ -384,11 +459,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 
   if (warp == 0) {
     if (lane == 0) {
-      Ring2 ring;
+      Ring2 ring, items;
       uint32_t ki = 0;
       int kv_armed = -1, qdo_armed[2] = {-1, -1};   // parity of each barrier's last arming
       bool ok = true;
-      for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+      while (ok) {
+        // dynamic scheduling: the next item from the counter, published to the other roles
+        int t = atomicAdd(p.counter, 1);
+        if (t >= p.n_items) t = -1;
+        ok = mbar_wait(smem_u32(item_empty + items.stage), items.phase ^ 1u, abort_flag);
+        if (!ok) break;
+        item_ids[items.stage] = t;
+        mbar_arrive(smem_u32(item_full + items.stage));
+        items.next();
+        if (t < 0) break;
         int bl, hk, kb, steps;
         const int32_t* lst;
         decode(t, bl, hk, kb, steps, lst);
@@ -408,13 +492,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
           ok = mbar_wait(smem_u32(qdo_empty + ring.stage), ring.phase ^ 1u, abort_flag);
           if (!ok) break;
           const uint32_t fb = smem_u32(qdo_full + ring.stage);
-          const uint32_t base = smem_u32(qdo_s) + ring.stage * 2 * kTile;
-          mbar_arrive_expect_tx(fb, 2 * kTile);
+          const uint32_t base = smem_u32(qdo_s) + ring.stage * kStage;
+          mbar_arrive_expect_tx(fb, 2 * kTile + kRowStat);
           qdo_armed[ring.stage] = (int)ring.phase;
           for (int c = 0; c < 2; ++c) {
             tma_load_3d(base + c * kChunk, &p.tq[bl], fb, c * 64, qt * kT, h);
             tma_load_3d(base + kTile + c * kChunk, &p.tdo[bl], fb, c * 64, qt * kT, h);
           }
+          bulk_load(base + 2 * kTile,
+                    p.rowstat + (((int64_t)(p.b0 + bl) * p.Hq + h) * p.nQt + qt) * (2 * kT), kRowStat, fb);
           ring.next();
         }
       }
@@ -426,60 +512,98 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false);
       constexpr uint32_t idesc_mn = idesc_bf16_f32(128, 128, true);
       Ring2 ring;
-      uint32_t ki = 0, pi = 0;
+      uint32_t ki = 0, ai = 0, pc[2] = {0u, 0u};
       bool ok = true;
       const uint32_t ka = smem_u32(k_s), va = smem_u32(v_s), qda = smem_u32(qdo_s);
-      for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+      // S^T_h = K Q_h^T, dP^T_h = V dO_h^T over the 64 query rows of half h
+      auto issue_ss = [&](uint32_t qt_s, int h) {
+        const uint32_t dot_s = qt_s + kTile;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + h * 128, kmaj(ka, kk), kmaj(qt_s + h * kHalfRows, kk), idesc_s, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + h * 128 + 64, kmaj(va, kk), kmaj(dot_s + h * kHalfRows, kk), idesc_s, kk > 0);
+        mma_commit(smem_u32(s_full + h));
+      };
+      // dV += P^T_h dO_h, dK += dS^T_h Q_h  (rows of half h as the MN-major B)
+      auto issue_ts = [&](uint32_t qt_s, int h, bool first) {
+        const uint32_t dot_s = qt_s + kTile;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + 256, tmem + h * 128 + kk * 8, mnmaj(dot_s, h * 4 + kk), idesc_mn,
+                 (first && kk == 0) ? 0u : 1u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + 384, tmem + h * 128 + 64 + kk * 8, mnmaj(qt_s, h * 4 + kk), idesc_mn,
+                 (first && kk == 0) ? 0u : 1u);
+      };
+      auto wait_p = [&](int h) {
+        const bool r = mbar_wait(smem_u32(p_full + h), pc[h] & 1u, abort_flag);
+        ++pc[h];
+        if (r) tc_fence_after();
+        return r;
+      };
+      ItemRing items;
+      while (ok) {
+        const int t = items.take(item_full, item_empty, item_ids, abort_flag, ok);
+        if (t < 0) break;
         int bl, hk, kb, steps;
         const int32_t* lst;
         decode(t, bl, hk, kb, steps, lst);
         if (steps == 0) continue;
-        ok = mbar_wait(smem_u32(kv_full), ki & 1u, abort_flag);
+        ok = mbar_wait(smem_u32(acc_empty), (ai & 1u) ^ 1u, abort_flag);    // last epilogue read dV/dK
+        ++ai;
+        if (ok) ok = mbar_wait(smem_u32(kv_full), ki & 1u, abort_flag);
         ++ki;
         if (!ok) break;
+        uint32_t prev_q = 0, prev_st = 0;
         for (int s = 0; s < steps && ok; ++s) {
           const uint32_t st = ring.stage;
           ok = mbar_wait(smem_u32(qdo_full + st), ring.phase, abort_flag);
           ring.next();
           if (!ok) break;
           tc_fence_after();
-          const uint32_t qt_s = qda + st * 2 * kTile, dot_s = qt_s + kTile;
-          // S^T = K Q^T, dP^T = V dO^T   (M = keys, N = query rows)
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem, kmaj(ka, kk), kmaj(qt_s, kk), idesc_s, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem + 128, kmaj(va, kk), kmaj(dot_s, kk), idesc_s, kk > 0);
-          mma_commit(smem_u32(s_full));
+          const uint32_t qs = qda + st * kStage;
+          issue_ss(qs, 0);
+          if (s > 0) {
+            if (!(ok = wait_p(1))) break;
+            issue_ts(prev_q, 1, false);
+            mma_commit(smem_u32(qdo_empty + prev_st));
+          }
+          issue_ss(qs, 1);
           if (s == steps - 1) mma_commit(smem_u32(kv_empty));
-          ok = mbar_wait(smem_u32(p_full), pi & 1u, abort_flag);
-          ++pi;
-          if (!ok) break;
-          tc_fence_after();
-          // dV += P^T dO, dK += dS^T Q   (A from TMEM, B = the row tiles as MN-major)
-#pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + 256, tmem + kk * 8, mnmaj(dot_s, kk), idesc_mn, (s > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + 384, tmem + 128 + kk * 8, mnmaj(qt_s, kk), idesc_mn, (s > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(smem_u32(qdo_empty + st));
-          if (s == steps - 1) mma_commit(smem_u32(acc_full));
+          if (!(ok = wait_p(0))) break;
+          issue_ts(qs, 0, s == 0);
+          prev_q = qs;
+          prev_st = st;
         }
+        if (!ok) break;
+        if (!(ok = wait_p(1))) break;
+        issue_ts(prev_q, 1, false);
+        mma_commit(smem_u32(qdo_empty + prev_st));
+        mma_commit(smem_u32(acc_full));
       }
       mma_commit(smem_u32(mma_done));        // every MMA issued above has finished
       mbar_drain(smem_u32(mma_done), 0);
     }
     __syncwarp();
   } else if (warp >= 4) {
+    const int half = (warp - 4) / 4;        // 0: query rows 0..63 of a tile, 1: rows 64..127
     const int wq = warp % 4;
     const int r = wq * 32 + lane;
-    const uint32_t lb = static_cast<uint32_t>(wq * 32) << 16;
-    uint32_t si = 0, ai = 0, gstep = 0;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t tb = tl + half * 128;
+    Ring2 ring;
+    ItemRing items;
+    uint32_t si = 0, ai = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
+    while (ok) {
+      const int t = items.take(item_full, item_empty, item_ids, abort_flag, ok);
+      if (t < 0) break;
       int bl, hk, kb, steps;
       const int32_t* lst;
       decode(t, bl, hk, kb, steps, lst);
@@ -488,92 +612,76 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
       const int key = kb * kBKb + r;
       const bool key_exists = key < p.Skv;
       const bool key_ok = key < p.prefix_len + L;
-      __nv_bfloat16* dkrow = p.dk + (((int64_t)b * p.Skv + key) * p.Hkv + hk) * kD;
-      __nv_bfloat16* dvrow = p.dv + (((int64_t)b * p.Skv + key) * p.Hkv + hk) * kD;
+      // keys past the end (zero-filled K/V rows) get P = 0; only the block
+      // holding the end has any, so the warp-uniform test skips the multiply
+      const bool warp_keys_ok = __all_sync(0xffffffffu, key_ok);
+      const float2 km2 = make_float2(key_ok ? 1.f : 0.f, key_ok ? 1.f : 0.f);
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      // group 0 writes dV, group 1 dK
+      __nv_bfloat16* grow = (half == 0 ? p.dv : p.dk) + (((int64_t)b * p.Skv + key) * p.Hkv + hk) * kD;
       if (steps == 0) {
-        if (key_exists) {
-          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int i = 0; i < kD / 8; ++i) {
-            reinterpret_cast<uint4*>(dkrow)[i] = z;
-            reinterpret_cast<uint4*>(dvrow)[i] = z;
-          }
-        }
+        if (key_exists) zero_row(grow, 0, kD);
         continue;
       }
-      for (int s = 0; s < steps; ++s, ++gstep) {
-        int h, qt;
-        step_tile(lst, hk, s, h, qt);
-        // per-column values of this query tile: lse (log2 units; +inf marks a
-        // padded row so its P is 0) and D, double-buffered by step parity
-        const uint32_t buf = gstep & 1u;
-        float* lse_b = rowv + buf * 2 * kT;
-        float* d_b = lse_b + kT;
-        {
-          const int row = qt * kT + r;
-          const int64_t li = ((int64_t)b * p.Hq + h) * p.Sq + row;
-          lse_b[r] = row < L ? __ldg(p.lse + li) * kLog2e : INFINITY;
-          d_b[r] = row < L ? __ldg(p.Dd + li) : 0.f;
-        }
-        // the buffer is rewritten two steps later, after every thread has
-        // arrived once more (so finished reading it)
-        mbar_arrive(smem_u32(row_ready + buf));
-        ok = mbar_wait(smem_u32(row_ready + buf), (gstep >> 1) & 1u, abort_flag);
-        if (!ok) break;
-        ok = mbar_wait(smem_u32(s_full), si & 1u, abort_flag);
+      for (int s = 0; s < steps; ++s) {
+        const uint32_t st = ring.stage;
+        // the stage's lse/D must be visible to this thread: wait for its copy too
+        ok = mbar_wait(smem_u32(qdo_full + st), ring.phase, abort_flag);
+        ring.next();
+        if (ok) ok = mbar_wait(smem_u32(s_full + half), si & 1u, abort_flag);
         ++si;
         if (!ok) break;
         tc_fence_after();
+        // per query-row column: -lse log2(e) (-inf on padded rows) and -D
+        const float* rs = reinterpret_cast<const float*>(qdo_s + st * kStage + 2 * kTile) + half * 64;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          float sv[64], dp[64];
-          tmem_ld32f(tmem + lb + h2 * 64, sv);
-          tmem_ld32f(tmem + lb + h2 * 64 + 32, sv + 32);
-          tmem_ld32f(tmem + lb + 128 + h2 * 64, dp);
-          tmem_ld32f(tmem + lb + 128 + h2 * 64 + 32, dp + 32);
+        for (int c = 0; c < 2; ++c) {
+          float sv[32], dp[32];
+          tmem_ld32f(tb + c * 32, sv);
+          tmem_ld32f(tb + 64 + c * 32, dp);
           tmem_wait_ld();
-          uint32_t pp[32], pd[32];
+          uint32_t pp[16], pd[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c0 = h2 * 64 + 2 * i;
-            const float p0 = key_ok ? ex2_approx(fmaf(sv[2 * i], p.scale_log2, -lse_b[c0])) : 0.f;
-            const float p1 = key_ok ? ex2_approx(fmaf(sv[2 * i + 1], p.scale_log2, -lse_b[c0 + 1])) : 0.f;
-            pp[i] = pack_bf16x2(p0, p1);
-            pd[i] = pack_bf16x2(p0 * (dp[2 * i] - d_b[c0]), p1 * (dp[2 * i + 1] - d_b[c0 + 1]));
+          for (int i = 0; i < 8; ++i) {
+            const float4 l4 = *reinterpret_cast<const float4*>(rs + c * 32 + 4 * i);
+            const float4 d4 = *reinterpret_cast<const float4*>(rs + kT + c * 32 + 4 * i);
+            const float2 t0 = __ffma2_rn(make_float2(sv[4 * i], sv[4 * i + 1]), sc2, make_float2(l4.x, l4.y));
+            const float2 t1 = __ffma2_rn(make_float2(sv[4 * i + 2], sv[4 * i + 3]), sc2, make_float2(l4.z, l4.w));
+            float2 p0 = make_float2(ex2_approx(t0.x), ex2_approx(t0.y));
+            float2 p1 = make_float2(ex2_approx(t1.x), ex2_approx(t1.y));
+            if (!warp_keys_ok) {
+              p0 = __fmul2_rn(p0, km2);
+              p1 = __fmul2_rn(p1, km2);
+            }
+            const float2 d0 = __fmul2_rn(p0, __fadd2_rn(make_float2(dp[4 * i], dp[4 * i + 1]), make_float2(d4.x, d4.y)));
+            const float2 d1 = __fmul2_rn(p1, __fadd2_rn(make_float2(dp[4 * i + 2], dp[4 * i + 3]), make_float2(d4.z, d4.w)));
+            pp[2 * i] = pack_bf16x2(p0.x, p0.y);
+            pp[2 * i + 1] = pack_bf16x2(p1.x, p1.y);
+            pd[2 * i] = pack_bf16x2(d0.x, d0.y);
+            pd[2 * i + 1] = pack_bf16x2(d1.x, d1.y);
           }
-          tmem_st32(tmem + lb + h2 * 32, pp);
-          tmem_st32(tmem + lb + 128 + h2 * 32, pd);
+          tmem_st16(tb + c * 16, pp);
+          tmem_st16(tb + 64 + c * 16, pd);
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(p_full));
+        mbar_arrive(smem_u32(p_full + half));
       }
       if (!ok) break;
       ok = mbar_wait(smem_u32(acc_full), ai & 1u, abort_flag);
       ++ai;
       if (!ok) break;
       tc_fence_after();
+      const float mul = half == 0 ? 1.f : p.scale;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* dst_row = which == 0 ? dvrow : dkrow;
-        const float mul = which == 0 ? 1.f : p.scale;
-#pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
-          float o[32];
-          tmem_ld32f(tmem + lb + 256 + which * 128 + c * 32, o);
-          tmem_wait_ld();
-          if (key_exists) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = key_ok ? pack_bf16x2(o[2 * i] * mul, o[2 * i + 1] * mul) : 0u;
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-        }
+      for (int c = 0; c < kD / 32; ++c) {
+        float o[32];
+        tmem_ld32f(tl + 256 + half * 128 + c * 32, o);
+        tmem_wait_ld();
+        if (key_exists) store_row32(grow + c * 32, o, mul, key_ok);
       }
       tc_fence_before();
+      mbar_arrive(smem_u32(acc_empty));
     }
   }
   tc_fence_before();
@@ -585,28 +693,33 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 }
 
 // ------------------------------------------------------- preprocessing ---
-// D[b, h, i] = sum_c dO[b, i, h, c] * O[b, i, h, c] for real rows (0 for
-// padding).  One warp per (b, row, h); 16-byte loads.
+// Per query tile (b, h, qt), 128 values of -lse * log2(e) (-inf on padded
+// rows, so their P is 0) and 128 of -D, D = sum_c dO_c O_c (0 on padded
+// rows), stored together so one bulk copy stages them.  One warp per (b, row, h)
+// over every row of the tiles, 8-byte loads.
 struct PrepParams {
   const __nv_bfloat16* o;
   const __nv_bfloat16* dout;
+  const float* lse;
   int64_t o_sb, o_ss, o_sh, d_sb, d_ss, d_sh;
-  int B, Sq, Hq;
+  int B, Sq, Hq, nQt;
   int seq_lens[kMaxSelectBatch];
-  float* Dd;
+  float* rowstat;
 };
 
 __global__ void bwd_prep_kernel(const __grid_constant__ PrepParams p) {
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
-  const int64_t total = (int64_t)p.B * p.Sq * p.Hq;
+  const int rows = p.nQt * kT;
+  const int64_t total = (int64_t)p.B * rows * p.Hq;
   if (w >= total) return;
   const int h = (int)(w % p.Hq);
   const int64_t rr = w / p.Hq;
-  const int row = (int)(rr % p.Sq);
-  const int b = (int)(rr / p.Sq);
+  const int row = (int)(rr % rows);
+  const int b = (int)(rr / rows);
+  const bool real = row < p.seq_lens[b];
   float acc = 0.f;
-  if (row < p.seq_lens[b] && lane < kD / 4) {
+  if (real) {
     const __nv_bfloat16* op = p.o + b * p.o_sb + (int64_t)row * p.o_ss + (int64_t)h * p.o_sh + lane * 4;
     const __nv_bfloat16* dp = p.dout + b * p.d_sb + (int64_t)row * p.d_ss + (int64_t)h * p.d_sh + lane * 4;
     const uint2 a = *reinterpret_cast<const uint2*>(op);
@@ -622,7 +735,11 @@ __global__ void bwd_prep_kernel(const __grid_constant__ PrepParams p) {
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) p.Dd[((int64_t)b * p.Hq + h) * p.Sq + row] = acc;
+  if (lane == 0) {
+    float* rs = p.rowstat + (((int64_t)b * p.Hq + h) * p.nQt + row / kT) * (2 * kT) + row % kT;
+    rs[0] = real ? -p.lse[((int64_t)b * p.Hq + h) * p.Sq + row] * kLog2e : -INFINITY;
+    rs[kT] = -acc;
+  }
 }
 
 // ------------------------------------------------------ inverse lists ---
@@ -722,8 +839,8 @@ bsa_status encode(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int
   return BSA_OK;
 }
 
-constexpr int kDqSmem = 2 * kTile + 2 * 2 * kTile + 256 + 1024;   // tiles, barriers, alignment
-constexpr int kDkvSmem = 2 * kTile + 2 * 2 * kTile + 2 * 2 * kT * 4 + 256 + 1024;
+constexpr int kDqSmem = 2 * kTile + 2 * 2 * kTile + 256 + 1024;              // tiles, barriers, alignment
+constexpr int kDkvSmem = 2 * kTile + 2 * (2 * kTile + kRowStat) + 256 + 1024;
 
 }  // namespace
 
@@ -731,7 +848,8 @@ size_t backward_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int blo
   const int64_t nQb = cdiv64(Sq, block_q), nKb = cdiv64(Skv, block_k), G = Hq / Hkv;
   const int64_t words = cdiv64(nKb, 32);
   auto al = [](int64_t x) { return (size_t)((x + 255) & ~(int64_t)255); };
-  return al((int64_t)B * Hq * Sq * 4)                      // D
+  return al((int64_t)B * Hq * cdiv64(Sq, kT) * kRowStat)  // lse * log2(e) and D per query tile
+         + 256                                             // item counters, one per launch chunk
          + al((int64_t)B * Hkv * G * nQb * words * 4)      // bitmaps
          + al((int64_t)B * Hkv * nKb * 4)                  // inverse counts
          + al((int64_t)B * Hkv * nKb * G * nQb * 4);       // inverse lists
@@ -744,28 +862,32 @@ bsa_status launch_backward(const BackwardArgs& a, cudaStream_t stream) {
   const int words = (nKb + 31) / 32;
   auto al = [](int64_t x) { return (size_t)((x + 255) & ~(int64_t)255); };
   char* ws = static_cast<char*>(a.workspace);
-  float* Dd = reinterpret_cast<float*>(ws);
-  ws += al((int64_t)a.B * a.Hq * a.Sq * 4);
-  uint32_t* bm = reinterpret_cast<uint32_t*>(ws);
+  const int nQt = (int)cdiv64(a.Sq, kT);
+  float* rowstat = reinterpret_cast<float*>(ws);
+  ws += al((int64_t)a.B * a.Hq * nQt * kRowStat);
+  int* counters = reinterpret_cast<int*>(ws);   // zeroed together with the bitmaps that follow
+  uint32_t* bm = reinterpret_cast<uint32_t*>(ws + 256);
   const size_t bm_bytes = al((int64_t)a.B * a.Hkv * G * nQb * words * 4);
-  ws += bm_bytes;
+  ws += 256 + bm_bytes;
   int32_t* inv_cnt = reinterpret_cast<int32_t*>(ws);
   ws += al((int64_t)a.B * a.Hkv * nKb * 4);
   int32_t* inv_list = reinterpret_cast<int32_t*>(ws);
 
-  {  // D = rowsum(dO * O)
+  {  // lse * log2(e) and D = rowsum(dO * O) per query tile
     PrepParams pp{};
     pp.o = static_cast<const __nv_bfloat16*>(a.o); pp.dout = static_cast<const __nv_bfloat16*>(a.dout);
+    pp.lse = a.lse;
     pp.o_sb = a.o_sb; pp.o_ss = a.o_ss; pp.o_sh = a.o_sh; pp.d_sb = a.d_sb; pp.d_ss = a.d_ss; pp.d_sh = a.d_sh;
-    pp.B = a.B; pp.Sq = a.Sq; pp.Hq = a.Hq;
+    pp.B = a.B; pp.Sq = a.Sq; pp.Hq = a.Hq; pp.nQt = nQt;
     for (int b = 0; b < a.B; ++b) pp.seq_lens[b] = a.seq_lens ? a.seq_lens[b] : a.Sq;
-    pp.Dd = Dd;
-    const int64_t warps = (int64_t)a.B * a.Sq * a.Hq;
+    pp.rowstat = rowstat;
+    const int64_t warps = (int64_t)a.B * nQt * kT * a.Hq;
     bwd_prep_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, stream>>>(pp);
     if ((st = cuda_check(cudaGetLastError(), "bwd_prep_kernel launch")) != BSA_OK) return st;
   }
   {  // inverse lists
-    if ((st = cuda_check(cudaMemsetAsync(bm, 0, bm_bytes, stream), "cudaMemsetAsync(bitmaps)")) != BSA_OK) return st;
+    if ((st = cuda_check(cudaMemsetAsync(counters, 0, 256 + bm_bytes, stream), "cudaMemsetAsync(bitmaps)")) != BSA_OK)
+      return st;
     BitmapParams bp{};
     bp.indices = a.indices; bp.counts = a.counts; bp.bm = bm;
     bp.B = a.B; bp.Hq = a.Hq; bp.Hkv = a.Hkv; bp.G = G; bp.nQb = nQb; bp.nKb = nKb; bp.block_q = a.block_q;
@@ -810,8 +932,8 @@ bsa_status launch_backward(const BackwardArgs& a, cudaStream_t stream) {
       if ((st = encode(&p.tv[i], vb, a.prefix_len + L, a.Hkv, a.v_ss, a.v_sh, "V")) != BSA_OK) return st;
     }
     p.b0 = b0; p.Bn = Bn; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.Sq = a.Sq; p.Skv = a.Skv;
-    p.nQb = nQb; p.nKb = nKb; p.nQt = (int)cdiv64(a.Sq, kT); p.block_q = a.block_q; p.prefix_len = a.prefix_len;
-    p.indices = a.indices; p.counts = a.counts; p.lse = a.lse; p.Dd = Dd;
+    p.nQb = nQb; p.nKb = nKb; p.nQt = nQt; p.block_q = a.block_q; p.prefix_len = a.prefix_len;
+    p.indices = a.indices; p.counts = a.counts; p.rowstat = rowstat;
     p.inv_cnt = inv_cnt; p.inv_list = inv_list;
     p.scale = a.scale; p.scale_log2 = a.scale * kLog2e;
     p.dq = static_cast<__nv_bfloat16*>(a.dq);
@@ -821,6 +943,7 @@ bsa_status launch_backward(const BackwardArgs& a, cudaStream_t stream) {
     bwd_dq_kernel<<<std::min(p.n_items, sms), kThreads, kDqSmem, stream>>>(p);
     if ((st = cuda_check(cudaGetLastError(), "bwd_dq_kernel launch")) != BSA_OK) return st;
     p.n_items = Bn * a.Hkv * nKb;
+    p.counter = counters + b0 / kMaxFwdBatch;
     bwd_dkdv_kernel<<<std::min(p.n_items, sms), kThreads, kDkvSmem, stream>>>(p);
     if ((st = cuda_check(cudaGetLastError(), "bwd_dkdv_kernel launch")) != BSA_OK) return st;
   }

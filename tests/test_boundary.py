@@ -287,11 +287,12 @@ def test_backward_rejects_bad_arguments(lib, case, status, needle):
 
 
 def test_backward_workspace_size_formula(lib):
-    # D [B,Hq,Sq] fp32, bitmaps [B,Hkv,G*nQb,ceil(nKb/32)] u32, inverse counts [B,Hkv,nKb] and
-    # lists [B,Hkv,nKb,G*nQb] int32, each rounded up to 256 B
+    # per 128-row query tile 128 lse and 128 D values (fp32), 256 B of item counters, bitmaps
+    # [B,Hkv,G*nQb,ceil(nKb/32)] u32, inverse counts [B,Hkv,nKb] and lists [B,Hkv,nKb,G*nQb] int32, each rounded up to 256 B
     B, Hq, Hkv, Sq, Skv, bq, bk = 1, 32, 8, 172800, 173824, 256, 128
     r = lambda x: ((x + 255) // 256) * 256
-    nQb, nKb, G = 675, 1358, 4
-    want = r(B * Hq * Sq * 4) + r(B * Hkv * G * nQb * 43 * 4) + r(B * Hkv * nKb * 4) + r(B * Hkv * nKb * G * nQb * 4)
+    nQb, nKb, G, nQt = 675, 1358, 4, 1350
+    want = (r(B * Hq * nQt * 256 * 4) + 256 + r(B * Hkv * G * nQb * 43 * 4) + r(B * Hkv * nKb * 4)
+            + r(B * Hkv * nKb * G * nQb * 4))
     assert lib.bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, bq, bk) == want
     assert lib.bsa_backward_workspace_size(B, Hq, 5, Sq, Skv, bq, bk) == 0
