@@ -16,11 +16,11 @@
 //    (an inverse list built from bitmaps, ordered by query tile) and
 //    accumulates dK and dV in TMEM (S^T = K Q^T, dP^T = V dO^T,
 //    dV += P^T dO, dK += dS^T Q).
-// Each 128 x 128 score tile is computed as two 64-wide halves in separate
-// TMEM buffers, handled by two elementwise warpgroups, so that one half's
-// exponentials overlap the other half's MMAs (the issue order is
-// SS(h0), TS(prev h1), SS(h1), TS(h0), ...).  TMA tile loads, one
-// MMA-issuing thread, every wait bounded.
+// Every MMA is M128 x N128 (an N64 MMA costs as long as an N128 one).  Two
+// elementwise warpgroups split each 128 x 128 score tile by columns and keep
+// P in registers between the exponentials and dS, which frees the score
+// columns early enough for the next tile's MMAs to overlap the elementwise
+// work.  TMA tile loads, one MMA-issuing thread, every wait bounded.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -39,7 +39,6 @@ constexpr int kBKb = 128;               // key block
 constexpr int kT = 128;                 // query tile rows
 constexpr int kChunk = 128 * 128;       // 128 rows x 64 bf16 (one 128-byte column chunk)
 constexpr int kTile = 2 * kChunk;       // 128 rows x 128 bf16 = 32 KB
-constexpr int kHalfRows = 64 * 128;     // byte offset of row 64 inside a chunk
 constexpr int kRowStat = 2 * kT * 4;    // per query tile: -lse * log2(e) [128], -D [128]
 constexpr int kThreads = 384;           // warp 0 TMA, warp 1 MMA, warps 4..7 / 8..11 elementwise halves
 constexpr float kLog2e = 1.4426950408889634f;
@@ -111,9 +110,12 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* o, 
 }
 
 // ---------------------------------------------------------------- dQ ---
-// TMEM: half h of the key block in columns [128 h, 128 h + 128): S in the
-// first 64 (dS bf16 over its first 32 once computed), dP in the next 64;
-// dQ accumulates in [256, 384).
+// TMEM: S in [0, 128); dP of key block j in buffer j % 2 at [128, 256) or
+// [256, 384), overwritten in place by dS (bf16, 32 columns per 64 keys);
+// dQ accumulates in [384, 512).  The two elementwise warpgroups split the
+// 128 keys of a block (group g: keys 64 g .. 64 g + 63) and keep P in
+// registers between the exponentials (which free S for the next block's
+// S MMA) and dS.  Issue order: S(j+1), dP(j+1), dQ(j), ...
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -124,26 +126,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + 2 * 2 * kTile);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* s_full = bars + 2;            // [2] per half
-  uint64_t* ds_full = bars + 4;           // [2]
-  uint64_t* dq_full = bars + 6;
-  uint64_t* acc_empty = bars + 7;
-  uint64_t* kv_full = bars + 8;           // [2]
-  uint64_t* kv_empty = bars + 10;         // [2]
-  uint64_t* mma_done = bars + 12;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* s_full = bars + 2;
+  uint64_t* s_free = bars + 3;
+  uint64_t* dp_full = bars + 4;           // [2] per dP buffer
+  uint64_t* ds_full = bars + 6;           // [2]
+  uint64_t* dq_full = bars + 8;
+  uint64_t* acc_empty = bars + 9;
+  uint64_t* kv_full = bars + 10;          // [2]
+  uint64_t* kv_empty = bars + 12;         // [2]
+  uint64_t* mma_done = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
     mbar_init(smem_u32(q_empty), 1);
+    mbar_init(smem_u32(s_full), 1);
+    mbar_init(smem_u32(s_free), 256);
     mbar_init(smem_u32(dq_full), 1);
     mbar_init(smem_u32(acc_empty), 256);
     mbar_init(smem_u32(mma_done), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(s_full + i), 1);
-      mbar_init(smem_u32(ds_full + i), 128);
+      mbar_init(smem_u32(dp_full + i), 1);
+      mbar_init(smem_u32(ds_full + i), 256);
       mbar_init(smem_u32(kv_full + i), 1);
       mbar_init(smem_u32(kv_empty + i), 1);
     }
@@ -224,35 +230,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA ---
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_mn = idesc_bf16_f32(128, 128, true);
       Ring2 ring;
-      uint32_t qi = 0, ai = 0, dc[2] = {0u, 0u};
+      uint32_t qi = 0, ai = 0, sf = 0, dsc[2] = {0u, 0u}, jj = 0;
       bool ok = true;
       const uint32_t qa = smem_u32(q_s), da = smem_u32(do_s), kva = smem_u32(kv_s);
-      // S_h = Q K_h^T, dP_h = dO V_h^T over the 64 keys of half h
-      auto issue_ss = [&](uint32_t kt, int h) {
-        const uint32_t vt = kt + kTile;
+      // S = Q K^T into [0, 128), dP = dO V^T into buffer `buf`
+      auto issue_s_dp = [&](uint32_t kt, uint32_t buf) {
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem, kmaj(qa, kk), kmaj(kt, kk), idesc_s, kk > 0);
+        mma_commit(smem_u32(s_full));
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + h * 128, kmaj(qa, kk), kmaj(kt + h * kHalfRows, kk), idesc_s, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + h * 128 + 64, kmaj(da, kk), kmaj(vt + h * kHalfRows, kk), idesc_s, kk > 0);
-        mma_commit(smem_u32(s_full + h));
+          mma_ss(tmem + 128 + buf * 128, kmaj(da, kk), kmaj(kt + kTile, kk), idesc_s, kk > 0);
+        mma_commit(smem_u32(dp_full + buf));
       };
-      // dQ += dS_h K_h  (dS bf16 in TMEM, K rows of half h as the MN-major B)
-      auto issue_ts = [&](uint32_t kt, int h, bool first) {
+      // dQ += dS K (dS bf16 of keys 64 g + .. at buffer column 64 g; K as the MN-major B)
+      auto issue_dq = [&](uint32_t kt, uint32_t buf, bool first) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + 256, tmem + h * 128 + kk * 8, mnmaj(kt, h * 4 + kk), idesc_mn,
+        for (int kk = 0; kk < kBKb / 16; ++kk)
+          mma_ts(tmem + 384, tmem + 128 + buf * 128 + (kk / 4) * 64 + (kk % 4) * 8, mnmaj(kt, kk), idesc_mn,
                  (first && kk == 0) ? 0u : 1u);
-      };
-      auto wait_ds = [&](int h) {
-        const bool r = mbar_wait(smem_u32(ds_full + h), dc[h] & 1u, abort_flag);
-        ++dc[h];
-        if (r) tc_fence_after();
-        return r;
       };
       for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
         int bl, h, qt, qb, n, L;
@@ -263,31 +262,43 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         if (ok) ok = mbar_wait(smem_u32(q_full), qi & 1u, abort_flag);
         ++qi;
         if (!ok) break;
-        uint32_t prev_kt = 0, prev_st = 0;
-        for (int j = 0; j < n && ok; ++j) {
-          const uint32_t st = ring.stage;
-          ok = mbar_wait(smem_u32(kv_full + st), ring.phase, abort_flag);
-          ring.next();
+        // block 0's S and dP
+        uint32_t st = ring.stage;
+        ok = mbar_wait(smem_u32(kv_full + st), ring.phase, abort_flag);
+        ring.next();
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t kt = kva + st * 2 * kTile;
+        issue_s_dp(kt, jj & 1u);
+        if (n == 1) mma_commit(smem_u32(q_empty));
+        for (int j = 0; j < n && ok; ++j, ++jj) {
+          const uint32_t buf = jj & 1u;
+          // S is free once both groups hold P(j) in registers
+          ok = mbar_wait(smem_u32(s_free), sf & 1u, abort_flag);
+          ++sf;
           if (!ok) break;
           tc_fence_after();
-          const uint32_t kt = kva + st * 2 * kTile;
-          issue_ss(kt, 0);
-          if (j > 0) {
-            if (!(ok = wait_ds(1))) break;
-            issue_ts(prev_kt, 1, false);
-            mma_commit(smem_u32(kv_empty + prev_st));
+          uint32_t nst = 0, nkt = 0;
+          if (j + 1 < n) {
+            nst = ring.stage;
+            ok = mbar_wait(smem_u32(kv_full + nst), ring.phase, abort_flag);
+            ring.next();
+            if (!ok) break;
+            tc_fence_after();
+            nkt = kva + nst * 2 * kTile;
+            issue_s_dp(nkt, buf ^ 1u);
+            if (j + 2 == n) mma_commit(smem_u32(q_empty));
           }
-          issue_ss(kt, 1);
-          if (j == n - 1) mma_commit(smem_u32(q_empty));
-          if (!(ok = wait_ds(0))) break;
-          issue_ts(kt, 0, j == 0);
-          prev_kt = kt;
-          prev_st = st;
+          ok = mbar_wait(smem_u32(ds_full + buf), dsc[buf] & 1u, abort_flag);
+          ++dsc[buf];
+          if (!ok) break;
+          tc_fence_after();
+          issue_dq(kt, buf, j == 0);
+          mma_commit(smem_u32(kv_empty + st));
+          st = nst;
+          kt = nkt;
         }
         if (!ok) break;
-        if (!(ok = wait_ds(1))) break;
-        issue_ts(prev_kt, 1, false);
-        mma_commit(smem_u32(kv_empty + prev_st));
         mma_commit(smem_u32(dq_full));
       }
       mma_commit(smem_u32(mma_done));        // every MMA issued above has finished
@@ -296,12 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     __syncwarp();
   } else if (warp >= 4) {
     // ----------------------------------------------------- elementwise ---
-    const int half = (warp - 4) / 4;        // 0: keys 0..63 of a block, 1: keys 64..127
+    const int grp = (warp - 4) / 4;         // keys 64 grp .. 64 grp + 63 of each block
     const int wq = warp % 4;
     const int r = wq * 32 + lane;
-    const uint32_t tb = tmem + (static_cast<uint32_t>(wq * 32) << 16) + half * 128;
-    const uint32_t tq = tmem + (static_cast<uint32_t>(wq * 32) << 16) + 256;
-    uint32_t si = 0, oi = 0;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    uint32_t sc = 0, oi = 0, jj = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
       int bl, h, qt, qb, n, L;
@@ -312,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       const bool row_ok = row < L;
       __nv_bfloat16* drow = p.dq + (((int64_t)b * p.Sq + row) * p.Hq + h) * kD;
       if (n == 0) {
-        if (row_exists) zero_row(drow, half * 64, 64);
+        if (row_exists) zero_row(drow, grp * 64, 64);
         continue;
       }
       const float* rs = p.rowstat + (((int64_t)b * p.Hq + h) * p.nQt + qt) * (2 * kT);
@@ -322,41 +332,59 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       const float2 nD2 = make_float2(nD, nD);
       const int valid_kv = p.prefix_len + L;
       const int32_t* lst = p.indices + (((int64_t)b * p.Hq + h) * p.nQb + qb) * p.nKb;
-      for (int j = 0; j < n; ++j) {
+      for (int j = 0; j < n; ++j, ++jj) {
+        const uint32_t buf = jj & 1u;
         int kb = __ldg(lst + j);
         if (kb < 0 || kb >= p.nKb) kb = p.nKb;
-        const int kvalid = valid_kv - kb * kBKb - half * 64;    // keys of this half below the end
-        ok = mbar_wait(smem_u32(s_full + half), si & 1u, abort_flag);
-        ++si;
+        // keys of this group's half below the end of the sequence (a block holding the end only)
+        const int kvalid = valid_kv - kb * kBKb - grp * 64;
+        const bool all_valid = kvalid >= 64;
+        ok = mbar_wait(smem_u32(s_full), sc & 1u, abort_flag);
+        ++sc;
         if (!ok) break;
         tc_fence_after();
-        // dS = P (dP - D), P = 2^(S scale log2(e) - lse log2(e)); keys past
-        // the end of the sequence (only in a block holding it) get P = 0
-        const bool all_valid = kvalid >= 64;
+        // P = 2^(S scale log2(e) - lse log2(e)), kept in registers
+        float pr[64];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          float s[32], dp[32];
-          tmem_ld32f(tb + c * 32, s);
-          tmem_ld32f(tb + 64 + c * 32, dp);
+          float s[32];
+          tmem_ld32f(tl + grp * 64 + c * 32, s);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), sc2, nl2);
+            pr[c * 32 + 2 * i] = ex2_approx(x.x);
+            pr[c * 32 + 2 * i + 1] = ex2_approx(x.y);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(s_free));
+        if (!all_valid) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) pr[i] = i < kvalid ? pr[i] : 0.f;
+        }
+        // dS = P (dP - D), written over this group's dP columns
+        ok = mbar_wait(smem_u32(dp_full + buf), (jj >> 1) & 1u, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tb = tl + 128 + buf * 128 + grp * 64;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float dp[32];
+          tmem_ld32f(tb + c * 32, dp);
           tmem_wait_ld();
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float2 t = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), sc2, nl2);
-            float2 pr = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-            if (!all_valid) {
-              const int c0 = c * 32 + 2 * i;
-              pr.x = c0 < kvalid ? pr.x : 0.f;
-              pr.y = c0 + 1 < kvalid ? pr.y : 0.f;
-            }
-            const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(dp[2 * i], dp[2 * i + 1]), nD2));
+            const float2 ds = __fmul2_rn(make_float2(pr[c * 32 + 2 * i], pr[c * 32 + 2 * i + 1]),
+                                         __fadd2_rn(make_float2(dp[2 * i], dp[2 * i + 1]), nD2));
             pk[i] = pack_bf16x2(ds.x, ds.y);
           }
           tmem_st16(tb + c * 16, pk);
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(ds_full + half));
+        mbar_arrive(smem_u32(ds_full + buf));
       }
       if (!ok) break;
       ok = mbar_wait(smem_u32(dq_full), oi & 1u, abort_flag);
@@ -366,9 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float o[32];
-        tmem_ld32f(tq + half * 64 + c * 32, o);
+        tmem_ld32f(tl + 384 + grp * 64 + c * 32, o);
         tmem_wait_ld();
-        if (row_exists) store_row32(drow + half * 64 + c * 32, o, p.scale, row_ok);
+        if (row_exists) store_row32(drow + grp * 64 + c * 32, o, p.scale, row_ok);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(acc_empty));
@@ -383,10 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 }
 
 // ------------------------------------------------------------- dK, dV ---
-// TMEM: half h of the query tile (rows 64 h .. 64 h + 63) in columns
-// [128 h, 128 h + 128): S^T in the first 64 (P^T bf16 over its first 32
-// once computed), dP^T in the next 64 (dS^T bf16 over its first 32);
-// dV accumulates in [256, 384), dK in [384, 512).
+// TMEM: S^T in [0, 128) (P^T bf16 over it: query columns 64 g .. at column
+// 64 g, 32 wide), dP^T in [128, 256) (dS^T bf16 the same way), dV in
+// [256, 384), dK in [384, 512).  The two elementwise warpgroups split the
+// 128 query rows of a step (group g: rows 64 g .. 64 g + 63) and keep P^T
+// in registers between P^T and dS^T.  Issue order: S^T(s), dP^T(s), dV(s),
+// S^T(s+1), dK(s), dP^T(s+1), ...
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -398,8 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
   uint64_t* bars = reinterpret_cast<uint64_t*>(qdo_s + 2 * kStage);
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
-  uint64_t* s_full = bars + 2;            // [2] per half
-  uint64_t* p_full = bars + 4;            // [2]
+  uint64_t* s_full = bars + 2;
+  uint64_t* dp_full = bars + 3;
+  uint64_t* p_full = bars + 4;
+  uint64_t* ds_full = bars + 5;
   uint64_t* acc_full = bars + 6;
   uint64_t* acc_empty = bars + 7;
   uint64_t* qdo_full = bars + 8;          // [2]
@@ -415,12 +447,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(kv_full), 1);
     mbar_init(smem_u32(kv_empty), 1);
+    mbar_init(smem_u32(s_full), 1);
+    mbar_init(smem_u32(dp_full), 1);
+    mbar_init(smem_u32(p_full), 256);
+    mbar_init(smem_u32(ds_full), 256);
     mbar_init(smem_u32(acc_full), 1);
     mbar_init(smem_u32(acc_empty), 256);
     mbar_init(smem_u32(mma_done), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(s_full + i), 1);
-      mbar_init(smem_u32(p_full + i), 128);
       mbar_init(smem_u32(qdo_full + i), 1);
       mbar_init(smem_u32(qdo_empty + i), 1);
       mbar_init(smem_u32(item_full + i), 1);
@@ -512,39 +546,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_mn = idesc_bf16_f32(128, 128, true);
       Ring2 ring;
-      uint32_t ki = 0, ai = 0, pc[2] = {0u, 0u};
+      uint32_t ki = 0, ai = 0, pc = 0, dc = 0;
       bool ok = true;
       const uint32_t ka = smem_u32(k_s), va = smem_u32(v_s), qda = smem_u32(qdo_s);
-      // S^T_h = K Q_h^T, dP^T_h = V dO_h^T over the 64 query rows of half h
-      auto issue_ss = [&](uint32_t qt_s, int h) {
-        const uint32_t dot_s = qt_s + kTile;
+      auto issue_st = [&](uint32_t qs) {        // S^T = K Q^T
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem, kmaj(ka, kk), kmaj(qs, kk), idesc_s, kk > 0);
+        mma_commit(smem_u32(s_full));
+      };
+      auto issue_dpt = [&](uint32_t qs) {       // dP^T = V dO^T
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + h * 128, kmaj(ka, kk), kmaj(qt_s + h * kHalfRows, kk), idesc_s, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + h * 128 + 64, kmaj(va, kk), kmaj(dot_s + h * kHalfRows, kk), idesc_s, kk > 0);
-        mma_commit(smem_u32(s_full + h));
+          mma_ss(tmem + 128, kmaj(va, kk), kmaj(qs + kTile, kk), idesc_s, kk > 0);
+        mma_commit(smem_u32(dp_full));
       };
-      // dV += P^T_h dO_h, dK += dS^T_h Q_h  (rows of half h as the MN-major B)
-      auto issue_ts = [&](uint32_t qt_s, int h, bool first) {
-        const uint32_t dot_s = qt_s + kTile;
+      // dV += P^T dO, dK += dS^T Q  (A from TMEM, the row tiles as the MN-major B)
+      auto issue_dv = [&](uint32_t qs, bool first) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + 256, tmem + h * 128 + kk * 8, mnmaj(dot_s, h * 4 + kk), idesc_mn,
-                 (first && kk == 0) ? 0u : 1u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + 384, tmem + h * 128 + 64 + kk * 8, mnmaj(qt_s, h * 4 + kk), idesc_mn,
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ts(tmem + 256, tmem + (kk / 4) * 64 + (kk % 4) * 8, mnmaj(qs + kTile, kk), idesc_mn,
                  (first && kk == 0) ? 0u : 1u);
       };
-      auto wait_p = [&](int h) {
-        const bool r = mbar_wait(smem_u32(p_full + h), pc[h] & 1u, abort_flag);
-        ++pc[h];
+      auto issue_dk = [&](uint32_t qs, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ts(tmem + 384, tmem + 128 + (kk / 4) * 64 + (kk % 4) * 8, mnmaj(qs, kk), idesc_mn,
+                 (first && kk == 0) ? 0u : 1u);
+      };
+      auto wait_stage = [&](uint32_t& qs, uint32_t& st) {
+        st = ring.stage;
+        const bool r = mbar_wait(smem_u32(qdo_full + st), ring.phase, abort_flag);
+        ring.next();
         if (r) tc_fence_after();
+        qs = qda + st * kStage;
         return r;
       };
       ItemRing items;
@@ -560,31 +597,33 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         if (ok) ok = mbar_wait(smem_u32(kv_full), ki & 1u, abort_flag);
         ++ki;
         if (!ok) break;
-        uint32_t prev_q = 0, prev_st = 0;
+        uint32_t qs, st;
+        if (!(ok = wait_stage(qs, st))) break;
+        issue_st(qs);
+        issue_dpt(qs);
         for (int s = 0; s < steps && ok; ++s) {
-          const uint32_t st = ring.stage;
-          ok = mbar_wait(smem_u32(qdo_full + st), ring.phase, abort_flag);
-          ring.next();
+          ok = mbar_wait(smem_u32(p_full), pc & 1u, abort_flag);
+          ++pc;
           if (!ok) break;
           tc_fence_after();
-          const uint32_t qs = qda + st * kStage;
-          issue_ss(qs, 0);
-          if (s > 0) {
-            if (!(ok = wait_p(1))) break;
-            issue_ts(prev_q, 1, false);
-            mma_commit(smem_u32(qdo_empty + prev_st));
+          issue_dv(qs, s == 0);
+          uint32_t nqs = 0, nst = 0;
+          if (s + 1 < steps) {
+            if (!(ok = wait_stage(nqs, nst))) break;
+            issue_st(nqs);
           }
-          issue_ss(qs, 1);
-          if (s == steps - 1) mma_commit(smem_u32(kv_empty));
-          if (!(ok = wait_p(0))) break;
-          issue_ts(qs, 0, s == 0);
-          prev_q = qs;
-          prev_st = st;
+          ok = mbar_wait(smem_u32(ds_full), dc & 1u, abort_flag);
+          ++dc;
+          if (!ok) break;
+          tc_fence_after();
+          issue_dk(qs, s == 0);
+          mma_commit(smem_u32(qdo_empty + st));
+          if (s + 1 < steps) issue_dpt(nqs);
+          qs = nqs;
+          st = nst;
         }
         if (!ok) break;
-        if (!(ok = wait_p(1))) break;
-        issue_ts(prev_q, 1, false);
-        mma_commit(smem_u32(qdo_empty + prev_st));
+        mma_commit(smem_u32(kv_empty));
         mma_commit(smem_u32(acc_full));
       }
       mma_commit(smem_u32(mma_done));        // every MMA issued above has finished
@@ -592,14 +631,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     }
     __syncwarp();
   } else if (warp >= 4) {
-    const int half = (warp - 4) / 4;        // 0: query rows 0..63 of a tile, 1: rows 64..127
+    const int grp = (warp - 4) / 4;         // query rows 64 grp .. 64 grp + 63 of each step
     const int wq = warp % 4;
     const int r = wq * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t tb = tl + half * 128;
     Ring2 ring;
     ItemRing items;
-    uint32_t si = 0, ai = 0;
+    uint32_t sc = 0, dc = 0, ai = 0;
     bool ok = true;
     while (ok) {
       const int t = items.take(item_full, item_empty, item_ids, abort_flag, ok);
@@ -618,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
       const float2 km2 = make_float2(key_ok ? 1.f : 0.f, key_ok ? 1.f : 0.f);
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       // group 0 writes dV, group 1 dK
-      __nv_bfloat16* grow = (half == 0 ? p.dv : p.dk) + (((int64_t)b * p.Skv + key) * p.Hkv + hk) * kD;
+      __nv_bfloat16* grow = (grp == 0 ? p.dv : p.dk) + (((int64_t)b * p.Skv + key) * p.Hkv + hk) * kD;
       if (steps == 0) {
         if (key_exists) zero_row(grow, 0, kD);
         continue;
@@ -628,23 +666,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         // the stage's lse/D must be visible to this thread: wait for its copy too
         ok = mbar_wait(smem_u32(qdo_full + st), ring.phase, abort_flag);
         ring.next();
-        if (ok) ok = mbar_wait(smem_u32(s_full + half), si & 1u, abort_flag);
-        ++si;
+        if (ok) ok = mbar_wait(smem_u32(s_full), sc & 1u, abort_flag);
+        ++sc;
         if (!ok) break;
         tc_fence_after();
         // per query-row column: -lse log2(e) (-inf on padded rows) and -D
-        const float* rs = reinterpret_cast<const float*>(qdo_s + st * kStage + 2 * kTile) + half * 64;
+        const float* rs = reinterpret_cast<const float*>(qdo_s + st * kStage + 2 * kTile) + grp * 64;
+        // P^T = 2^(S^T scale log2(e) - lse log2(e)), kept in registers; bf16 over S^T
+        float pr[64];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          float sv[32], dp[32];
-          tmem_ld32f(tb + c * 32, sv);
-          tmem_ld32f(tb + 64 + c * 32, dp);
+          float sv[32];
+          tmem_ld32f(tl + grp * 64 + c * 32, sv);
           tmem_wait_ld();
-          uint32_t pp[16], pd[16];
+          uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float4 l4 = *reinterpret_cast<const float4*>(rs + c * 32 + 4 * i);
-            const float4 d4 = *reinterpret_cast<const float4*>(rs + kT + c * 32 + 4 * i);
             const float2 t0 = __ffma2_rn(make_float2(sv[4 * i], sv[4 * i + 1]), sc2, make_float2(l4.x, l4.y));
             const float2 t1 = __ffma2_rn(make_float2(sv[4 * i + 2], sv[4 * i + 3]), sc2, make_float2(l4.z, l4.w));
             float2 p0 = make_float2(ex2_approx(t0.x), ex2_approx(t0.y));
@@ -653,30 +691,55 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
               p0 = __fmul2_rn(p0, km2);
               p1 = __fmul2_rn(p1, km2);
             }
-            const float2 d0 = __fmul2_rn(p0, __fadd2_rn(make_float2(dp[4 * i], dp[4 * i + 1]), make_float2(d4.x, d4.y)));
-            const float2 d1 = __fmul2_rn(p1, __fadd2_rn(make_float2(dp[4 * i + 2], dp[4 * i + 3]), make_float2(d4.z, d4.w)));
-            pp[2 * i] = pack_bf16x2(p0.x, p0.y);
-            pp[2 * i + 1] = pack_bf16x2(p1.x, p1.y);
-            pd[2 * i] = pack_bf16x2(d0.x, d0.y);
-            pd[2 * i + 1] = pack_bf16x2(d1.x, d1.y);
+            pr[c * 32 + 4 * i] = p0.x;
+            pr[c * 32 + 4 * i + 1] = p0.y;
+            pr[c * 32 + 4 * i + 2] = p1.x;
+            pr[c * 32 + 4 * i + 3] = p1.y;
+            pk[2 * i] = pack_bf16x2(p0.x, p0.y);
+            pk[2 * i + 1] = pack_bf16x2(p1.x, p1.y);
           }
-          tmem_st16(tb + c * 16, pp);
-          tmem_st16(tb + 64 + c * 16, pd);
+          tmem_st16(tl + grp * 64 + c * 16, pk);
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(p_full + half));
+        mbar_arrive(smem_u32(p_full));
+        // dS^T = P^T (dP^T - D), bf16 over this group's dP^T columns
+        ok = mbar_wait(smem_u32(dp_full), dc & 1u, abort_flag);
+        ++dc;
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float dp[32];
+          tmem_ld32f(tl + 128 + grp * 64 + c * 32, dp);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 d4 = *reinterpret_cast<const float4*>(rs + kT + c * 32 + 4 * i);
+            const float2 d0 = __fmul2_rn(make_float2(pr[c * 32 + 4 * i], pr[c * 32 + 4 * i + 1]),
+                                         __fadd2_rn(make_float2(dp[4 * i], dp[4 * i + 1]), make_float2(d4.x, d4.y)));
+            const float2 d1 = __fmul2_rn(make_float2(pr[c * 32 + 4 * i + 2], pr[c * 32 + 4 * i + 3]),
+                                         __fadd2_rn(make_float2(dp[4 * i + 2], dp[4 * i + 3]), make_float2(d4.z, d4.w)));
+            pk[2 * i] = pack_bf16x2(d0.x, d0.y);
+            pk[2 * i + 1] = pack_bf16x2(d1.x, d1.y);
+          }
+          tmem_st16(tl + 128 + grp * 64 + c * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(ds_full));
       }
       if (!ok) break;
       ok = mbar_wait(smem_u32(acc_full), ai & 1u, abort_flag);
       ++ai;
       if (!ok) break;
       tc_fence_after();
-      const float mul = half == 0 ? 1.f : p.scale;
+      const float mul = grp == 0 ? 1.f : p.scale;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         float o[32];
-        tmem_ld32f(tl + 256 + half * 128 + c * 32, o);
+        tmem_ld32f(tl + 256 + grp * 128 + c * 32, o);
         tmem_wait_ld();
         if (key_exists) store_row32(grow + c * 32, o, mul, key_ok);
       }
