@@ -62,12 +62,16 @@ struct BwdParams {
   __nv_bfloat16* dv;
 };
 
-struct Ring2 {
+template <int N>
+struct RingN {
   uint32_t stage = 0, phase = 0;
   __device__ __forceinline__ void next() {
-    if (++stage == 2) { stage = 0; phase ^= 1u; }
+    if (++stage == N) { stage = 0; phase ^= 1u; }
   }
 };
+using Ring2 = RingN<2>;
+constexpr int kKStages = 3;             // dQ kernel: K tiles are held until dQ += dS K
+constexpr int kVStages = 2;             // V tiles only until dP = dO V^T
 
 // Two-slot ring through which the producer hands the item ids it takes from
 // the global counter to the other roles (-1 ends the loop).
@@ -122,8 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* q_s = smem;                    // Q tile
   uint8_t* do_s = smem + kTile;           // dO tile
-  uint8_t* kv_s = smem + 2 * kTile;       // 2 stages of (K tile, V tile)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(kv_s + 2 * 2 * kTile);
+  uint8_t* k_s = smem + 2 * kTile;        // kKStages K tiles
+  uint8_t* v_s = k_s + kKStages * kTile;  // kVStages V tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(v_s + kVStages * kTile);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
   uint64_t* s_full = bars + 2;
@@ -132,10 +137,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   uint64_t* ds_full = bars + 6;           // [2]
   uint64_t* dq_full = bars + 8;
   uint64_t* acc_empty = bars + 9;
-  uint64_t* kv_full = bars + 10;          // [2]
-  uint64_t* kv_empty = bars + 12;         // [2]
-  uint64_t* mma_done = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint64_t* mma_done = bars + 10;
+  uint64_t* k_full = bars + 11;           // [kKStages]
+  uint64_t* k_empty = k_full + kKStages;  // [kKStages]
+  uint64_t* v_full = k_empty + kKStages;  // [kVStages]
+  uint64_t* v_empty = v_full + kVStages;  // [kVStages]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(v_empty + kVStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -150,8 +157,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(dp_full + i), 1);
       mbar_init(smem_u32(ds_full + i), 256);
-      mbar_init(smem_u32(kv_full + i), 1);
-      mbar_init(smem_u32(kv_empty + i), 1);
+    }
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(smem_u32(k_full + i), 1);
+      mbar_init(smem_u32(k_empty + i), 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(smem_u32(v_full + i), 1);
+      mbar_init(smem_u32(v_empty + i), 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -186,9 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   if (warp == 0) {
     // ------------------------------------------------------------ TMA ---
     if (lane == 0) {
-      Ring2 ring;
+      RingN<kKStages> kr;
+      RingN<kVStages> vr;
       uint32_t qi = 0;
-      int q_armed = -1, kv_armed[2] = {-1, -1};     // parity of each barrier's last arming
+      int q_armed = -1, k_armed[kKStages], v_armed[kVStages];     // parity of each barrier's last arming
+      for (int i = 0; i < kKStages; ++i) k_armed[i] = -1;
+      for (int i = 0; i < kVStages; ++i) v_armed[i] = -1;
       bool ok = true;
       for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
         int bl, h, qt, qb, n, L;
@@ -208,23 +224,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         for (int j = 0; j < n && ok; ++j) {
           int kb = __ldg(lst + j);
           if (kb < 0 || kb >= p.nKb) kb = p.nKb;
-          ok = mbar_wait(smem_u32(kv_empty + ring.stage), ring.phase ^ 1u, abort_flag);
+          ok = mbar_wait(smem_u32(k_empty + kr.stage), kr.phase ^ 1u, abort_flag);
           if (!ok) break;
-          const uint32_t fb = smem_u32(kv_full + ring.stage);
-          const uint32_t base = smem_u32(kv_s) + ring.stage * 2 * kTile;
-          mbar_arrive_expect_tx(fb, 2 * kTile);
-          kv_armed[ring.stage] = (int)ring.phase;
-          for (int c = 0; c < 2; ++c) {
-            tma_load_3d(base + c * kChunk, &p.tk[bl], fb, c * 64, kb * kBKb, hk);
-            tma_load_3d(base + kTile + c * kChunk, &p.tv[bl], fb, c * 64, kb * kBKb, hk);
-          }
-          ring.next();
+          uint32_t fb = smem_u32(k_full + kr.stage);
+          uint32_t base = smem_u32(k_s) + kr.stage * kTile;
+          mbar_arrive_expect_tx(fb, kTile);
+          k_armed[kr.stage] = (int)kr.phase;
+          for (int c = 0; c < 2; ++c) tma_load_3d(base + c * kChunk, &p.tk[bl], fb, c * 64, kb * kBKb, hk);
+          kr.next();
+          ok = mbar_wait(smem_u32(v_empty + vr.stage), vr.phase ^ 1u, abort_flag);
+          if (!ok) break;
+          fb = smem_u32(v_full + vr.stage);
+          base = smem_u32(v_s) + vr.stage * kTile;
+          mbar_arrive_expect_tx(fb, kTile);
+          v_armed[vr.stage] = (int)vr.phase;
+          for (int c = 0; c < 2; ++c) tma_load_3d(base + c * kChunk, &p.tv[bl], fb, c * 64, kb * kBKb, hk);
+          vr.next();
         }
       }
       // let this thread's copies land before the CTA can exit
       if (q_armed >= 0) mbar_drain(smem_u32(q_full), (uint32_t)q_armed);
-      for (int i = 0; i < 2; ++i)
-        if (kv_armed[i] >= 0) mbar_drain(smem_u32(kv_full + i), (uint32_t)kv_armed[i]);
+      for (int i = 0; i < kKStages; ++i)
+        if (k_armed[i] >= 0) mbar_drain(smem_u32(k_full + i), (uint32_t)k_armed[i]);
+      for (int i = 0; i < kVStages; ++i)
+        if (v_armed[i] >= 0) mbar_drain(smem_u32(v_full + i), (uint32_t)v_armed[i]);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -232,19 +255,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idesc_mn = idesc_bf16_f32(128, 128, true);
-      Ring2 ring;
+      RingN<kKStages> kr;
+      RingN<kVStages> vr;
       uint32_t qi = 0, ai = 0, sf = 0, dsc[2] = {0u, 0u}, jj = 0;
       bool ok = true;
-      const uint32_t qa = smem_u32(q_s), da = smem_u32(do_s), kva = smem_u32(kv_s);
-      // S = Q K^T into [0, 128), dP = dO V^T into buffer `buf`
-      auto issue_s_dp = [&](uint32_t kt, uint32_t buf) {
+      const uint32_t qa = smem_u32(q_s), da = smem_u32(do_s), ka = smem_u32(k_s), va = smem_u32(v_s);
+      // S = Q K^T into [0, 128), dP = dO V^T into buffer `buf`; frees the V stage.
+      // Waits for the block's K and V tiles; returns the K stage.
+      auto issue_s_dp = [&](uint32_t buf, uint32_t& kst) {
+        kst = kr.stage;
+        if (!mbar_wait(smem_u32(k_full + kst), kr.phase, abort_flag)) return false;
+        kr.next();
+        const uint32_t vst = vr.stage;
+        if (!mbar_wait(smem_u32(v_full + vst), vr.phase, abort_flag)) return false;
+        vr.next();
+        tc_fence_after();
+        const uint32_t kt = ka + kst * kTile, vt = va + vst * kTile;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem, kmaj(qa, kk), kmaj(kt, kk), idesc_s, kk > 0);
         mma_commit(smem_u32(s_full));
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + 128 + buf * 128, kmaj(da, kk), kmaj(kt + kTile, kk), idesc_s, kk > 0);
+          mma_ss(tmem + 128 + buf * 128, kmaj(da, kk), kmaj(vt, kk), idesc_s, kk > 0);
         mma_commit(smem_u32(dp_full + buf));
+        mma_commit(smem_u32(v_empty + vst));
+        return true;
       };
       // dQ += dS K (dS bf16 of keys 64 g + .. at buffer column 64 g; K as the MN-major B)
       auto issue_dq = [&](uint32_t kt, uint32_t buf, bool first) {
@@ -263,13 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         ++qi;
         if (!ok) break;
         // block 0's S and dP
-        uint32_t st = ring.stage;
-        ok = mbar_wait(smem_u32(kv_full + st), ring.phase, abort_flag);
-        ring.next();
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t kt = kva + st * 2 * kTile;
-        issue_s_dp(kt, jj & 1u);
+        uint32_t kst = 0;
+        if (!(ok = issue_s_dp(jj & 1u, kst))) break;
         if (n == 1) mma_commit(smem_u32(q_empty));
         for (int j = 0; j < n && ok; ++j, ++jj) {
           const uint32_t buf = jj & 1u;
@@ -278,25 +308,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
           ++sf;
           if (!ok) break;
           tc_fence_after();
-          uint32_t nst = 0, nkt = 0;
+          uint32_t nkst = 0;
           if (j + 1 < n) {
-            nst = ring.stage;
-            ok = mbar_wait(smem_u32(kv_full + nst), ring.phase, abort_flag);
-            ring.next();
-            if (!ok) break;
-            tc_fence_after();
-            nkt = kva + nst * 2 * kTile;
-            issue_s_dp(nkt, buf ^ 1u);
+            if (!(ok = issue_s_dp(buf ^ 1u, nkst))) break;
             if (j + 2 == n) mma_commit(smem_u32(q_empty));
           }
           ok = mbar_wait(smem_u32(ds_full + buf), dsc[buf] & 1u, abort_flag);
           ++dsc[buf];
           if (!ok) break;
           tc_fence_after();
-          issue_dq(kt, buf, j == 0);
-          mma_commit(smem_u32(kv_empty + st));
-          st = nst;
-          kt = nkt;
+          issue_dq(ka + kst * kTile, buf, j == 0);
+          mma_commit(smem_u32(k_empty + kst));
+          kst = nkst;
         }
         if (!ok) break;
         mma_commit(smem_u32(dq_full));
@@ -902,7 +925,8 @@ bsa_status encode(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int
   return BSA_OK;
 }
 
-constexpr int kDqSmem = 2 * kTile + 2 * 2 * kTile + 256 + 1024;              // tiles, barriers, alignment
+constexpr int kDqSmem = (2 + kKStages + kVStages) * kTile + 256 + 1024;     // tiles, barriers, alignment
+static_assert(kDqSmem <= 232448, "dQ kernel shared memory above the per-block limit");
 constexpr int kDkvSmem = 2 * kTile + 2 * (2 * kTile + kRowStat) + 256 + 1024;
 
 }  // namespace
