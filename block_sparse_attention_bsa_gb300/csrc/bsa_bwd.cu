@@ -114,12 +114,13 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* o, 
 }
 
 // ---------------------------------------------------------------- dQ ---
-// TMEM: S in [0, 128); dP of key block j in buffer j % 2 at [128, 256) or
+// TMEM: S of key block j in buffer j % 2 at [0, 128) or [128, 256); dP in
 // [256, 384), overwritten in place by dS (bf16, 32 columns per 64 keys);
 // dQ accumulates in [384, 512).  The two elementwise warpgroups split the
 // 128 keys of a block (group g: keys 64 g .. 64 g + 63) and keep P in
-// registers between the exponentials (which free S for the next block's
-// S MMA) and dS.  Issue order: S(j+1), dP(j+1), dQ(j), ...
+// registers between the exponentials and dS.  Issue order: S(j+1), dQ(j),
+// dP(j+1), S(j+2), ...: block j+1's exponentials overlap dQ(j), dP(j+1)
+// and S(j+2).
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -131,10 +132,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   uint64_t* bars = reinterpret_cast<uint64_t*>(v_s + kVStages * kTile);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* s_full = bars + 2;
-  uint64_t* s_free = bars + 3;
-  uint64_t* dp_full = bars + 4;           // [2] per dP buffer
-  uint64_t* ds_full = bars + 6;           // [2]
+  uint64_t* s_full = bars + 2;            // [2] per S buffer
+  uint64_t* dp_full = bars + 4;
+  uint64_t* ds_full = bars + 5;
   uint64_t* dq_full = bars + 8;
   uint64_t* acc_empty = bars + 9;
   uint64_t* mma_done = bars + 10;
@@ -149,15 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
     mbar_init(smem_u32(q_empty), 1);
-    mbar_init(smem_u32(s_full), 1);
-    mbar_init(smem_u32(s_free), 256);
+    mbar_init(smem_u32(dp_full), 1);
+    mbar_init(smem_u32(ds_full), 256);
     mbar_init(smem_u32(dq_full), 1);
     mbar_init(smem_u32(acc_empty), 256);
     mbar_init(smem_u32(mma_done), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(dp_full + i), 1);
-      mbar_init(smem_u32(ds_full + i), 256);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(s_full + i), 1);
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(smem_u32(k_full + i), 1);
       mbar_init(smem_u32(k_empty + i), 1);
@@ -257,35 +254,39 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       constexpr uint32_t idesc_mn = idesc_bf16_f32(128, 128, true);
       RingN<kKStages> kr;
       RingN<kVStages> vr;
-      uint32_t qi = 0, ai = 0, sf = 0, dsc[2] = {0u, 0u}, jj = 0;
+      uint32_t qi = 0, ai = 0, dsc = 0, jj = 0;
       bool ok = true;
       const uint32_t qa = smem_u32(q_s), da = smem_u32(do_s), ka = smem_u32(k_s), va = smem_u32(v_s);
-      // S = Q K^T into [0, 128), dP = dO V^T into buffer `buf`; frees the V stage.
-      // Waits for the block's K and V tiles; returns the K stage.
-      auto issue_s_dp = [&](uint32_t buf, uint32_t& kst) {
+      // S = Q K^T into S buffer `buf`; waits for the block's K tile, returns its stage
+      auto issue_s = [&](uint32_t buf, uint32_t& kst) {
         kst = kr.stage;
         if (!mbar_wait(smem_u32(k_full + kst), kr.phase, abort_flag)) return false;
         kr.next();
+        tc_fence_after();
+        const uint32_t kt = ka + kst * kTile;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem + buf * 128, kmaj(qa, kk), kmaj(kt, kk), idesc_s, kk > 0);
+        mma_commit(smem_u32(s_full + buf));
+        return true;
+      };
+      // dP = dO V^T into [256, 384); waits for the block's V tile and frees it
+      auto issue_dp = [&]() {
         const uint32_t vst = vr.stage;
         if (!mbar_wait(smem_u32(v_full + vst), vr.phase, abort_flag)) return false;
         vr.next();
         tc_fence_after();
-        const uint32_t kt = ka + kst * kTile, vt = va + vst * kTile;
+        const uint32_t vt = va + vst * kTile;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem, kmaj(qa, kk), kmaj(kt, kk), idesc_s, kk > 0);
-        mma_commit(smem_u32(s_full));
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + 128 + buf * 128, kmaj(da, kk), kmaj(vt, kk), idesc_s, kk > 0);
-        mma_commit(smem_u32(dp_full + buf));
+        for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem + 256, kmaj(da, kk), kmaj(vt, kk), idesc_s, kk > 0);
+        mma_commit(smem_u32(dp_full));
         mma_commit(smem_u32(v_empty + vst));
         return true;
       };
-      // dQ += dS K (dS bf16 of keys 64 g + .. at buffer column 64 g; K as the MN-major B)
-      auto issue_dq = [&](uint32_t kt, uint32_t buf, bool first) {
+      // dQ += dS K (dS bf16 of keys 64 g + .. at dP column 64 g; K as the MN-major B)
+      auto issue_dq = [&](uint32_t kt, bool first) {
 #pragma unroll
         for (int kk = 0; kk < kBKb / 16; ++kk)
-          mma_ts(tmem + 384, tmem + 128 + buf * 128 + (kk / 4) * 64 + (kk % 4) * 8, mnmaj(kt, kk), idesc_mn,
+          mma_ts(tmem + 384, tmem + 256 + (kk / 4) * 64 + (kk % 4) * 8, mnmaj(kt, kk), idesc_mn,
                  (first && kk == 0) ? 0u : 1u);
       };
       for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
@@ -299,26 +300,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         if (!ok) break;
         // block 0's S and dP
         uint32_t kst = 0;
-        if (!(ok = issue_s_dp(jj & 1u, kst))) break;
+        if (!(ok = issue_s(jj & 1u, kst))) break;
+        if (!(ok = issue_dp())) break;
         if (n == 1) mma_commit(smem_u32(q_empty));
         for (int j = 0; j < n && ok; ++j, ++jj) {
-          const uint32_t buf = jj & 1u;
-          // S is free once both groups hold P(j) in registers
-          ok = mbar_wait(smem_u32(s_free), sf & 1u, abort_flag);
-          ++sf;
+          // S(j+1) goes to the other buffer, whose S(j-1) the elementwise
+          // groups finished with before dS(j-1) (waited for below, last block)
+          uint32_t nkst = 0;
+          if (j + 1 < n && !(ok = issue_s((jj + 1) & 1u, nkst))) break;
+          ok = mbar_wait(smem_u32(ds_full), dsc & 1u, abort_flag);
+          ++dsc;
           if (!ok) break;
           tc_fence_after();
-          uint32_t nkst = 0;
+          issue_dq(ka + kst * kTile, j == 0);
+          mma_commit(smem_u32(k_empty + kst));
           if (j + 1 < n) {
-            if (!(ok = issue_s_dp(buf ^ 1u, nkst))) break;
+            if (!(ok = issue_dp())) break;
             if (j + 2 == n) mma_commit(smem_u32(q_empty));
           }
-          ok = mbar_wait(smem_u32(ds_full + buf), dsc[buf] & 1u, abort_flag);
-          ++dsc[buf];
-          if (!ok) break;
-          tc_fence_after();
-          issue_dq(ka + kst * kTile, buf, j == 0);
-          mma_commit(smem_u32(k_empty + kst));
           kst = nkst;
         }
         if (!ok) break;
@@ -334,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     const int wq = warp % 4;
     const int r = wq * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    uint32_t sc = 0, oi = 0, jj = 0;
+    uint32_t oi = 0, jj = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
       int bl, h, qt, qb, n, L;
@@ -362,8 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         // keys of this group's half below the end of the sequence (a block holding the end only)
         const int kvalid = valid_kv - kb * kBKb - grp * 64;
         const bool all_valid = kvalid >= 64;
-        ok = mbar_wait(smem_u32(s_full), sc & 1u, abort_flag);
-        ++sc;
+        ok = mbar_wait(smem_u32(s_full + buf), (jj >> 1) & 1u, abort_flag);
         if (!ok) break;
         tc_fence_after();
         // P = 2^(S scale log2(e) - lse log2(e)), kept in registers
@@ -371,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           float s[32];
-          tmem_ld32f(tl + grp * 64 + c * 32, s);
+          tmem_ld32f(tl + buf * 128 + grp * 64 + c * 32, s);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -380,17 +378,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             pr[c * 32 + 2 * i + 1] = ex2_approx(x.y);
           }
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(s_free));
         if (!all_valid) {
 #pragma unroll
           for (int i = 0; i < 64; ++i) pr[i] = i < kvalid ? pr[i] : 0.f;
         }
         // dS = P (dP - D), written over this group's dP columns
-        ok = mbar_wait(smem_u32(dp_full + buf), (jj >> 1) & 1u, abort_flag);
+        ok = mbar_wait(smem_u32(dp_full), jj & 1u, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t tb = tl + 128 + buf * 128 + grp * 64;
+        const uint32_t tb = tl + 256 + grp * 64;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           float dp[32];
@@ -407,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(ds_full + buf));
+        mbar_arrive(smem_u32(ds_full));
       }
       if (!ok) break;
       ok = mbar_wait(smem_u32(dq_full), oi & 1u, abort_flag);
