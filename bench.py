@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="also time bsa_backward (dQ, dK, dV) on the step's outputs and report it")
     ap.add_argument("--schedule", choices=["cosmos3", "h3"], default=None,
                     help="time the dense pass and the sparse step and report a dense->sparse schedule")
     return ap.parse_args()
@@ -64,9 +66,8 @@ def peaks():
 # launch, from an ncu capture of the build whose FMHA sources hash to `sha`.
 # When the sources change the figure no longer applies and traffic is null.
 FMHA_TRAFFIC = {
-    "sha": "f68df8a7ab548f42",
-    "720p_75": 14.24e9 + 1.78e9,          # profiles/launches_720p_75.md (1-pass capture)
-    "480p_75": 504364544 + 267939072,     # profiles/fmha_fwd_480p_75.md
+    "sha": "af3445d2b8cae8a7",
+    "720p_75": 13861869824 + 1741903616,  # profiles/launches_720p_75.md (1-pass capture)
 }
 
 
@@ -94,14 +95,7 @@ def fmha_traffic(cfg, counts):
         return None, "forward kernel changed since the last ncu capture"
     if cfg.name in FMHA_TRAFFIC:
         return float(FMHA_TRAFFIC[cfg.name]), f"ncu capture of {cfg.name}"
-    from bsa_inputs import CONFIGS
-    ref = CONFIGS["480p_75"]
-    import numpy as np
-    # scale the 480p capture by algorithmic bytes (traffic tracks Q/K/V/O sizes)
-    ref_counts = np.full(1, 4536 * 99)
-    ratio = FMHA_TRAFFIC["480p_75"] / algorithmic_bytes(ref, ref_counts)
-    return ratio * algorithmic_bytes(cfg, counts), (
-        f"480p_75 ncu capture scaled by algorithmic bytes (traffic/algorithmic = {ratio:.3f} there)")
+    return None, f"no ncu capture of {cfg.name} for this build"
 
 
 def tile_flops(counts, d, bq, bk) -> float:
@@ -512,6 +506,43 @@ def main():
         e2e = {"value": whole_job_tflops(flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    # ---- backward pass (dQ, dK, dV) over the same lists, outputs and LSE ----
+    bwd = None
+    if args.backward:
+        if d != 128 or bk != 128 or bq not in (128, 256):
+            bwd = {"unavailable": "bsa_backward supports d=128, block_k=128, block_q 128 or 256"}
+        else:
+            g = torch.Generator(device="cuda").manual_seed(cfg.seed + 11)
+            dout = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            bws = torch.empty(bsa.bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, bq, bk), dtype=torch.uint8,
+                              device="cuda")
+
+            def bstep():
+                bsa.bsa_backward(q, k, v, out, dout, lse, idx, cnt, P, lens, bq, bk, dq=dq, dk=dk, dv=dv,
+                                 workspace=bws, stream=stream)
+
+            for _ in range(3):
+                bstep()
+            bsa.bsa_device_status(stream)
+            n_b = max(3, min(args.steps, 10))
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(n_b):
+                bstep()
+            b_.record(stream)
+            torch.cuda.synchronize()
+            bsa.bsa_device_status(stream)
+            b_ms = max_over_ranks(a.elapsed_time(b_) / n_b, device="cuda")
+            # 5 GEMM-equivalents per (row, key) pair (S, dP, dV, dK, dQ) = 2.5x the forward's 2
+            b_flops = 2.5 * flops
+            b_tf = b_flops / (b_ms * 1e-3) / 1e12
+            bwd = {"ms": b_ms, "tflops_effective": b_tf, "frac_of_bf16_peak": b_tf / pk["bf16"],
+                   "flops_note": "10*d per selected (row, key) pair; the kernels issue 14*d (S and dP are "
+                                 "computed by both the dQ and the dK/dV kernel, no atomics)",
+                   "launches": 5, "calls": n_b, "dout": "seeded N(0,1) bf16"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, idx, cnt)
@@ -539,6 +570,7 @@ def main():
                          "algorithmic_flops": flops},
             "clocks": clocks,
             "e2e": e2e,
+            **({"backward": bwd} if bwd is not None else {}),
             "cpu_baseline": cpu,
             "gpu_launches": launches_per_step * args.steps,
         }
