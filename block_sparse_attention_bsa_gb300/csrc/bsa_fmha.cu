@@ -108,7 +108,9 @@ constexpr int kEntryBlockMask = (1 << 24) - 1;
 constexpr int kEntryGroupShift = 24;
 
 struct TileInfo {
-  int bl, b, qb, h, hk, L, valid_kv, n;
+  int bl, b, qb, h, hk, L, valid_kv;
+  int n;          // list entries (key blocks of the lists' geometry)
+  int steps;      // key tiles the kernel walks: n, or ceil(n / 2) when 64-key blocks are paired
   const int32_t* idx;
 };
 
@@ -118,7 +120,7 @@ struct TileInfo {
 // GQA siblings are innermost, then neighbouring query blocks.  The CTAs
 // running at any moment therefore share one KV head's K/V (<= 90 MB at
 // 720p), which stays resident in the 126 MB L2.
-__device__ __forceinline__ TileInfo decode_tile(const FmhaParams& p, int t, int BK) {
+__device__ __forceinline__ TileInfo decode_tile(const FmhaParams& p, int t, int KB, int BK) {
   TileInfo ti;
   const int per_group = p.G * p.nQb;
   const int gi = t / per_group;
@@ -138,12 +140,13 @@ __device__ __forceinline__ TileInfo decode_tile(const FmhaParams& p, int t, int 
   } else if (p.indices == nullptr) {
     // dense pass; a causal pass stops at the block holding the block's last row
     const int kv_end = p.causal ? min(ti.valid_kv, min((ti.qb + 1) * p.block_q, ti.L)) : ti.valid_kv;
-    ti.n = (kv_end + BK - 1) / BK;
+    ti.n = (kv_end + KB - 1) / KB;
   } else {
     const int c = p.counts[row];
     ti.n = c < 0 ? 0 : (c > p.nKb ? p.nKb : c);
   }
   ti.idx = p.indices ? p.indices + row * p.nKb : nullptr;
+  ti.steps = KB < BK ? (ti.n + 1) / 2 : ti.n;
   return ti;
 }
 
@@ -172,9 +175,14 @@ struct TileRing {
   }
 };
 
-template <int D, int BK, int NH>
+// BK is the key tile of the MMAs (128); KB the key block of the lists.  With
+// KB = 64 two consecutive list entries fill one 128-key tile (rows 0..63 and
+// 64..127 of the K/V stage), so the S MMA stays 128 wide (a 64-wide MMA
+// costs as long as a 128-wide one) and each half is masked on its own.
+template <int D, int BK, int NH, int KB = BK>
 __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ FmhaParams p) {
+  static_assert(KB == BK || (KB == 64 && BK == 128), "key block pairing");
   using C = Cfg<D, BK, NH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       t = __shfl_sync(0xffffffffu, t, 0);
       tr.next();
       if (!ok || t < 0) break;
-      const TileInfo ti = decode_tile(p, t, BK);
+      const TileInfo ti = decode_tile(p, t, KB, BK);
       if (ti.n == 0) continue;
       if (lane == 0) {
         ok = mbar_wait(smem_u32(q_empty), (qi & 1u) ^ 1u, abort_flag);
@@ -280,9 +288,16 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
         int my_kb = ti.idx ? (j0 + lane < ti.n ? __ldg(ti.idx + j0 + lane) : 0) : j0 + lane;
         if (p.masked) my_kb &= kEntryBlockMask;
         const int m = min(32, ti.n - j0);
-        for (int jj = 0; jj < m && ok; ++jj) {
+        for (int jj = 0; jj < m && ok; jj += BK / KB) {
           int kb = __shfl_sync(0xffffffffu, my_kb, jj);
           if (kb < 0 || kb >= p.nKb) kb = p.nKb;   // out of range: rows past the end read zeros
+          // paired 64-key blocks: the second entry of the pair (past the end
+          // of the list, the block past the end: zeros, fully masked)
+          int kb1 = p.nKb;
+          if constexpr (KB < BK) {
+            const int t1 = __shfl_sync(0xffffffffu, my_kb, (jj + 1) & 31);
+            if (jj + 1 < m && t1 >= 0 && t1 < p.nKb) kb1 = t1;
+          }
           if (lane == 0) {
 #if BSA_KV_PAIR
             // K at the stage base, V right after it; one barrier for both.
@@ -292,13 +307,20 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
               mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
               for (int which = 0; which < 2; ++which) {
                 const CUtensorMap* tm = which == 0 ? &p.tk[ti.bl] : &p.tv[ti.bl];
-                for (int c = 0; c < C::kChunks; ++c)
-                  tma_load_3d(kv_base + ring.stage * C::kStageBytes + which * C::kTileBytes + c * (BK * 128),
-                              tm, fb, c * 64, kb * BK, ti.hk);
+                for (int c = 0; c < C::kChunks; ++c) {
+                  const uint32_t dst = kv_base + ring.stage * C::kStageBytes + which * C::kTileBytes + c * (BK * 128);
+                  if constexpr (KB == BK) {
+                    tma_load_3d(dst, tm, fb, c * 64, kb * BK, ti.hk);
+                  } else {            // rows 0..63 from the first block, 64..127 from the second
+                    tma_load_3d(dst, tm, fb, c * 64, kb * KB, ti.hk);
+                    tma_load_3d(dst + KB * 128, tm, fb, c * 64, kb1 * KB, ti.hk);
+                  }
+                }
               }
               ring.next<C::kStages>();
             }
 #else
+            static_assert(KB == BK, "64-key pairing needs K and V in one stage");
             for (int which = 0; which < 2 && ok; ++which) {
               ok = mbar_wait(smem_u32(kv_empty + ring.stage), ring.phase ^ 1u, abort_flag);
               if (!ok) break;
@@ -366,8 +388,8 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       while (ok) {
         const int t = tr.take(tile_full, tile_empty, tile_ids, abort_flag, ok);
         if (t < 0) break;
-        const TileInfo ti = decode_tile(p, t, BK);
-        const int n = ti.n;
+        const TileInfo ti = decode_tile(p, t, KB, BK);
+        const int n = ti.steps;
         if (n == 0) continue;
         ok = mbar_wait(smem_u32(q_full), qi & 1u, abort_flag);
         ++qi;
@@ -484,7 +506,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
     while (ok) {
       const int t = tr.take(tile_full, tile_empty, tile_ids, abort_flag, ok);
       if (t < 0) break;
-      const TileInfo ti = decode_tile(p, t, BK);
+      const TileInfo ti = decode_tile(p, t, KB, BK);
       const int row_in_blk = hh * 128 + r;
       const int row = ti.qb * p.block_q + row_in_blk;
       const bool row_exists = row_in_blk < p.block_q && row < p.Sq;
@@ -502,13 +524,22 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       }
       float m_ref = -INFINITY;
       float l = 0.f;
-      for (int j = 0; j < ti.n; ++j) {
-        const int entry = ti.idx ? __ldg(ti.idx + j) : j;
+      // list entry e -> key block this row attends (the block past the end,
+      // i.e. fully masked, when out of range or not selected by the row's
+      // own query block in a merged list)
+      auto entry_block = [&](int e) {
+        if (e >= ti.n) return p.nKb;
+        const int entry = ti.idx ? __ldg(ti.idx + e) : e;
         int kb = (ti.idx && p.masked) ? (entry & kEntryBlockMask) : entry;
         if (kb < 0 || kb >= p.nKb) kb = p.nKb;     // same clamp as the producer: fully masked
         // merged lists: a key block that this row's own query block did not
         // select is masked whole (it contributes exact zeros)
         if (p.masked && !((entry >> (kEntryGroupShift + row_in_blk / p.group_rows)) & 1)) kb = p.nKb;
+        return kb;
+      };
+      for (int j = 0; j < ti.steps; ++j) {
+        const int kb = entry_block(KB < BK ? 2 * j : j);
+        const int kb1 = KB < BK ? entry_block(2 * j + 1) : 0;    // second 64-key half of the tile
         ok = mbar_wait(smem_u32(s_full + hh), sph & 1u, abort_flag);
         ++sph;
         if (!ok) break;
@@ -520,11 +551,22 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
         // keys of this block this row may see: the real keys, and in a causal
         // pass only positions <= the row
         const int kv_end = p.causal ? min(ti.valid_kv, row + 1) : ti.valid_kv;
-        const int kvalid = kv_end - kb * BK;
-        if (kvalid < BK) {
+        if constexpr (KB == BK) {
+          const int kvalid = kv_end - kb * BK;
+          if (kvalid < BK) {
 #pragma unroll
-          for (int c = 0; c < BK; ++c)
-            if (c >= kvalid) s[c] = -INFINITY;
+            for (int c = 0; c < BK; ++c)
+              if (c >= kvalid) s[c] = -INFINITY;
+          }
+        } else {
+          const int kvalid0 = kv_end - kb * KB, kvalid1 = kv_end - kb1 * KB;
+          if (kvalid0 < KB || kvalid1 < KB) {
+#pragma unroll
+            for (int c = 0; c < KB; ++c) {
+              if (c >= kvalid0) s[c] = -INFINITY;
+              if (c >= kvalid1) s[KB + c] = -INFINITY;
+            }
+          }
         }
         // Row max: four independent chains of three-input max.
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
@@ -735,7 +777,7 @@ bsa_status encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H,
   return BSA_OK;
 }
 
-template <int D, int BK, int NH>
+template <int D, int BK, int NH, int KB = BK>
 bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
   using C = Cfg<D, BK, NH>;
   static bool attr_set[64] = {false};
@@ -743,7 +785,7 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
   cudaGetDevice(&dev);
   bsa_status st;
   if (dev < 64 && !attr_set[dev]) {
-    if ((st = cuda_check(cudaFuncSetAttribute(fmha_fwd_kernel<D, BK, NH>,
+    if ((st = cuda_check(cudaFuncSetAttribute(fmha_fwd_kernel<D, BK, NH, KB>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               C::kSmemBytes),
                          "cudaFuncSetAttribute(fmha_fwd_kernel)")) != BSA_OK)
@@ -763,9 +805,9 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
       const char* kb = static_cast<const char*>(a.k) + (int64_t)b * a.k_sb * 2;
       const char* vb = static_cast<const char*>(a.v) + (int64_t)b * a.v_sb * 2;
       if ((st = encode_map(&p.tq[i], qb, L, a.Hq, D, a.q_ss, a.q_sh, 128, "Q")) != BSA_OK) return st;
-      if ((st = encode_map(&p.tk[i], kb, a.prefix_len + L, a.Hkv, D, a.k_ss, a.k_sh, BK, "K")) != BSA_OK)
+      if ((st = encode_map(&p.tk[i], kb, a.prefix_len + L, a.Hkv, D, a.k_ss, a.k_sh, KB, "K")) != BSA_OK)
         return st;
-      if ((st = encode_map(&p.tv[i], vb, a.prefix_len + L, a.Hkv, D, a.v_ss, a.v_sh, BK, "V")) != BSA_OK)
+      if ((st = encode_map(&p.tv[i], vb, a.prefix_len + L, a.Hkv, D, a.v_ss, a.v_sh, KB, "V")) != BSA_OK)
         return st;
     }
     p.b0 = b0;
@@ -796,13 +838,13 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
     sp.counts = a.indices ? a.counts : nullptr;
     sp.causal = a.causal ? 1 : 0;
     sp.b0 = b0; sp.Bn = Bn; sp.Hq = a.Hq; sp.Hkv = a.Hkv; sp.G = a.Hq / a.Hkv;
-    sp.nQb = a.nQb; sp.nKb = a.nKb; sp.block_q = a.block_q; sp.block_k = BK; sp.prefix_len = a.prefix_len;
+    sp.nQb = a.nQb; sp.nKb = a.nKb; sp.block_q = a.block_q; sp.block_k = KB; sp.prefix_len = a.prefix_len;
     for (int i = 0; i < Bn; ++i) sp.seq_lens[i] = p.seq_lens[i];
     sp.counter = p.counter;
     sp.order = const_cast<int*>(p.group_order);
     schedule_kernel<<<1, 1024, 0, stream>>>(sp);
     if ((st = cuda_check(cudaGetLastError(), "schedule_kernel launch")) != BSA_OK) return st;
-    fmha_fwd_kernel<D, BK, NH><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
+    fmha_fwd_kernel<D, BK, NH, KB><<<grid, C::kThreads, C::kSmemBytes, stream>>>(p);
     if ((st = cuda_check(cudaGetLastError(), "fmha_fwd_kernel launch")) != BSA_OK) return st;
   }
   return BSA_OK;
@@ -918,9 +960,9 @@ bsa_status launch_forward(const ForwardArgs& a_in, cudaStream_t stream) {
     a.nQb = nSb;
   }
   if (a.d == 128 && a.block_k == 128) return launch_t<128, 128, 2>(a, stream);
-  if (a.d == 128 && a.block_k == 64) return launch_t<128, 64, 2>(a, stream);
+  if (a.d == 128 && a.block_k == 64) return launch_t<128, 128, 2, 64>(a, stream);   // paired 64-key blocks
   if (a.d == 64 && a.block_k == 128) return launch_t<64, 128, 2>(a, stream);
-  if (a.d == 64 && a.block_k == 64) return launch_t<64, 64, 2>(a, stream);
+  if (a.d == 64 && a.block_k == 64) return launch_t<64, 128, 2, 64>(a, stream);
   return set_error(BSA_ERR_UNSUPPORTED, "bsa_forward: unsupported (d, block_k)");
 }
 

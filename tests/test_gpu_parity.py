@@ -206,8 +206,16 @@ def test_merged_small_query_blocks_match_per_block_lists(name):
         out_g, lse_g = run_forward(inp, idx, cnt_g)
         for qb in range(g, cnt.shape[2], ratio):
             r0, r1 = qb * c.block_q, min((qb + 1) * c.block_q, c.Sq)
-            assert torch.equal(out[:, r0:r1], out_g[:, r0:r1])
-            assert torch.equal(lse[:, :, r0:r1], lse_g[:, :, r0:r1])
+            if c.block_k == 128:
+                assert torch.equal(out[:, r0:r1], out_g[:, r0:r1])
+                assert torch.equal(lse[:, :, r0:r1], lse_g[:, :, r0:r1])
+            else:
+                # 64-key blocks are attended two per 128-key tile, in list
+                # order, so the pairs (and the fp32 order of the row sums)
+                # follow the list: equal up to rounding.  A row that saw
+                # another block's selection would differ by far more.
+                assert torch.allclose(out[:, r0:r1].float(), out_g[:, r0:r1].float(), rtol=1e-2, atol=1e-3)
+                assert torch.allclose(lse[:, :, r0:r1], lse_g[:, :, r0:r1], rtol=0, atol=1e-4)
 
 
 def test_keep_zero_without_prefix_gives_empty_rows():
