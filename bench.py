@@ -546,39 +546,37 @@ def main():
     # ---- backward pass (dQ, dK, dV) over the same lists, outputs and LSE ----
     bwd = None
     if args.backward:
-        if d != 128 or bk != 128 or bq not in (128, 256):
-            bwd = {"unavailable": "bsa_backward supports d=128, block_k=128, block_q 128 or 256"}
-        else:
-            g = torch.Generator(device="cuda").manual_seed(cfg.seed + 11)
-            dout = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
-            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-            bws = torch.empty(bsa.bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, bq, bk), dtype=torch.uint8,
-                              device="cuda")
+        g = torch.Generator(device="cuda").manual_seed(cfg.seed + 11)
+        dout = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws = torch.empty(bsa.bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, bq, bk), dtype=torch.uint8,
+                          device="cuda")
 
-            def bstep():
-                bsa.bsa_backward(q, k, v, out, dout, lse, idx, cnt, P, lens, bq, bk, dq=dq, dk=dk, dv=dv,
-                                 workspace=bws, stream=stream)
+        def bstep():
+            bsa.bsa_backward(q, k, v, out, dout, lse, idx, cnt, P, lens, bq, bk, dq=dq, dk=dk, dv=dv,
+                             workspace=bws, stream=stream)
 
-            for _ in range(3):
-                bstep()
-            bsa.bsa_device_status(stream)
-            n_b = max(3, min(args.steps, 10))
-            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            a.record(stream)
-            for _ in range(n_b):
-                bstep()
-            b_.record(stream)
-            torch.cuda.synchronize()
-            bsa.bsa_device_status(stream)
-            b_ms = max_over_ranks(a.elapsed_time(b_) / n_b, device="cuda")
-            # 5 GEMM-equivalents per (row, key) pair (S, dP, dV, dK, dQ) = 2.5x the forward's 2
-            b_flops = 2.5 * flops
-            b_tf = b_flops / (b_ms * 1e-3) / 1e12
-            bwd = {"ms": b_ms, "tflops_effective": b_tf, "frac_of_bf16_peak": b_tf / pk["bf16"],
-                   "flops_note": "10*d per selected (row, key) pair; the kernels issue 14*d (S and dP are "
-                                 "computed by both the dQ and the dK/dV kernel, no atomics)",
-                   "launches": 5, "calls": n_b, "dout": "seeded N(0,1) bf16"}
+        for _ in range(3):
+            bstep()
+        bsa.bsa_device_status(stream)
+        n_b = max(3, min(args.steps, 10))
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(n_b):
+            bstep()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        bsa.bsa_device_status(stream)
+        b_ms = max_over_ranks(a.elapsed_time(b_) / n_b, device="cuda")
+        # 5 GEMM-equivalents per (row, key) pair (S, dP, dV, dK, dQ) = 2.5x the forward's 2
+        b_flops = 2.5 * flops
+        b_tf = b_flops / (b_ms * 1e-3) / 1e12
+        bwd = {"ms": b_ms, "tflops_effective": b_tf, "frac_of_bf16_peak": b_tf / pk["bf16"],
+               "flops_note": "10*d per selected (row, key) pair; the kernels issue 14*d (S and dP are "
+                             "computed by both the dQ and the dK/dV kernel, no atomics)",
+               "launches": 6, "launch_note": "prep, bitmap, tile lists, inverse lists, dQ, dK/dV (+1 memset)",
+               "calls": n_b, "dout": "seeded N(0,1) bf16"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -349,9 +349,6 @@ bsa_status bsa_backward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tens
     if (t->B != q->B || t->S != q->S || t->H != q->H || t->D != q->D)
       return set_error(BSA_ERR_INVALID_ARG, std::string("bsa_backward: ") + (t == out ? "out" : "dout") +
                                                 " shape differs from q shape");
-  if (q->D != 128 || block_k != 128 || (block_q != 128 && block_q != 256))
-    return set_error(BSA_ERR_UNSUPPORTED, "bsa_backward: supports head dim 128, block_k 128 and block_q 128 or 256; got d=" +
-                                              s(q->D) + ", block_q=" + s(block_q) + ", block_k=" + s(block_k));
   if (!indices || !counts) return set_error(BSA_ERR_INVALID_ARG, "bsa_backward: indices and counts are required");
   if (!lse) return set_error(BSA_ERR_INVALID_ARG, "bsa_backward: lse is NULL");
   if (!dq || !dk || !dv) return set_error(BSA_ERR_INVALID_ARG, "bsa_backward: dq, dk and dv must be non-NULL");
@@ -370,7 +367,7 @@ bsa_status bsa_backward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tens
   a.o = out->ptr; a.o_sb = out->stride_b; a.o_ss = out->stride_s; a.o_sh = out->stride_h;
   a.dout = dout->ptr; a.d_sb = dout->stride_b; a.d_ss = dout->stride_s; a.d_sh = dout->stride_h;
   a.lse = lse;
-  a.B = (int)q->B; a.Hq = (int)q->H; a.Hkv = (int)k->H; a.Sq = (int)q->S; a.Skv = (int)k->S;
+  a.B = (int)q->B; a.Hq = (int)q->H; a.Hkv = (int)k->H; a.Sq = (int)q->S; a.Skv = (int)k->S; a.d = (int)q->D;
   a.block_q = block_q; a.block_k = block_k; a.prefix_len = prefix_len;
   a.seq_lens = seq_lens; a.indices = indices; a.counts = counts;
   a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)q->D);

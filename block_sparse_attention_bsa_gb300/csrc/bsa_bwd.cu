@@ -34,28 +34,39 @@
 namespace bsa {
 namespace {
 
-constexpr int kD = 128;                 // head dim
-constexpr int kBKb = 128;               // key block
 constexpr int kT = 128;                 // query tile rows
+constexpr int kKT = 128;                // key tile
 constexpr int kChunk = 128 * 128;       // 128 rows x 64 bf16 (one 128-byte column chunk)
-constexpr int kTile = 2 * kChunk;       // 128 rows x 128 bf16 = 32 KB
 constexpr int kRowStat = 2 * kT * 4;    // per query tile: -lse * log2(e) [128], -D [128]
+constexpr int kEntryMask = (1 << 24) - 1;   // list entries: tile index | pair mask << 24
+
+// A 128-row tile of Q, dO, K or V: D / 64 swizzled column chunks of 16 KB.
+template <int D>
+struct Tiles {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTile = kChunks * kChunk;
+};
 constexpr int kThreads = 384;           // warp 0 TMA, warp 1 MMA, warps 4..7 / 8..11 elementwise halves
 constexpr float kLog2e = 1.4426950408889634f;
 
+// The selector's lists (any block geometry) are re-expressed on 128 x 128
+// (query tile, key tile) pairs.  A pair's mask has bit 2 i + j set when rows
+// 64 i .. 64 i + 63 of the query tile belong to a query block that listed the
+// key block holding keys 64 j .. 64 j + 63 of the key tile; with 256- or
+// 128-row query blocks and 128-key blocks all four bits are equal.
 struct BwdParams {
   CUtensorMap tq[kMaxFwdBatch];
   CUtensorMap tk[kMaxFwdBatch];
   CUtensorMap tv[kMaxFwdBatch];
   CUtensorMap tdo[kMaxFwdBatch];
   int seq_lens[kMaxFwdBatch];
-  int b0, Bn, Hq, Hkv, G, Sq, Skv, nQb, nKb, nQt, block_q, prefix_len, n_items;
-  const int32_t* indices;     // [B, Hq, nQb, nKb]
-  const int32_t* counts;      // [B, Hq, nQb]
+  int b0, Bn, Hq, Hkv, G, Sq, Skv, nQt, nKt, prefix_len, n_items;
+  const int32_t* dq_list;     // [B, Hq, nQt, nKt]: key tiles kt | mask << 24, ascending
+  const int32_t* dq_cnt;      // [B, Hq, nQt]
   const float* rowstat;       // [B, Hq, nQt, 2, 128]: -lse * log2(e) (-inf on padded rows), -D
   int* counter;               // next dK/dV item (zeroed before the launch)
-  const int32_t* inv_cnt;     // [B, Hkv, nKb]
-  const int32_t* inv_list;    // [B, Hkv, nKb, G * nQb]: listing rows g * nQb + qb, ascending
+  const int32_t* inv_cnt;     // [B, Hkv, nKt]
+  const int32_t* inv_list;    // [B, Hkv, nKt, G * nQt]: rows (g * nQt + qt) | mask << 24, ascending
   float scale, scale_log2;
   __nv_bfloat16* dq;          // [B, Sq, Hq, d]
   __nv_bfloat16* dk;          // [B, Skv, Hkv, d]
@@ -120,8 +131,12 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* o, 
 // 128 keys of a block (group g: keys 64 g .. 64 g + 63) and keep P in
 // registers between the exponentials and dS.  Issue order: S(j+1), dQ(j),
 // dP(j+1), S(j+2), ...: block j+1's exponentials overlap dQ(j), dP(j+1)
-// and S(j+2).
+// and S(j+2).  Entries whose mask excludes a (row half, key half) give P = 0
+// there.
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using T = Tiles<D>;
+  constexpr int kTile = T::kTile;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -175,8 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // item -> (request, KV head, query tile, query head of the group)
-  auto decode = [&](int t, int& bl, int& h, int& qt, int& qb, int& n, int& L) {
+  // item -> (request, KV head, query tile, query head of the group) and its key-tile list
+  auto decode = [&](int t, int& bl, int& h, int& qt, int& n, int& L, const int32_t*& lst) {
     const int g = t % p.G;
     int r = t / p.G;
     qt = r % p.nQt;
@@ -184,13 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     const int hk = r % p.Hkv;
     bl = r / p.Hkv;
     h = hk * p.G + g;
-    qb = qt * kT / p.block_q;
     L = p.seq_lens[bl];
-    n = 0;
-    if (qt * kT < L) {
-      const int c = p.counts[((int64_t)(p.b0 + bl) * p.Hq + h) * p.nQb + qb];
-      n = c < 0 ? 0 : min(c, p.nKb);
-    }
+    const int64_t row = ((int64_t)(p.b0 + bl) * p.Hq + h) * p.nQt + qt;
+    lst = p.dq_list + row * p.nKt;
+    n = qt * kT < L ? min(max(p.dq_cnt[row], 0), p.nKt) : 0;
   };
 
   if (warp == 0) {
@@ -204,30 +216,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       for (int i = 0; i < kVStages; ++i) v_armed[i] = -1;
       bool ok = true;
       for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
-        int bl, h, qt, qb, n, L;
-        decode(t, bl, h, qt, qb, n, L);
+        int bl, h, qt, n, L;
+        const int32_t* lst;
+        decode(t, bl, h, qt, n, L, lst);
         if (n == 0) continue;
         ok = mbar_wait(smem_u32(q_empty), (qi & 1u) ^ 1u, abort_flag);
         if (!ok) break;
         q_armed = (int)(qi & 1u);
         ++qi;
         mbar_arrive_expect_tx(smem_u32(q_full), 2 * kTile);
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < T::kChunks; ++c) {
           tma_load_3d(smem_u32(q_s) + c * kChunk, &p.tq[bl], smem_u32(q_full), c * 64, qt * kT, h);
           tma_load_3d(smem_u32(do_s) + c * kChunk, &p.tdo[bl], smem_u32(q_full), c * 64, qt * kT, h);
         }
-        const int32_t* lst = p.indices + (((int64_t)(p.b0 + bl) * p.Hq + h) * p.nQb + qb) * p.nKb;
         const int hk = h / p.G;
         for (int j = 0; j < n && ok; ++j) {
-          int kb = __ldg(lst + j);
-          if (kb < 0 || kb >= p.nKb) kb = p.nKb;
+          int kb = __ldg(lst + j) & kEntryMask;       // key tile
+          if (kb >= p.nKt) kb = p.nKt;
           ok = mbar_wait(smem_u32(k_empty + kr.stage), kr.phase ^ 1u, abort_flag);
           if (!ok) break;
           uint32_t fb = smem_u32(k_full + kr.stage);
           uint32_t base = smem_u32(k_s) + kr.stage * kTile;
           mbar_arrive_expect_tx(fb, kTile);
           k_armed[kr.stage] = (int)kr.phase;
-          for (int c = 0; c < 2; ++c) tma_load_3d(base + c * kChunk, &p.tk[bl], fb, c * 64, kb * kBKb, hk);
+          for (int c = 0; c < T::kChunks; ++c) tma_load_3d(base + c * kChunk, &p.tk[bl], fb, c * 64, kb * kKT, hk);
           kr.next();
           ok = mbar_wait(smem_u32(v_empty + vr.stage), vr.phase ^ 1u, abort_flag);
           if (!ok) break;
@@ -235,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
           base = smem_u32(v_s) + vr.stage * kTile;
           mbar_arrive_expect_tx(fb, kTile);
           v_armed[vr.stage] = (int)vr.phase;
-          for (int c = 0; c < 2; ++c) tma_load_3d(base + c * kChunk, &p.tv[bl], fb, c * 64, kb * kBKb, hk);
+          for (int c = 0; c < T::kChunks; ++c) tma_load_3d(base + c * kChunk, &p.tv[bl], fb, c * 64, kb * kKT, hk);
           vr.next();
         }
       }
@@ -251,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     // ------------------------------------------------------------ MMA ---
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
-      constexpr uint32_t idesc_mn = idesc_bf16_f32(128, 128, true);
+      constexpr uint32_t idesc_mn = idesc_bf16_f32(128, D, true);
       RingN<kKStages> kr;
       RingN<kVStages> vr;
       uint32_t qi = 0, ai = 0, dsc = 0, jj = 0;
@@ -265,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         tc_fence_after();
         const uint32_t kt = ka + kst * kTile;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem + buf * 128, kmaj(qa, kk), kmaj(kt, kk), idesc_s, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + buf * 128, kmaj(qa, kk), kmaj(kt, kk), idesc_s, kk > 0);
         mma_commit(smem_u32(s_full + buf));
         return true;
       };
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         tc_fence_after();
         const uint32_t vt = va + vst * kTile;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem + 256, kmaj(da, kk), kmaj(vt, kk), idesc_s, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + 256, kmaj(da, kk), kmaj(vt, kk), idesc_s, kk > 0);
         mma_commit(smem_u32(dp_full));
         mma_commit(smem_u32(v_empty + vst));
         return true;
@@ -285,13 +297,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       // dQ += dS K (dS bf16 of keys 64 g + .. at dP column 64 g; K as the MN-major B)
       auto issue_dq = [&](uint32_t kt, bool first) {
 #pragma unroll
-        for (int kk = 0; kk < kBKb / 16; ++kk)
+        for (int kk = 0; kk < kKT / 16; ++kk)
           mma_ts(tmem + 384, tmem + 256 + (kk / 4) * 64 + (kk % 4) * 8, mnmaj(kt, kk), idesc_mn,
                  (first && kk == 0) ? 0u : 1u);
       };
       for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
-        int bl, h, qt, qb, n, L;
-        decode(t, bl, h, qt, qb, n, L);
+        int bl, h, qt, n, L;
+        const int32_t* lst;
+        decode(t, bl, h, qt, n, L, lst);
         if (n == 0) continue;
         ok = mbar_wait(smem_u32(acc_empty), (ai & 1u) ^ 1u, abort_flag);    // last epilogue read dQ
         ++ai;
@@ -336,15 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     uint32_t oi = 0, jj = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.n_items && ok; t += gridDim.x) {
-      int bl, h, qt, qb, n, L;
-      decode(t, bl, h, qt, qb, n, L);
+      int bl, h, qt, n, L;
+      const int32_t* lst;
+      decode(t, bl, h, qt, n, L, lst);
       const int b = p.b0 + bl;
       const int row = qt * kT + r;
       const bool row_exists = row < p.Sq;
       const bool row_ok = row < L;
-      __nv_bfloat16* drow = p.dq + (((int64_t)b * p.Sq + row) * p.Hq + h) * kD;
+      __nv_bfloat16* drow = p.dq + (((int64_t)b * p.Sq + row) * p.Hq + h) * D;
       if (n == 0) {
-        if (row_exists) zero_row(drow, grp * 64, 64);
+        if (row_exists) zero_row(drow, grp * (D / 2), D / 2);
         continue;
       }
       const float* rs = p.rowstat + (((int64_t)b * p.Hq + h) * p.nQt + qt) * (2 * kT);
@@ -353,14 +367,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nl2 = make_float2(nl, nl);
       const float2 nD2 = make_float2(nD, nD);
       const int valid_kv = p.prefix_len + L;
-      const int32_t* lst = p.indices + (((int64_t)b * p.Hq + h) * p.nQb + qb) * p.nKb;
+      const int qhalf = wq >> 1;              // rows 64 qhalf .. of the tile (warp-uniform)
       for (int j = 0; j < n; ++j, ++jj) {
         const uint32_t buf = jj & 1u;
-        int kb = __ldg(lst + j);
-        if (kb < 0 || kb >= p.nKb) kb = p.nKb;
-        // keys of this group's half below the end of the sequence (a block holding the end only)
-        const int kvalid = valid_kv - kb * kBKb - grp * 64;
-        const bool all_valid = kvalid >= 64;
+        const int e = __ldg(lst + j);
+        int kb = e & kEntryMask;
+        if (kb >= p.nKt) kb = p.nKt;
+        // this (row half, key half) pair selected?  keys of this group's half
+        // below the end of the sequence (a tile holding the end only)
+        const bool pair_ok = (e >> (24 + qhalf * 2 + grp)) & 1;
+        const int kvalid = valid_kv - kb * kKT - grp * 64;
+        const bool all_valid = pair_ok && kvalid >= 64;
         ok = mbar_wait(smem_u32(s_full + buf), (jj >> 1) & 1u, abort_flag);
         if (!ok) break;
         tc_fence_after();
@@ -380,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         }
         if (!all_valid) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) pr[i] = i < kvalid ? pr[i] : 0.f;
+          for (int i = 0; i < 64; ++i) pr[i] = (pair_ok && i < kvalid) ? pr[i] : 0.f;
         }
         // dS = P (dP - D), written over this group's dP columns
         ok = mbar_wait(smem_u32(dp_full), jj & 1u, abort_flag);
@@ -411,11 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < D / 64; ++c) {         // group g writes columns g D / 2 ..
         float o[32];
-        tmem_ld32f(tl + 384 + grp * 64 + c * 32, o);
+        tmem_ld32f(tl + 384 + grp * (D / 2) + c * 32, o);
         tmem_wait_ld();
-        if (row_exists) store_row32(drow + grp * 64 + c * 32, o, p.scale, row_ok);
+        if (row_exists) store_row32(drow + grp * (D / 2) + c * 32, o, p.scale, row_ok);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(acc_empty));
@@ -432,11 +449,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 // ------------------------------------------------------------- dK, dV ---
 // TMEM: S^T in [0, 128) (P^T bf16 over it: query columns 64 g .. at column
 // 64 g, 32 wide), dP^T in [128, 256) (dS^T bf16 the same way), dV in
-// [256, 384), dK in [384, 512).  The two elementwise warpgroups split the
+// [256, 256 + D), dK in [256 + D, 256 + 2 D).  The two elementwise warpgroups split the
 // 128 query rows of a step (group g: rows 64 g .. 64 g + 63) and keep P^T
 // in registers between P^T and dS^T.  Issue order: S^T(s), dP^T(s), dV(s),
 // S^T(s+1), dK(s), dP^T(s+1), ...
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using T = Tiles<D>;
+  constexpr int kTile = T::kTile;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -490,24 +510,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int tiles_per_block = p.block_q / kT;
 
-  // item -> (request, KV head, key block); steps = listed query blocks x tiles per block
+  // item -> (request, KV head, key tile); one step per query tile that listed it
   auto decode = [&](int t, int& bl, int& hk, int& kb, int& steps, const int32_t*& lst) {
-    kb = t % p.nKb;
-    const int r = t / p.nKb;
+    kb = t % p.nKt;
+    const int r = t / p.nKt;
     hk = r % p.Hkv;
     bl = r / p.Hkv;
-    const int64_t key = ((int64_t)(p.b0 + bl) * p.Hkv + hk) * p.nKb + kb;
-    steps = p.inv_cnt[key] * tiles_per_block;
-    lst = p.inv_list + key * p.G * p.nQb;
+    const int64_t key = ((int64_t)(p.b0 + bl) * p.Hkv + hk) * p.nKt + kb;
+    steps = min(max(p.inv_cnt[key], 0), p.G * p.nQt);
+    lst = p.inv_list + key * p.G * p.nQt;
   };
   // step s of an item -> (query head, query tile)
   auto step_tile = [&](const int32_t* lst, int hk, int s, int& h, int& qt) {
-    const int e = __ldg(lst + s / tiles_per_block);
-    const int g = e / p.nQb, qb = e - g * p.nQb;
+    const int row = __ldg(lst + s) & kEntryMask;
+    const int g = row / p.nQt;
+    qt = row - g * p.nQt;
     h = hk * p.G + g;
-    qt = qb * tiles_per_block + s % tiles_per_block;
   };
 
   if (warp == 0) {
@@ -535,9 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         kv_armed = (int)(ki & 1u);
         ++ki;
         mbar_arrive_expect_tx(smem_u32(kv_full), 2 * kTile);
-        for (int c = 0; c < 2; ++c) {
-          tma_load_3d(smem_u32(k_s) + c * kChunk, &p.tk[bl], smem_u32(kv_full), c * 64, kb * kBKb, hk);
-          tma_load_3d(smem_u32(v_s) + c * kChunk, &p.tv[bl], smem_u32(kv_full), c * 64, kb * kBKb, hk);
+        for (int c = 0; c < T::kChunks; ++c) {
+          tma_load_3d(smem_u32(k_s) + c * kChunk, &p.tk[bl], smem_u32(kv_full), c * 64, kb * kKT, hk);
+          tma_load_3d(smem_u32(v_s) + c * kChunk, &p.tv[bl], smem_u32(kv_full), c * 64, kb * kKT, hk);
         }
         for (int s = 0; s < steps && ok; ++s) {
           int h, qt;
@@ -548,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
           const uint32_t base = smem_u32(qdo_s) + ring.stage * kStage;
           mbar_arrive_expect_tx(fb, 2 * kTile + kRowStat);
           qdo_armed[ring.stage] = (int)ring.phase;
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < T::kChunks; ++c) {
             tma_load_3d(base + c * kChunk, &p.tq[bl], fb, c * 64, qt * kT, h);
             tma_load_3d(base + kTile + c * kChunk, &p.tdo[bl], fb, c * 64, qt * kT, h);
           }
@@ -566,19 +585,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
-      constexpr uint32_t idesc_mn = idesc_bf16_f32(128, 128, true);
+      constexpr uint32_t idesc_mn = idesc_bf16_f32(128, D, true);
       Ring2 ring;
       uint32_t ki = 0, ai = 0, pc = 0, dc = 0;
       bool ok = true;
       const uint32_t ka = smem_u32(k_s), va = smem_u32(v_s), qda = smem_u32(qdo_s);
       auto issue_st = [&](uint32_t qs) {        // S^T = K Q^T
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) mma_ss(tmem, kmaj(ka, kk), kmaj(qs, kk), idesc_s, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem, kmaj(ka, kk), kmaj(qs, kk), idesc_s, kk > 0);
         mma_commit(smem_u32(s_full));
       };
       auto issue_dpt = [&](uint32_t qs) {       // dP^T = V dO^T
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
+        for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + 128, kmaj(va, kk), kmaj(qs + kTile, kk), idesc_s, kk > 0);
         mma_commit(smem_u32(dp_full));
       };
@@ -592,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
       auto issue_dk = [&](uint32_t qs, bool first) {
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ts(tmem + 384, tmem + 128 + (kk / 4) * 64 + (kk % 4) * 8, mnmaj(qs, kk), idesc_mn,
+          mma_ts(tmem + 256 + D, tmem + 128 + (kk / 4) * 64 + (kk % 4) * 8, mnmaj(qs, kk), idesc_mn,
                  (first && kk == 0) ? 0u : 1u);
       };
       auto wait_stage = [&](uint32_t& qs, uint32_t& st) {
@@ -666,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
       decode(t, bl, hk, kb, steps, lst);
       const int b = p.b0 + bl;
       const int L = p.seq_lens[bl];
-      const int key = kb * kBKb + r;
+      const int key = kb * kKT + r;
       const bool key_exists = key < p.Skv;
       const bool key_ok = key < p.prefix_len + L;
       // keys past the end (zero-filled K/V rows) get P = 0; only the block
@@ -675,9 +694,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
       const float2 km2 = make_float2(key_ok ? 1.f : 0.f, key_ok ? 1.f : 0.f);
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       // group 0 writes dV, group 1 dK
-      __nv_bfloat16* grow = (grp == 0 ? p.dv : p.dk) + (((int64_t)b * p.Skv + key) * p.Hkv + hk) * kD;
+      __nv_bfloat16* grow = (grp == 0 ? p.dv : p.dk) + (((int64_t)b * p.Skv + key) * p.Hkv + hk) * D;
       if (steps == 0) {
-        if (key_exists) zero_row(grow, 0, kD);
+        if (key_exists) zero_row(grow, 0, D);
         continue;
       }
       for (int s = 0; s < steps; ++s) {
@@ -691,6 +710,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         tc_fence_after();
         // per query-row column: -lse log2(e) (-inf on padded rows) and -D
         const float* rs = reinterpret_cast<const float*>(qdo_s + st * kStage + 2 * kTile) + grp * 64;
+        // this group's query-row half and this warp's key half selected as a pair?
+        const bool pair_ok = (__ldg(lst + s) >> (24 + grp * 2 + (wq >> 1))) & 1;
+        const bool need_mask = !(warp_keys_ok && pair_ok);      // warp-uniform
+        const float2 km = pair_ok ? km2 : make_float2(0.f, 0.f);
         // P^T = 2^(S^T scale log2(e) - lse log2(e)), kept in registers; bf16 over S^T
         float pr[64];
 #pragma unroll
@@ -706,9 +729,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             const float2 t1 = __ffma2_rn(make_float2(sv[4 * i + 2], sv[4 * i + 3]), sc2, make_float2(l4.z, l4.w));
             float2 p0 = make_float2(ex2_approx(t0.x), ex2_approx(t0.y));
             float2 p1 = make_float2(ex2_approx(t1.x), ex2_approx(t1.y));
-            if (!warp_keys_ok) {
-              p0 = __fmul2_rn(p0, km2);
-              p1 = __fmul2_rn(p1, km2);
+            if (need_mask) {
+              p0 = __fmul2_rn(p0, km);
+              p1 = __fmul2_rn(p1, km);
             }
             pr[c * 32 + 4 * i] = p0.x;
             pr[c * 32 + 4 * i + 1] = p0.y;
@@ -756,9 +779,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
       tc_fence_after();
       const float mul = grp == 0 ? 1.f : p.scale;
 #pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         float o[32];
-        tmem_ld32f(tl + 256 + grp * 128 + c * 32, o);
+        tmem_ld32f(tl + 256 + grp * D + c * 32, o);
         tmem_wait_ld();
         if (key_exists) store_row32(grow + c * 32, o, mul, key_ok);
       }
@@ -777,8 +800,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 // ------------------------------------------------------- preprocessing ---
 // Per query tile (b, h, qt), 128 values of -lse * log2(e) (-inf on padded
 // rows, so their P is 0) and 128 of -D, D = sum_c dO_c O_c (0 on padded
-// rows), stored together so one bulk copy stages them.  One warp per (b, row, h)
-// over every row of the tiles, 8-byte loads.
+// rows), stored together so one bulk copy stages them.  One warp per
+// (b, row, h) over every row of the tiles; each lane reads D / 32 elements.
 struct PrepParams {
   const __nv_bfloat16* o;
   const __nv_bfloat16* dout;
@@ -789,6 +812,7 @@ struct PrepParams {
   float* rowstat;
 };
 
+template <int D>
 __global__ void bwd_prep_kernel(const __grid_constant__ PrepParams p) {
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
@@ -802,15 +826,13 @@ __global__ void bwd_prep_kernel(const __grid_constant__ PrepParams p) {
   const bool real = row < p.seq_lens[b];
   float acc = 0.f;
   if (real) {
-    const __nv_bfloat16* op = p.o + b * p.o_sb + (int64_t)row * p.o_ss + (int64_t)h * p.o_sh + lane * 4;
-    const __nv_bfloat16* dp = p.dout + b * p.d_sb + (int64_t)row * p.d_ss + (int64_t)h * p.d_sh + lane * 4;
-    const uint2 a = *reinterpret_cast<const uint2*>(op);
-    const uint2 c = *reinterpret_cast<const uint2*>(dp);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(
+        p.o + b * p.o_sb + (int64_t)row * p.o_ss + (int64_t)h * p.o_sh + lane * (D / 32));
+    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(
+        p.dout + b * p.d_sb + (int64_t)row * p.d_ss + (int64_t)h * p.d_sh + lane * (D / 32));
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float2 x = __bfloat1622float2(a2[i]), y = __bfloat1622float2(c2[i]);
+    for (int i = 0; i < D / 64; ++i) {
+      const float2 x = __bfloat1622float2(o2[i]), y = __bfloat1622float2(d2[i]);
       acc = fmaf(x.x, y.x, acc);
       acc = fmaf(x.y, y.y, acc);
     }
@@ -824,16 +846,17 @@ __global__ void bwd_prep_kernel(const __grid_constant__ PrepParams p) {
   }
 }
 
-// ------------------------------------------------------ inverse lists ---
-// Bitmaps: bit (g * nQb + qb, kb) of a KV head is set when query head
-// hk * G + g listed block kb for query block qb (blocks with no real row are
-// skipped).  One warp per list; OR is order-free, so the result is
-// deterministic.
+// ------------------------------------------------------- tile lists ---
+// Four bitmap planes, one per mask bit 2 i + j: row (b, hk, g, qt), bit kt.
+// One warp per selector list (b, h, qb) sets, for every listed key block,
+// the bits of the (query tile, row half) x (key tile, key half) pairs the
+// two blocks cover.  OR is order-free, so the result is deterministic.
 struct BitmapParams {
   const int32_t* indices;
   const int32_t* counts;
-  uint32_t* bm;               // [B, Hkv, G * nQb, words]
-  int B, Hq, Hkv, G, nQb, nKb, block_q, words;
+  uint32_t* planes;           // 4 x [B, Hkv, G, nQt, words]
+  int64_t plane_words;
+  int B, Hq, Hkv, G, nQb, nKb, nQt, nKt, block_q, block_k, words;
   int seq_lens[kMaxSelectBatch];
 };
 
@@ -845,26 +868,91 @@ __global__ void bwd_bitmap_kernel(const __grid_constant__ BitmapParams p) {
   const int qb = (int)(w % p.nQb);
   const int64_t bh = w / p.nQb;
   const int h = (int)(bh % p.Hq), b = (int)(bh / p.Hq);
-  if (qb * p.block_q >= p.seq_lens[b]) return;
+  const int L = p.seq_lens[b];
+  if (qb * p.block_q >= L) return;
   const int hk = h / p.G, g = h - hk * p.G;
+  // query tiles and row halves of this query block (tiles past the last real row skipped)
+  int qt0, nqt, ibits;
+  if (p.block_q == 64) {
+    qt0 = qb >> 1; nqt = 1; ibits = 1 << (qb & 1);
+  } else {
+    qt0 = qb * p.block_q / kT; nqt = p.block_q / kT; ibits = 3;
+  }
   const int c = min(max(p.counts[w], 0), p.nKb);
   const int32_t* lst = p.indices + w * p.nKb;
-  uint32_t* row = p.bm + ((((int64_t)b * p.Hkv + hk) * p.G + g) * p.nQb + qb) * p.words;
+  const int64_t row0 = (((int64_t)b * p.Hkv + hk) * p.G + g) * p.nQt;
   for (int i = lane; i < c; i += 32) {
     const int kb = lst[i];
-    if (kb >= 0 && kb < p.nKb) atomicOr(row + (kb >> 5), 1u << (kb & 31));
+    if (kb < 0 || kb >= p.nKb) continue;
+    const int kt = p.block_k == 64 ? kb >> 1 : kb;
+    const int jbits = p.block_k == 64 ? 1 << (kb & 1) : 3;
+    for (int q = 0; q < nqt; ++q) {
+      const int qt = qt0 + q;
+      if (qt * kT >= L) break;
+      for (int ii = 0; ii < 2; ++ii) {
+        if (!((ibits >> ii) & 1)) continue;
+        for (int jj = 0; jj < 2; ++jj) {
+          if (!((jbits >> jj) & 1)) continue;
+          uint32_t* pl = p.planes + (ii * 2 + jj) * p.plane_words;
+          atomicOr(pl + (row0 + qt) * p.words + (kt >> 5), 1u << (kt & 31));
+        }
+      }
+    }
   }
 }
 
-// One warp per (b, hk, 32 key blocks): reads the bitmap 32 rows at a time
-// (one row per lane), transposes each 32 x 32 bit square with ballots so that
-// lane i holds the rows that listed key block 32 w + i, and appends them in
-// ascending row order to that block's list.
+// One warp per (b, h, qt): the ascending key tiles of its four plane rows,
+// each with its mask (the dQ kernel's lists).
+struct TileListParams {
+  const uint32_t* planes;
+  int64_t plane_words;
+  int32_t* dq_list;
+  int32_t* dq_cnt;
+  int n_rows, nKt, words;
+};
+
+__global__ void bwd_tilelist_kernel(const __grid_constant__ TileListParams p) {
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;   // (b, hk, g, qt) = (b, h, qt)
+  const int lane = threadIdx.x % 32;
+  if (row >= p.n_rows) return;
+  int32_t* out = p.dq_list + row * p.nKt;
+  int running = 0;
+  for (int w0 = 0; w0 < p.words; w0 += 32) {
+    const int w = w0 + lane;
+    uint32_t m[4] = {0u, 0u, 0u, 0u};
+    if (w < p.words)
+      for (int i = 0; i < 4; ++i) m[i] = p.planes[i * p.plane_words + row * p.words + w];
+    uint32_t u = m[0] | m[1] | m[2] | m[3];
+    const int cnt = __popc(u);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int pos = running + incl - cnt;
+    while (u) {
+      const int bit = __ffs(u) - 1;
+      u &= u - 1;
+      int mask = 0;
+      for (int i = 0; i < 4; ++i) mask |= (int)((m[i] >> bit) & 1u) << i;
+      out[pos++] = (w * 32 + bit) | (mask << 24);
+    }
+    running += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) p.dq_cnt[row] = running;
+}
+
+// One warp per (b, hk, 32 key tiles): reads the plane rows 32 at a time (one
+// row per lane), transposes each 32 x 32 bit square with ballots so that lane
+// i holds the rows that selected key tile 32 w + i, and appends them in
+// ascending row order with their masks (the dK/dV kernel's lists).
 struct InvParams {
-  const uint32_t* bm;
+  const uint32_t* planes;
+  int64_t plane_words;
   int32_t* inv_cnt;
   int32_t* inv_list;
-  int n_groups, nrows, nKb, words;
+  int n_groups, nrows, nKt, words;
 };
 
 __global__ void bwd_inverse_kernel(const __grid_constant__ InvParams p) {
@@ -873,32 +961,43 @@ __global__ void bwd_inverse_kernel(const __grid_constant__ InvParams p) {
   if (wid >= (int64_t)p.n_groups * p.words) return;
   const int w = (int)(wid % p.words);
   const int64_t gi = wid / p.words;
-  const uint32_t* bm = p.bm + gi * p.nrows * p.words;
-  const int kb = w * 32 + lane;
-  int32_t* out = p.inv_list + (gi * p.nKb + min(kb, p.nKb - 1)) * p.nrows;
+  const int64_t base = gi * p.nrows * p.words;
+  const int kt = w * 32 + lane;
+  int32_t* out = p.inv_list + (gi * p.nKt + min(kt, p.nKt - 1)) * p.nrows;
   int cnt = 0;
   for (int r0 = 0; r0 < p.nrows; r0 += 32) {
     const int r = r0 + lane;
-    const uint32_t word = r < p.nrows ? bm[(int64_t)r * p.words + w] : 0u;
-    uint32_t mine = 0;
+    uint32_t word[4];
+    for (int i = 0; i < 4; ++i)
+      word[i] = r < p.nrows ? p.planes[i * p.plane_words + base + (int64_t)r * p.words + w] : 0u;
+    uint32_t mine[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int bit = 0; bit < 32; ++bit) {
-      const uint32_t m = __ballot_sync(0xffffffffu, (word >> bit) & 1u);
-      if (lane == bit) mine = m;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t m = __ballot_sync(0xffffffffu, (word[i] >> bit) & 1u);
+        if (lane == bit) mine[i] = m;
+      }
     }
-    while (mine) {                      // bits exist only for kb < nKb
-      out[cnt++] = r0 + __ffs(mine) - 1;
-      mine &= mine - 1;
+    uint32_t u = mine[0] | mine[1] | mine[2] | mine[3];
+    while (u) {                          // bits exist only for kt < nKt
+      const int bit = __ffs(u) - 1;
+      u &= u - 1;
+      int mask = 0;
+      for (int i = 0; i < 4; ++i) mask |= (int)((mine[i] >> bit) & 1u) << i;
+      out[cnt++] = (r0 + bit) | (mask << 24);
     }
   }
-  if (kb < p.nKb) p.inv_cnt[gi * p.nKb + kb] = cnt;
+  if (kt < p.nKt) p.inv_cnt[gi * p.nKt + kt] = cnt;
 }
 
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-bsa_status encode(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int64_t ss, int64_t sh,
+// [rows, H, D] bf16 view: dims (D, rows, H), box (64, 128, 1), 128-byte
+// swizzle; rows past `rows` read as zeros.
+bsa_status encode(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int D, int64_t ss, int64_t sh,
                   const char* name) {
   static EncodeFn fn = nullptr;
   if (!fn) {
@@ -909,7 +1008,7 @@ bsa_status encode(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int
       return set_error(BSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     fn = reinterpret_cast<EncodeFn>(f);
   }
-  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)H};
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)H};
   cuuint64_t strides[2] = {(cuuint64_t)(ss * 2), (cuuint64_t)(sh * 2)};
   cuuint32_t box[3] = {64u, 128u, 1u};
   cuuint32_t es[3] = {1u, 1u, 1u};
@@ -921,81 +1020,71 @@ bsa_status encode(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int
   return BSA_OK;
 }
 
-constexpr int kDqSmem = (2 + kKStages + kVStages) * kTile + 256 + 1024;     // tiles, barriers, alignment
-static_assert(kDqSmem <= 232448, "dQ kernel shared memory above the per-block limit");
-constexpr int kDkvSmem = 2 * kTile + 2 * (2 * kTile + kRowStat) + 256 + 1024;
+template <int D>
+constexpr int dq_smem() { return (2 + kKStages + kVStages) * Tiles<D>::kTile + 256 + 1024; }
+template <int D>
+constexpr int dkdv_smem() { return 2 * Tiles<D>::kTile + 2 * (2 * Tiles<D>::kTile + kRowStat) + 256 + 1024; }
+static_assert(dq_smem<128>() <= 232448 && dkdv_smem<128>() <= 232448, "shared memory above the per-block limit");
 
-}  // namespace
+// Workspace layout (each part rounded up to 256 bytes).
+struct BwdWorkspace {
+  float* rowstat;
+  int* counters;              // 256 bytes, zeroed together with the planes that follow
+  uint32_t* planes;
+  size_t planes_bytes;
+  int64_t plane_words;
+  int32_t* dq_list;
+  int32_t* dq_cnt;
+  int32_t* inv_cnt;
+  int32_t* inv_list;
+  size_t total;
+};
 
-size_t backward_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int block_q, int block_k) {
-  const int64_t nQb = cdiv64(Sq, block_q), nKb = cdiv64(Skv, block_k), G = Hq / Hkv;
-  const int64_t words = cdiv64(nKb, 32);
+BwdWorkspace carve(void* base, int B, int Hq, int Hkv, int Sq, int Skv) {
+  const int64_t nQt = cdiv64(Sq, kT), nKt = cdiv64(Skv, kKT), G = Hq / Hkv, words = cdiv64(nKt, 32);
   auto al = [](int64_t x) { return (size_t)((x + 255) & ~(int64_t)255); };
-  return al((int64_t)B * Hq * cdiv64(Sq, kT) * kRowStat)  // lse * log2(e) and D per query tile
-         + 256                                             // item counters, one per launch chunk
-         + al((int64_t)B * Hkv * G * nQb * words * 4)      // bitmaps
-         + al((int64_t)B * Hkv * nKb * 4)                  // inverse counts
-         + al((int64_t)B * Hkv * nKb * G * nQb * 4);       // inverse lists
+  char* c = static_cast<char*>(base);
+  size_t off = 0;
+  BwdWorkspace w{};
+  w.rowstat = reinterpret_cast<float*>(c + off);
+  off += al((int64_t)B * Hq * nQt * kRowStat);
+  w.counters = reinterpret_cast<int*>(c + off);
+  off += 256;
+  w.plane_words = (int64_t)B * Hkv * G * nQt * words;
+  w.planes = reinterpret_cast<uint32_t*>(c + off);
+  w.planes_bytes = al(4 * w.plane_words * 4);
+  off += w.planes_bytes;
+  w.dq_list = reinterpret_cast<int32_t*>(c + off);
+  off += al((int64_t)B * Hq * nQt * nKt * 4);
+  w.dq_cnt = reinterpret_cast<int32_t*>(c + off);
+  off += al((int64_t)B * Hq * nQt * 4);
+  w.inv_cnt = reinterpret_cast<int32_t*>(c + off);
+  off += al((int64_t)B * Hkv * nKt * 4);
+  w.inv_list = reinterpret_cast<int32_t*>(c + off);
+  off += al((int64_t)B * Hkv * nKt * G * nQt * 4);
+  w.total = off;
+  return w;
 }
 
-bsa_status launch_backward(const BackwardArgs& a, cudaStream_t stream) {
+template <int D>
+bsa_status launch_tiles(const BackwardArgs& a, const BwdWorkspace& w, cudaStream_t stream) {
   bsa_status st;
-  const int G = a.Hq / a.Hkv;
-  const int nQb = (int)cdiv64(a.Sq, a.block_q), nKb = (int)cdiv64(a.Skv, a.block_k);
-  const int words = (nKb + 31) / 32;
-  auto al = [](int64_t x) { return (size_t)((x + 255) & ~(int64_t)255); };
-  char* ws = static_cast<char*>(a.workspace);
-  const int nQt = (int)cdiv64(a.Sq, kT);
-  float* rowstat = reinterpret_cast<float*>(ws);
-  ws += al((int64_t)a.B * a.Hq * nQt * kRowStat);
-  int* counters = reinterpret_cast<int*>(ws);   // zeroed together with the bitmaps that follow
-  uint32_t* bm = reinterpret_cast<uint32_t*>(ws + 256);
-  const size_t bm_bytes = al((int64_t)a.B * a.Hkv * G * nQb * words * 4);
-  ws += 256 + bm_bytes;
-  int32_t* inv_cnt = reinterpret_cast<int32_t*>(ws);
-  ws += al((int64_t)a.B * a.Hkv * nKb * 4);
-  int32_t* inv_list = reinterpret_cast<int32_t*>(ws);
-
-  {  // lse * log2(e) and D = rowsum(dO * O) per query tile
-    PrepParams pp{};
-    pp.o = static_cast<const __nv_bfloat16*>(a.o); pp.dout = static_cast<const __nv_bfloat16*>(a.dout);
-    pp.lse = a.lse;
-    pp.o_sb = a.o_sb; pp.o_ss = a.o_ss; pp.o_sh = a.o_sh; pp.d_sb = a.d_sb; pp.d_ss = a.d_ss; pp.d_sh = a.d_sh;
-    pp.B = a.B; pp.Sq = a.Sq; pp.Hq = a.Hq; pp.nQt = nQt;
-    for (int b = 0; b < a.B; ++b) pp.seq_lens[b] = a.seq_lens ? a.seq_lens[b] : a.Sq;
-    pp.rowstat = rowstat;
-    const int64_t warps = (int64_t)a.B * nQt * kT * a.Hq;
-    bwd_prep_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, stream>>>(pp);
-    if ((st = cuda_check(cudaGetLastError(), "bwd_prep_kernel launch")) != BSA_OK) return st;
-  }
-  {  // inverse lists
-    if ((st = cuda_check(cudaMemsetAsync(counters, 0, 256 + bm_bytes, stream), "cudaMemsetAsync(bitmaps)")) != BSA_OK)
-      return st;
-    BitmapParams bp{};
-    bp.indices = a.indices; bp.counts = a.counts; bp.bm = bm;
-    bp.B = a.B; bp.Hq = a.Hq; bp.Hkv = a.Hkv; bp.G = G; bp.nQb = nQb; bp.nKb = nKb; bp.block_q = a.block_q;
-    bp.words = words;
-    for (int b = 0; b < a.B; ++b) bp.seq_lens[b] = a.seq_lens ? a.seq_lens[b] : a.Sq;
-    const int64_t rows = (int64_t)a.B * a.Hq * nQb;
-    bwd_bitmap_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(bp);
-    if ((st = cuda_check(cudaGetLastError(), "bwd_bitmap_kernel launch")) != BSA_OK) return st;
-    InvParams ip{};
-    ip.bm = bm; ip.inv_cnt = inv_cnt; ip.inv_list = inv_list;
-    ip.n_groups = a.B * a.Hkv; ip.nrows = G * nQb; ip.nKb = nKb; ip.words = words;
-    const int64_t warps = (int64_t)ip.n_groups * words;
-    bwd_inverse_kernel<<<(unsigned)((warps * 32 + 127) / 128), 128, 0, stream>>>(ip);
-    if ((st = cuda_check(cudaGetLastError(), "bwd_inverse_kernel launch")) != BSA_OK) return st;
-  }
-  static bool attr = false;
-  if (!attr) {
-    if ((st = cuda_check(cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem),
+  static bool attr[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr[dev]) {
+    if ((st = cuda_check(cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              dq_smem<D>()),
                          "cudaFuncSetAttribute(bwd_dq_kernel)")) != BSA_OK)
       return st;
-    if ((st = cuda_check(cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDkvSmem),
+    if ((st = cuda_check(cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              dkdv_smem<D>()),
                          "cudaFuncSetAttribute(bwd_dkdv_kernel)")) != BSA_OK)
       return st;
-    attr = true;
+    attr[dev] = true;
   }
+  const int G = a.Hq / a.Hkv;
+  const int nQt = (int)cdiv64(a.Sq, kT), nKt = (int)cdiv64(a.Skv, kKT);
   const int sms = num_sms();
   for (int b0 = 0; b0 < a.B; b0 += kMaxFwdBatch) {
     const int Bn = std::min(kMaxFwdBatch, a.B - b0);
@@ -1009,28 +1098,86 @@ bsa_status launch_backward(const BackwardArgs& a, cudaStream_t stream) {
       const char* kb = static_cast<const char*>(a.k) + (int64_t)b * a.k_sb * 2;
       const char* vb = static_cast<const char*>(a.v) + (int64_t)b * a.v_sb * 2;
       const char* db = static_cast<const char*>(a.dout) + (int64_t)b * a.d_sb * 2;
-      if ((st = encode(&p.tq[i], qb, L, a.Hq, a.q_ss, a.q_sh, "Q")) != BSA_OK) return st;
-      if ((st = encode(&p.tdo[i], db, L, a.Hq, a.d_ss, a.d_sh, "dO")) != BSA_OK) return st;
-      if ((st = encode(&p.tk[i], kb, a.prefix_len + L, a.Hkv, a.k_ss, a.k_sh, "K")) != BSA_OK) return st;
-      if ((st = encode(&p.tv[i], vb, a.prefix_len + L, a.Hkv, a.v_ss, a.v_sh, "V")) != BSA_OK) return st;
+      if ((st = encode(&p.tq[i], qb, L, a.Hq, D, a.q_ss, a.q_sh, "Q")) != BSA_OK) return st;
+      if ((st = encode(&p.tdo[i], db, L, a.Hq, D, a.d_ss, a.d_sh, "dO")) != BSA_OK) return st;
+      if ((st = encode(&p.tk[i], kb, a.prefix_len + L, a.Hkv, D, a.k_ss, a.k_sh, "K")) != BSA_OK) return st;
+      if ((st = encode(&p.tv[i], vb, a.prefix_len + L, a.Hkv, D, a.v_ss, a.v_sh, "V")) != BSA_OK) return st;
     }
     p.b0 = b0; p.Bn = Bn; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.Sq = a.Sq; p.Skv = a.Skv;
-    p.nQb = nQb; p.nKb = nKb; p.nQt = nQt; p.block_q = a.block_q; p.prefix_len = a.prefix_len;
-    p.indices = a.indices; p.counts = a.counts; p.rowstat = rowstat;
-    p.inv_cnt = inv_cnt; p.inv_list = inv_list;
+    p.nQt = nQt; p.nKt = nKt; p.prefix_len = a.prefix_len;
+    p.dq_list = w.dq_list; p.dq_cnt = w.dq_cnt; p.rowstat = w.rowstat;
+    p.inv_cnt = w.inv_cnt; p.inv_list = w.inv_list;
     p.scale = a.scale; p.scale_log2 = a.scale * kLog2e;
     p.dq = static_cast<__nv_bfloat16*>(a.dq);
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
-    p.n_items = Bn * a.Hkv * p.nQt * G;
-    bwd_dq_kernel<<<std::min(p.n_items, sms), kThreads, kDqSmem, stream>>>(p);
+    p.n_items = Bn * a.Hkv * nQt * G;
+    bwd_dq_kernel<D><<<std::min(p.n_items, sms), kThreads, dq_smem<D>(), stream>>>(p);
     if ((st = cuda_check(cudaGetLastError(), "bwd_dq_kernel launch")) != BSA_OK) return st;
-    p.n_items = Bn * a.Hkv * nKb;
-    p.counter = counters + b0 / kMaxFwdBatch;
-    bwd_dkdv_kernel<<<std::min(p.n_items, sms), kThreads, kDkvSmem, stream>>>(p);
+    p.n_items = Bn * a.Hkv * nKt;
+    p.counter = w.counters + b0 / kMaxFwdBatch;
+    bwd_dkdv_kernel<D><<<std::min(p.n_items, sms), kThreads, dkdv_smem<D>(), stream>>>(p);
     if ((st = cuda_check(cudaGetLastError(), "bwd_dkdv_kernel launch")) != BSA_OK) return st;
   }
   return BSA_OK;
+}
+
+}  // namespace
+
+size_t backward_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int block_q, int block_k) {
+  (void)block_q;
+  (void)block_k;
+  return carve(nullptr, B, Hq, Hkv, Sq, Skv).total;
+}
+
+bsa_status launch_backward(const BackwardArgs& a, cudaStream_t stream) {
+  bsa_status st;
+  const int G = a.Hq / a.Hkv;
+  const int nQb = (int)cdiv64(a.Sq, a.block_q), nKb = (int)cdiv64(a.Skv, a.block_k);
+  const int nQt = (int)cdiv64(a.Sq, kT), nKt = (int)cdiv64(a.Skv, kKT);
+  const int words = (nKt + 31) / 32;
+  const BwdWorkspace w = carve(a.workspace, a.B, a.Hq, a.Hkv, a.Sq, a.Skv);
+
+  {  // -lse * log2(e) and -D per query tile
+    PrepParams pp{};
+    pp.o = static_cast<const __nv_bfloat16*>(a.o); pp.dout = static_cast<const __nv_bfloat16*>(a.dout);
+    pp.lse = a.lse;
+    pp.o_sb = a.o_sb; pp.o_ss = a.o_ss; pp.o_sh = a.o_sh; pp.d_sb = a.d_sb; pp.d_ss = a.d_ss; pp.d_sh = a.d_sh;
+    pp.B = a.B; pp.Sq = a.Sq; pp.Hq = a.Hq; pp.nQt = nQt;
+    for (int b = 0; b < a.B; ++b) pp.seq_lens[b] = a.seq_lens ? a.seq_lens[b] : a.Sq;
+    pp.rowstat = w.rowstat;
+    const int64_t warps = (int64_t)a.B * nQt * kT * a.Hq;
+    const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
+    if (a.d == 128) bwd_prep_kernel<128><<<grid, 256, 0, stream>>>(pp);
+    else bwd_prep_kernel<64><<<grid, 256, 0, stream>>>(pp);
+    if ((st = cuda_check(cudaGetLastError(), "bwd_prep_kernel launch")) != BSA_OK) return st;
+  }
+  {  // tile lists for dQ and inverse tile lists for dK/dV
+    if ((st = cuda_check(cudaMemsetAsync(w.counters, 0, 256 + w.planes_bytes, stream), "cudaMemsetAsync(bitmaps)")) !=
+        BSA_OK)
+      return st;
+    BitmapParams bp{};
+    bp.indices = a.indices; bp.counts = a.counts; bp.planes = w.planes; bp.plane_words = w.plane_words;
+    bp.B = a.B; bp.Hq = a.Hq; bp.Hkv = a.Hkv; bp.G = G; bp.nQb = nQb; bp.nKb = nKb; bp.nQt = nQt; bp.nKt = nKt;
+    bp.block_q = a.block_q; bp.block_k = a.block_k; bp.words = words;
+    for (int b = 0; b < a.B; ++b) bp.seq_lens[b] = a.seq_lens ? a.seq_lens[b] : a.Sq;
+    const int64_t rows = (int64_t)a.B * a.Hq * nQb;
+    bwd_bitmap_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(bp);
+    if ((st = cuda_check(cudaGetLastError(), "bwd_bitmap_kernel launch")) != BSA_OK) return st;
+    TileListParams tp{};
+    tp.planes = w.planes; tp.plane_words = w.plane_words; tp.dq_list = w.dq_list; tp.dq_cnt = w.dq_cnt;
+    tp.n_rows = a.B * a.Hq * nQt; tp.nKt = nKt; tp.words = words;
+    bwd_tilelist_kernel<<<(unsigned)(((int64_t)tp.n_rows * 32 + 255) / 256), 256, 0, stream>>>(tp);
+    if ((st = cuda_check(cudaGetLastError(), "bwd_tilelist_kernel launch")) != BSA_OK) return st;
+    InvParams ip{};
+    ip.planes = w.planes; ip.plane_words = w.plane_words; ip.inv_cnt = w.inv_cnt; ip.inv_list = w.inv_list;
+    ip.n_groups = a.B * a.Hkv; ip.nrows = G * nQt; ip.nKt = nKt; ip.words = words;
+    const int64_t warps = (int64_t)ip.n_groups * words;
+    bwd_inverse_kernel<<<(unsigned)((warps * 32 + 127) / 128), 128, 0, stream>>>(ip);
+    if ((st = cuda_check(cudaGetLastError(), "bwd_inverse_kernel launch")) != BSA_OK) return st;
+  }
+  if (a.d == 128) return launch_tiles<128>(a, w, stream);
+  return launch_tiles<64>(a, w, stream);
 }
 
 }  // namespace bsa

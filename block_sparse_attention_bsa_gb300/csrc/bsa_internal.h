@@ -79,7 +79,7 @@ struct BackwardArgs {
   const void* o; int64_t o_sb, o_ss, o_sh;
   const void* dout; int64_t d_sb, d_ss, d_sh;
   const float* lse;          // [B, Hq, Sq]
-  int B, Hq, Hkv, Sq, Skv, block_q, block_k, prefix_len;
+  int B, Hq, Hkv, Sq, Skv, d, block_q, block_k, prefix_len;
   const int32_t* seq_lens;   // host, B values
   const int32_t* indices;
   const int32_t* counts;

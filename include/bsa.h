@@ -243,15 +243,18 @@ BSA_API bsa_status bsa_forward_causal(const bsa_tensor* q_und, const bsa_tensor*
  * indices, counts and lse must be the ones the forward used, and out its
  * output.  Results do not depend on scheduling: no atomics touch dQ/dK/dV.
  *
- * Supported: head dim 128, block_k 128, block_q 128 or 256 (others return
- *   BSA_ERR_UNSUPPORTED); indices/counts are required (dense lists come from
- *   bsa_select with keep_ratio 1).
+ * Supported: every geometry bsa_forward takes (head dim 64 or 128, block_q
+ *   64, 128 or 256, block_k 64 or 128); indices/counts are required (dense
+ *   lists come from bsa_select with keep_ratio 1).
  * q, k, v, out, dout: bf16 descriptors as in bsa_forward; out and dout have
  *   q's shape.  lse: device fp32 [B, Hq, Sq] contiguous from bsa_forward.
  * dq: device bf16 [B, Sq, Hq, d]; dk, dv: device bf16 [B, Skv, Hkv, d]; all
  *   contiguous and fully written (padded rows and keys no query reads get 0).
  * workspace: device, >= bsa_backward_workspace_size(...) bytes, 256-B
- *   aligned; it holds D, the key-block -> query-block lists and their bitmaps.
+ *   aligned; it holds -lse and -D per 128-row query tile and the lists re-cut
+ *   on 128 x 128 (query tile, key tile) pairs with their bitmaps: per query
+ *   tile its key tiles, per key tile the query tiles, each with a mask of the
+ *   selected 64-row / 64-key halves.
  * Gradient buffers may not alias any input. */
 BSA_API size_t bsa_backward_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int block_q, int block_k);
 BSA_API bsa_status bsa_backward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tensor* v,

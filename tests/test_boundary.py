@@ -244,9 +244,9 @@ def call_backward(lib, q, k, v, o=None, do=None, lse=FAKE, ind=FAKE, cnt=FAKE, p
 
 
 @pytest.mark.parametrize("case,status,needle", [
-    ("head_dim64", 2, "head dim 128"),
-    ("block_q64", 2, "block_q 128 or 256"),
-    ("block_k64", 2, "block_k 128"),
+    ("head_dim96", 2, "head dim 96"),
+    ("block_q96", 2, "block geometry"),
+    ("block_k256", 2, "block geometry"),
     ("dout_shape", 1, "dout shape"),
     ("out_shape", 1, "out shape"),
     ("no_indices", 1, "indices and counts are required"),
@@ -259,12 +259,12 @@ def call_backward(lib, q, k, v, o=None, do=None, lse=FAKE, ind=FAKE, cnt=FAKE, p
 def test_backward_rejects_bad_arguments(lib, case, status, needle):
     q, k, v = T(H=4), T(H=2, S=768), T(H=2, S=768)
     kw = dict(prefix=256)
-    if case == "head_dim64":
-        q, k, v = T(H=4, D=64), T(H=2, S=768, D=64), T(H=2, S=768, D=64)
-    elif case == "block_q64":
-        kw["bq"] = 64
-    elif case == "block_k64":
-        kw["bk"] = 64
+    if case == "head_dim96":
+        q, k, v = T(H=4, D=96), T(H=2, S=768, D=96), T(H=2, S=768, D=96)
+    elif case == "block_q96":
+        kw["bq"] = 96
+    elif case == "block_k256":
+        kw["bk"] = 256
     elif case == "dout_shape":
         kw["do"] = T(H=4, S=256)
     elif case == "out_shape":
@@ -287,12 +287,15 @@ def test_backward_rejects_bad_arguments(lib, case, status, needle):
 
 
 def test_backward_workspace_size_formula(lib):
-    # per 128-row query tile 128 lse and 128 D values (fp32), 256 B of item counters, bitmaps
-    # [B,Hkv,G*nQb,ceil(nKb/32)] u32, inverse counts [B,Hkv,nKb] and lists [B,Hkv,nKb,G*nQb] int32, each rounded up to 256 B
-    B, Hq, Hkv, Sq, Skv, bq, bk = 1, 32, 8, 172800, 173824, 256, 128
+    # On 128 x 128 (query tile, key tile) pairs, each part rounded up to 256 B: per query tile 128
+    # lse and 128 D values (fp32); 256 B of item counters; 4 mask bitmaps [B,Hkv,G*nQt,ceil(nKt/32)]
+    # u32; dQ lists [B,Hq,nQt,nKt] + counts [B,Hq,nQt]; inverse counts [B,Hkv,nKt] and lists
+    # [B,Hkv,nKt,G*nQt] int32.  The block geometry does not change the size.
+    B, Hq, Hkv, Sq, Skv = 1, 32, 8, 172800, 173824
     r = lambda x: ((x + 255) // 256) * 256
-    nQb, nKb, G, nQt = 675, 1358, 4, 1350
-    want = (r(B * Hq * nQt * 256 * 4) + 256 + r(B * Hkv * G * nQb * 43 * 4) + r(B * Hkv * nKb * 4)
-            + r(B * Hkv * nKb * G * nQb * 4))
-    assert lib.bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, bq, bk) == want
-    assert lib.bsa_backward_workspace_size(B, Hq, 5, Sq, Skv, bq, bk) == 0
+    nQt, nKt, G = 1350, 1358, 4
+    want = (r(B * Hq * nQt * 256 * 4) + 256 + r(4 * B * Hkv * G * nQt * 43 * 4) + r(B * Hq * nQt * nKt * 4)
+            + r(B * Hq * nQt * 4) + r(B * Hkv * nKt * 4) + r(B * Hkv * nKt * G * nQt * 4))
+    for bq, bk in ((256, 128), (64, 64), (128, 64)):
+        assert lib.bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, bq, bk) == want
+    assert lib.bsa_backward_workspace_size(B, Hq, 5, Sq, Skv, 256, 128) == 0

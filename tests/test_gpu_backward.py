@@ -83,7 +83,7 @@ def compare_grad(name, g, r, real):
     return dict(rel_fro=float(rel_fro), rel_max=float(rel_max))
 
 
-@pytest.mark.parametrize("name", ["small_gqa", "small_mha_perhead"])
+@pytest.mark.parametrize("name", ["small_gqa", "small_mha_perhead", "tiny", "small_mqa_d64", "small_64x64_d128"])
 def test_backward_parity_small(name):
     inp, idx, cnt, out_bf, lse32, dout, (dq_r, dk_r, dv_r) = oracle_case(name)
     c = inp["cfg"]
@@ -129,12 +129,13 @@ def dq_rounding_bound(q, k, v, out, dout, lse, pos, rows, h, hk, scale):
     return 2.0 ** -8 * scale * (np.abs(ds) @ np.abs(kk)) + 2.0 ** -8 * np.abs(ref)
 
 
-def test_backward_480p_identities_and_sampled_dq():
+@pytest.mark.parametrize("name", ["480p_75", "480p_75_64x64"])
+def test_backward_480p_identities_and_sampled_dq(name):
     """480p latent, keep 25%, the oracle's lists through the CUDA forward and
     backward: identities over all keys, and sampled dQ tiles against the
     oracle's backward of those tiles on the same out/lse (the oracle's
     forward of the tiles, written into the forward's buffers)."""
-    cfg = CONFIGS["480p_75"]
+    cfg = CONFIGS[name]
     inp = make_inputs(cfg, "cpu")
     L = inp["seq_lens"][0]
     G = cfg.Hq // cfg.Hkv
