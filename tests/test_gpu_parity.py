@@ -68,15 +68,23 @@ def test_select_parity_small(name):
     print(name, stats)
 
 
+def oracle_lists(inp):
+    """The oracle's selection as int32 numpy arrays (the lists both forwards attend)."""
+    c = inp["cfg"]
+    ref = O.select_blocks(to_f32_np(inp["q"]), to_f32_np(inp["k"]), c.prefix, inp["seq_lens"], c.block_q,
+                          c.block_k, inp["keep_ratio"])
+    return ref, ref["indices"].astype(np.int32), ref["counts"].astype(np.int32)
+
+
 @pytest.mark.parametrize("name", SMALL)
 def test_forward_parity_small(name):
+    """The CUDA forward and the oracle's attention over the oracle's lists."""
     inp = cuda_inputs(name)
     c = inp["cfg"]
-    idx, cnt = run_select(inp)
-    out, lse = run_forward(inp, idx, cnt)
+    _, ri, rc = oracle_lists(inp)
+    out, lse = run_forward(inp, torch.from_numpy(ri).cuda(), torch.from_numpy(rc).cuda())
     q, k, v = (to_f32_np(inp[x]).astype(np.float64) for x in ("q", "k", "v"))
-    o_ref, l_ref = O.attention(q, k, v, idx.cpu().numpy(), cnt.cpu().numpy(), c.prefix, inp["seq_lens"],
-                               c.block_q, c.block_k)
+    o_ref, l_ref = O.attention(q, k, v, ri, rc, c.prefix, inp["seq_lens"], c.block_q, c.block_k)
     stats = compare_attention(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, inp["seq_lens"])
     print(name, stats)
 
@@ -365,20 +373,24 @@ def test_workload_config_parity(name):
     inp = full_inputs(name)
     c = inp["cfg"]
     idx, cnt = run_select(inp)
-    out, lse = run_forward(inp, idx, cnt)
     gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
     q32, k32 = to_f32_np(inp["q"]), to_f32_np(inp["k"])
     ref = O.select_blocks(q32, k32, c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
     sel_stats = compare_selection(gi, gc, ref)
     check_structure(gi, gc, c.prefix, inp["seq_lens"], c.block_q, c.block_k)
+    if name == "480p_dense":
+        out_g, lse_g = run_forward(inp, idx, cnt)
+        o_null, l_null = run_forward(inp, None, None)
+        assert torch.equal(o_null, out_g) and torch.equal(l_null, lse_g)
+        del out_g, lse_g, o_null, l_null
+    # the forward in the bench's launch configuration, over the oracle's lists
+    ri, rc = ref["indices"].astype(np.int32), ref["counts"].astype(np.int32)
+    out, lse = run_forward(inp, torch.from_numpy(ri).cuda(), torch.from_numpy(rc).cuda())
     tiles = sample_tiles(c.B, c.Hq, gc.shape[2], inp["seq_lens"], c.block_q, n_random=8, seed=c.seed)
     v32 = to_f32_np(inp["v"])
-    o_ref, l_ref = O.attention(q32, k32, v32, gi, gc, c.prefix, inp["seq_lens"], c.block_q, c.block_k,
+    o_ref, l_ref = O.attention(q32, k32, v32, ri, rc, c.prefix, inp["seq_lens"], c.block_q, c.block_k,
                                tiles=tiles)
     att = compare_attention(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, inp["seq_lens"])
-    if name == "480p_dense":
-        o_null, l_null = run_forward(inp, None, None)
-        assert torch.equal(o_null, out) and torch.equal(l_null, lse)
     kept = gc.sum() / max(1, sum(O.cdiv(c.prefix + L, c.block_k) * O.cdiv(L, c.block_q)
                                  for L in inp["seq_lens"]) * c.Hq)
     print(name, sel_stats, att, f"tile keep fraction {kept:.4f}")
