@@ -66,8 +66,8 @@ def peaks():
 # launch, from an ncu capture of the build whose FMHA sources hash to `sha`.
 # When the sources change the figure no longer applies and traffic is null.
 FMHA_TRAFFIC = {
-    "sha": "af3445d2b8cae8a7",
-    "720p_75": 13861869824 + 1741903616,  # profiles/launches_720p_75.md (1-pass capture)
+    "sha": "2da9ecc6859ccccd",
+    "720p_75": 13991214080 + 1763857664,  # profiles/launches_720p_75.md (1-pass capture)
 }
 
 

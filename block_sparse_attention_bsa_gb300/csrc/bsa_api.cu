@@ -3,6 +3,8 @@
 // here follows the contract written in include/bsa.h.
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <mutex>
 #include <cmath>
 #include <cstdint>
 #include <string>
@@ -29,14 +31,55 @@ bsa_status cuda_check(cudaError_t e, const char* what) {
 }
 
 int num_sms() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  if (dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 1;
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  if (dev < 64) cached[dev] = n;
+  if (dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
+}
+
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's cuTensorMapEncodeTiled, looked up once per process.
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+}  // namespace
+
+bsa_status encode_tensor_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int D, int64_t ss,
+                             int64_t sh, int box_rows, const char* name) {
+  const EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(BSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)H};
+  cuuint64_t strides[2] = {(cuuint64_t)(ss * 2), (cuuint64_t)(sh * 2)};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(BSA_ERR_CUDA, std::string("cuTensorMapEncodeTiled failed for ") + name + " (CUresult " +
+                                       std::to_string((int)r) + ")");
+  return BSA_OK;
 }
 
 size_t select_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int d, int bq, int bk) {

@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -61,6 +62,7 @@ struct BwdParams {
   CUtensorMap tdo[kMaxFwdBatch];
   int seq_lens[kMaxFwdBatch];
   int b0, Bn, Hq, Hkv, G, Sq, Skv, nQt, nKt, prefix_len, n_items;
+  int full_masks;             // 1: every pair mask is full (256/128-row query blocks, 128-key blocks)
   const int32_t* dq_list;     // [B, Hq, nQt, nKt]: key tiles kt | mask << 24, ascending
   const int32_t* dq_cnt;      // [B, Hq, nQt]
   const float* rowstat;       // [B, Hq, nQt, 2, 128]: -lse * log2(e) (-inf on padded rows), -D
@@ -711,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         // per query-row column: -lse log2(e) (-inf on padded rows) and -D
         const float* rs = reinterpret_cast<const float*>(qdo_s + st * kStage + 2 * kTile) + grp * 64;
         // this group's query-row half and this warp's key half selected as a pair?
-        const bool pair_ok = (__ldg(lst + s) >> (24 + grp * 2 + (wq >> 1))) & 1;
+        const bool pair_ok = p.full_masks || ((__ldg(lst + s) >> (24 + grp * 2 + (wq >> 1))) & 1);
         const bool need_mask = !(warp_keys_ok && pair_ok);      // warp-uniform
         const float2 km = pair_ok ? km2 : make_float2(0.f, 0.f);
         // P^T = 2^(S^T scale log2(e) - lse log2(e)), kept in registers; bf16 over S^T
@@ -991,35 +993,6 @@ __global__ void bwd_inverse_kernel(const __grid_constant__ InvParams p) {
   if (kt < p.nKt) p.inv_cnt[gi * p.nKt + kt] = cnt;
 }
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// [rows, H, D] bf16 view: dims (D, rows, H), box (64, 128, 1), 128-byte
-// swizzle; rows past `rows` read as zeros.
-bsa_status encode(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int D, int64_t ss, int64_t sh,
-                  const char* name) {
-  static EncodeFn fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess || q != cudaDriverEntryPointSuccess)
-      return set_error(BSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    fn = reinterpret_cast<EncodeFn>(f);
-  }
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)H};
-  cuuint64_t strides[2] = {(cuuint64_t)(ss * 2), (cuuint64_t)(sh * 2)};
-  cuuint32_t box[3] = {64u, 128u, 1u};
-  cuuint32_t es[3] = {1u, 1u, 1u};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return set_error(BSA_ERR_CUDA, std::string("cuTensorMapEncodeTiled failed for ") + name);
-  return BSA_OK;
-}
-
 template <int D>
 constexpr int dq_smem() { return (2 + kKStages + kVStages) * Tiles<D>::kTile + 256 + 1024; }
 template <int D>
@@ -1069,10 +1042,10 @@ BwdWorkspace carve(void* base, int B, int Hq, int Hkv, int Sq, int Skv) {
 template <int D>
 bsa_status launch_tiles(const BackwardArgs& a, const BwdWorkspace& w, cudaStream_t stream) {
   bsa_status st;
-  static bool attr[64] = {false};
+  static std::atomic<bool> attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr[dev]) {
+  if (dev < 64 && !attr[dev].load(std::memory_order_acquire)) {
     if ((st = cuda_check(cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               dq_smem<D>()),
                          "cudaFuncSetAttribute(bwd_dq_kernel)")) != BSA_OK)
@@ -1081,7 +1054,7 @@ bsa_status launch_tiles(const BackwardArgs& a, const BwdWorkspace& w, cudaStream
                                               dkdv_smem<D>()),
                          "cudaFuncSetAttribute(bwd_dkdv_kernel)")) != BSA_OK)
       return st;
-    attr[dev] = true;
+    attr[dev].store(true, std::memory_order_release);
   }
   const int G = a.Hq / a.Hkv;
   const int nQt = (int)cdiv64(a.Sq, kT), nKt = (int)cdiv64(a.Skv, kKT);
@@ -1098,13 +1071,14 @@ bsa_status launch_tiles(const BackwardArgs& a, const BwdWorkspace& w, cudaStream
       const char* kb = static_cast<const char*>(a.k) + (int64_t)b * a.k_sb * 2;
       const char* vb = static_cast<const char*>(a.v) + (int64_t)b * a.v_sb * 2;
       const char* db = static_cast<const char*>(a.dout) + (int64_t)b * a.d_sb * 2;
-      if ((st = encode(&p.tq[i], qb, L, a.Hq, D, a.q_ss, a.q_sh, "Q")) != BSA_OK) return st;
-      if ((st = encode(&p.tdo[i], db, L, a.Hq, D, a.d_ss, a.d_sh, "dO")) != BSA_OK) return st;
-      if ((st = encode(&p.tk[i], kb, a.prefix_len + L, a.Hkv, D, a.k_ss, a.k_sh, "K")) != BSA_OK) return st;
-      if ((st = encode(&p.tv[i], vb, a.prefix_len + L, a.Hkv, D, a.v_ss, a.v_sh, "V")) != BSA_OK) return st;
+      if ((st = encode_tensor_map(&p.tq[i], qb, L, a.Hq, D, a.q_ss, a.q_sh, 128, "Q")) != BSA_OK) return st;
+      if ((st = encode_tensor_map(&p.tdo[i], db, L, a.Hq, D, a.d_ss, a.d_sh, 128, "dO")) != BSA_OK) return st;
+      if ((st = encode_tensor_map(&p.tk[i], kb, a.prefix_len + L, a.Hkv, D, a.k_ss, a.k_sh, 128, "K")) != BSA_OK) return st;
+      if ((st = encode_tensor_map(&p.tv[i], vb, a.prefix_len + L, a.Hkv, D, a.v_ss, a.v_sh, 128, "V")) != BSA_OK) return st;
     }
     p.b0 = b0; p.Bn = Bn; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.Sq = a.Sq; p.Skv = a.Skv;
     p.nQt = nQt; p.nKt = nKt; p.prefix_len = a.prefix_len;
+    p.full_masks = (a.block_q >= kT && a.block_k == kKT) ? 1 : 0;
     p.dq_list = w.dq_list; p.dq_cnt = w.dq_cnt; p.rowstat = w.rowstat;
     p.inv_cnt = w.inv_cnt; p.inv_list = w.inv_list;
     p.scale = a.scale; p.scale_log2 = a.scale * kLog2e;

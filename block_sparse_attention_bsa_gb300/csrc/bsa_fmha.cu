@@ -28,6 +28,7 @@
 //    raises the device error word, leaves its loops and frees its TMEM.
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
@@ -41,9 +42,6 @@
 #endif
 #ifndef BSA_SOFTMAX_MAX3
 #define BSA_SOFTMAX_MAX3 1       // three-input max for the row max
-#endif
-#ifndef BSA_KV_PAIR
-#define BSA_KV_PAIR 1            // K and V of one key block share one ring stage (measured +2.5%)
 #endif
 #ifndef BSA_REG_CONTROL
 #define BSA_REG_CONTROL 0        // registers of the control warpgroup (0: no split; measured faster)
@@ -82,7 +80,7 @@ struct Cfg {
   static constexpr int kBarBytes = 256;
   static constexpr int kAlignSlack = 1024;
   static constexpr int kSmemMax = 232448;                 // 227 KB per CTA
-  static constexpr int kStageBytes = (BSA_KV_PAIR ? 2 : 1) * kTileBytes;   // one ring stage
+  static constexpr int kStageBytes = 2 * kTileBytes;      // one ring stage: K and V of one key block
   static constexpr int kStagesFit = (kSmemMax - kQBytes - kBarBytes - kAlignSlack) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kSmemBytes = kQBytes + kStages * kStageBytes + kBarBytes + kAlignSlack;
@@ -299,7 +297,6 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
             if (jj + 1 < m && t1 >= 0 && t1 < p.nKb) kb1 = t1;
           }
           if (lane == 0) {
-#if BSA_KV_PAIR
             // K at the stage base, V right after it; one barrier for both.
             ok = mbar_wait(smem_u32(kv_empty + ring.stage), ring.phase ^ 1u, abort_flag);
             if (ok) {
@@ -319,20 +316,6 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
               }
               ring.next<C::kStages>();
             }
-#else
-            static_assert(KB == BK, "64-key pairing needs K and V in one stage");
-            for (int which = 0; which < 2 && ok; ++which) {
-              ok = mbar_wait(smem_u32(kv_empty + ring.stage), ring.phase ^ 1u, abort_flag);
-              if (!ok) break;
-              const uint32_t fb = smem_u32(kv_full + ring.stage);
-              mbar_arrive_expect_tx(fb, C::kTileBytes);
-              const CUtensorMap* tm = which == 0 ? &p.tk[ti.bl] : &p.tv[ti.bl];
-              for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(kv_base + ring.stage * C::kTileBytes + c * (BK * 128), tm, fb, c * 64,
-                            kb * BK, ti.hk);
-              ring.next<C::kStages>();
-            }
-#endif
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
@@ -394,7 +377,6 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
         ok = mbar_wait(smem_u32(q_full), qi & 1u, abort_flag);
         ++qi;
         if (!ok) break;
-#if BSA_KV_PAIR
         // K_j and V_j share stage sJ (K at +0, V at +kTileBytes).
         uint32_t sJ = ring.stage;
         ok = mbar_wait(smem_u32(kv_full + sJ), ring.phase, abort_flag);
@@ -437,56 +419,6 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
           if (has_next && j + 2 == n) mma_commit(smem_u32(q_empty));
           sJ = sN;
         }
-#else
-        // S_h(0) for every half
-        uint32_t sK = ring.stage;
-        ok = mbar_wait(smem_u32(kv_full + sK), ring.phase, abort_flag);
-        ring.next<C::kStages>();
-        if (!ok) break;
-        tc_fence_after();
-        for (int hh = 0; hh < NH; ++hh) {
-          issue_s(hh, sK * C::kTileBytes);
-          mma_commit(smem_u32(s_full + hh));
-        }
-        mma_commit(smem_u32(kv_empty + sK));
-        if (n == 1) mma_commit(smem_u32(q_empty));
-        for (int j = 0; j < n && ok; ++j) {
-          const uint32_t sV = ring.stage;
-          ok = mbar_wait(smem_u32(kv_full + sV), ring.phase, abort_flag);
-          ring.next<C::kStages>();
-          if (!ok) break;
-          const bool has_next = j + 1 < n;
-          uint32_t sKn = 0, sKn_phase = 0;
-          if (has_next) {
-            sKn = ring.stage;
-            sKn_phase = ring.phase;
-            ring.next<C::kStages>();
-          }
-          for (int hh = 0; hh < NH && ok; ++hh) {
-            ok = mbar_wait(smem_u32(p_full + hh), pph[hh] & 1u, abort_flag);
-            ++pph[hh];
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(hh, sV * C::kTileBytes, j > 0);
-            if (j == n - 1) mma_commit(smem_u32(o_full + hh));
-            if (has_next) {
-              if (hh == 0) {
-                ok = mbar_wait(smem_u32(kv_full + sKn), sKn_phase, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-              }
-              issue_s(hh, sKn * C::kTileBytes);
-              mma_commit(smem_u32(s_full + hh));
-            }
-          }
-          if (!ok) break;
-          mma_commit(smem_u32(kv_empty + sV));
-          if (has_next) {
-            mma_commit(smem_u32(kv_empty + sKn));
-            if (j + 2 == n) mma_commit(smem_u32(q_empty));
-          }
-        }
-#endif
       }
     }
     __syncwarp();
@@ -738,59 +670,20 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const __grid_constant__ 
 
 // ------------------------------------------------------------- host side ---
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
-
-// [rows, H, D] bf16 view starting at `base`: dims (D, rows, H), box (64, box_rows, 1),
-// 128-byte swizzle; rows past `rows` read as zeros.
-bsa_status encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int D,
-                      int64_t ss, int64_t sh, int box_rows, const char* name) {
-  EncodeTiledFn fn = get_encode_fn();
-  if (!fn) return set_error(BSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)H};
-  cuuint64_t strides[2] = {(cuuint64_t)(ss * 2), (cuuint64_t)(sh * 2)};
-  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
-  cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return set_error(BSA_ERR_CUDA, std::string("cuTensorMapEncodeTiled failed for ") + name +
-                                       " (CUresult " + std::to_string((int)r) + ")");
-  return BSA_OK;
-}
-
 template <int D, int BK, int NH, int KB = BK>
 bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
   using C = Cfg<D, BK, NH>;
-  static bool attr_set[64] = {false};
+  static std::atomic<bool> attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   bsa_status st;
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     if ((st = cuda_check(cudaFuncSetAttribute(fmha_fwd_kernel<D, BK, NH, KB>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               C::kSmemBytes),
                          "cudaFuncSetAttribute(fmha_fwd_kernel)")) != BSA_OK)
       return st;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const int sms = num_sms();
   for (int b0 = 0; b0 < a.B; b0 += kMaxFwdBatch) {
@@ -804,10 +697,10 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
       const char* qb = static_cast<const char*>(a.q) + (int64_t)b * a.q_sb * 2;
       const char* kb = static_cast<const char*>(a.k) + (int64_t)b * a.k_sb * 2;
       const char* vb = static_cast<const char*>(a.v) + (int64_t)b * a.v_sb * 2;
-      if ((st = encode_map(&p.tq[i], qb, L, a.Hq, D, a.q_ss, a.q_sh, 128, "Q")) != BSA_OK) return st;
-      if ((st = encode_map(&p.tk[i], kb, a.prefix_len + L, a.Hkv, D, a.k_ss, a.k_sh, KB, "K")) != BSA_OK)
+      if ((st = encode_tensor_map(&p.tq[i], qb, L, a.Hq, D, a.q_ss, a.q_sh, 128, "Q")) != BSA_OK) return st;
+      if ((st = encode_tensor_map(&p.tk[i], kb, a.prefix_len + L, a.Hkv, D, a.k_ss, a.k_sh, KB, "K")) != BSA_OK)
         return st;
-      if ((st = encode_map(&p.tv[i], vb, a.prefix_len + L, a.Hkv, D, a.v_ss, a.v_sh, KB, "V")) != BSA_OK)
+      if ((st = encode_tensor_map(&p.tv[i], vb, a.prefix_len + L, a.Hkv, D, a.v_ss, a.v_sh, KB, "V")) != BSA_OK)
         return st;
     }
     p.b0 = b0;

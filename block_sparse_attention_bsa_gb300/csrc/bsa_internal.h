@@ -27,6 +27,12 @@ bsa_status cuda_check(cudaError_t e, const char* what);
 // Number of SMs of the current device (cached per device).
 int num_sms();
 
+// TMA tensor map of a [rows, H, D] bf16 view (row stride ss, head stride sh,
+// in elements): dims (D, rows, H), box (64, box_rows, 1), 128-byte swizzle;
+// rows past `rows` read as zeros.  `name` labels the error message.
+bsa_status encode_tensor_map(CUtensorMap* m, const void* base, int64_t rows, int64_t H, int D, int64_t ss,
+                             int64_t sh, int box_rows, const char* name);
+
 // ---- selector (bsa_select.cu) ----
 struct SelectArgs {
   const void* q; int64_t q_sb, q_ss, q_sh;
