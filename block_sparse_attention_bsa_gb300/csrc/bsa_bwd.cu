@@ -62,7 +62,6 @@ struct BwdParams {
   CUtensorMap tdo[kMaxFwdBatch];
   int seq_lens[kMaxFwdBatch];
   int b0, Bn, Hq, Hkv, G, Sq, Skv, nQt, nKt, prefix_len, n_items;
-  int full_masks;             // 1: every pair mask is full (256/128-row query blocks, 128-key blocks)
   const int32_t* dq_list;     // [B, Hq, nQt, nKt]: key tiles kt | mask << 24, ascending
   const int32_t* dq_cnt;      // [B, Hq, nQt]
   const float* rowstat;       // [B, Hq, nQt, 2, 128]: -lse * log2(e) (-inf on padded rows), -D
@@ -134,8 +133,9 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* o, 
 // registers between the exponentials and dS.  Issue order: S(j+1), dQ(j),
 // dP(j+1), S(j+2), ...: block j+1's exponentials overlap dQ(j), dP(j+1)
 // and S(j+2).  Entries whose mask excludes a (row half, key half) give P = 0
-// there.
-template <int D>
+// there.  kFull: every mask is full (256/128-row query blocks, 128-key
+// blocks), so the mask tests compile away.
+template <int D, bool kFull>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using T = Tiles<D>;
   constexpr int kTile = T::kTile;
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         if (kb >= p.nKt) kb = p.nKt;
         // this (row half, key half) pair selected?  keys of this group's half
         // below the end of the sequence (a tile holding the end only)
-        const bool pair_ok = (e >> (24 + qhalf * 2 + grp)) & 1;
+        const bool pair_ok = kFull || ((e >> (24 + qhalf * 2 + grp)) & 1);
         const int kvalid = valid_kv - kb * kKT - grp * 64;
         const bool all_valid = pair_ok && kvalid >= 64;
         ok = mbar_wait(smem_u32(s_full + buf), (jj >> 1) & 1u, abort_flag);
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 // 128 query rows of a step (group g: rows 64 g .. 64 g + 63) and keep P^T
 // in registers between P^T and dS^T.  Issue order: S^T(s), dP^T(s), dV(s),
 // S^T(s+1), dK(s), dP^T(s+1), ...
-template <int D>
+template <int D, bool kFull>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using T = Tiles<D>;
   constexpr int kTile = T::kTile;
@@ -713,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         // per query-row column: -lse log2(e) (-inf on padded rows) and -D
         const float* rs = reinterpret_cast<const float*>(qdo_s + st * kStage + 2 * kTile) + grp * 64;
         // this group's query-row half and this warp's key half selected as a pair?
-        const bool pair_ok = p.full_masks || ((__ldg(lst + s) >> (24 + grp * 2 + (wq >> 1))) & 1);
+        const bool pair_ok = kFull || ((__ldg(lst + s) >> (24 + grp * 2 + (wq >> 1))) & 1);
         const bool need_mask = !(warp_keys_ok && pair_ok);      // warp-uniform
         const float2 km = pair_ok ? km2 : make_float2(0.f, 0.f);
         // P^T = 2^(S^T scale log2(e) - lse log2(e)), kept in registers; bf16 over S^T
@@ -1039,18 +1039,18 @@ BwdWorkspace carve(void* base, int B, int Hq, int Hkv, int Sq, int Skv) {
   return w;
 }
 
-template <int D>
+template <int D, bool kFull>
 bsa_status launch_tiles(const BackwardArgs& a, const BwdWorkspace& w, cudaStream_t stream) {
   bsa_status st;
   static std::atomic<bool> attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr[dev].load(std::memory_order_acquire)) {
-    if ((st = cuda_check(cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((st = cuda_check(cudaFuncSetAttribute(bwd_dq_kernel<D, kFull>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               dq_smem<D>()),
                          "cudaFuncSetAttribute(bwd_dq_kernel)")) != BSA_OK)
       return st;
-    if ((st = cuda_check(cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((st = cuda_check(cudaFuncSetAttribute(bwd_dkdv_kernel<D, kFull>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               dkdv_smem<D>()),
                          "cudaFuncSetAttribute(bwd_dkdv_kernel)")) != BSA_OK)
       return st;
@@ -1078,7 +1078,6 @@ bsa_status launch_tiles(const BackwardArgs& a, const BwdWorkspace& w, cudaStream
     }
     p.b0 = b0; p.Bn = Bn; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.Sq = a.Sq; p.Skv = a.Skv;
     p.nQt = nQt; p.nKt = nKt; p.prefix_len = a.prefix_len;
-    p.full_masks = (a.block_q >= kT && a.block_k == kKT) ? 1 : 0;
     p.dq_list = w.dq_list; p.dq_cnt = w.dq_cnt; p.rowstat = w.rowstat;
     p.inv_cnt = w.inv_cnt; p.inv_list = w.inv_list;
     p.scale = a.scale; p.scale_log2 = a.scale * kLog2e;
@@ -1086,11 +1085,11 @@ bsa_status launch_tiles(const BackwardArgs& a, const BwdWorkspace& w, cudaStream
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
     p.n_items = Bn * a.Hkv * nQt * G;
-    bwd_dq_kernel<D><<<std::min(p.n_items, sms), kThreads, dq_smem<D>(), stream>>>(p);
+    bwd_dq_kernel<D, kFull><<<std::min(p.n_items, sms), kThreads, dq_smem<D>(), stream>>>(p);
     if ((st = cuda_check(cudaGetLastError(), "bwd_dq_kernel launch")) != BSA_OK) return st;
     p.n_items = Bn * a.Hkv * nKt;
     p.counter = w.counters + b0 / kMaxFwdBatch;
-    bwd_dkdv_kernel<D><<<std::min(p.n_items, sms), kThreads, dkdv_smem<D>(), stream>>>(p);
+    bwd_dkdv_kernel<D, kFull><<<std::min(p.n_items, sms), kThreads, dkdv_smem<D>(), stream>>>(p);
     if ((st = cuda_check(cudaGetLastError(), "bwd_dkdv_kernel launch")) != BSA_OK) return st;
   }
   return BSA_OK;
@@ -1150,8 +1149,9 @@ bsa_status launch_backward(const BackwardArgs& a, cudaStream_t stream) {
     bwd_inverse_kernel<<<(unsigned)((warps * 32 + 127) / 128), 128, 0, stream>>>(ip);
     if ((st = cuda_check(cudaGetLastError(), "bwd_inverse_kernel launch")) != BSA_OK) return st;
   }
-  if (a.d == 128) return launch_tiles<128>(a, w, stream);
-  return launch_tiles<64>(a, w, stream);
+  const bool full = a.block_q >= kT && a.block_k == kKT;     // every pair mask full
+  if (a.d == 128) return full ? launch_tiles<128, true>(a, w, stream) : launch_tiles<128, false>(a, w, stream);
+  return full ? launch_tiles<64, true>(a, w, stream) : launch_tiles<64, false>(a, w, stream);
 }
 
 }  // namespace bsa
