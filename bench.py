@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--backward", action="store_true",
                     help="also time bsa_backward (dQ, dK, dV) on the step's outputs and report it")
+    ap.add_argument("--extras", action="store_true",
+                    help="also time the rotary prologue fused with the selector and the causal "
+                         "understanding-stream pass, each against its roofline")
     ap.add_argument("--schedule", choices=["cosmos3", "h3"], default=None,
                     help="time the dense pass and the sparse step and report a dense->sparse schedule")
     return ap.parse_args()
@@ -578,6 +581,65 @@ def main():
                "launches": 6, "launch_note": "prep, bitmap, tile lists, inverse lists, dQ, dK/dV (+1 memset)",
                "calls": n_b, "dout": "seeded N(0,1) bf16"}
 
+    # ---- rotary prologue + selector, causal understanding pass ----
+    extras = None
+    if args.extras:
+        extras = {}
+
+        def timed(fn, n=10):
+            for _ in range(3):
+                fn()
+            bsa.bsa_device_status(stream)
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(n):
+                fn()
+            b_.record(stream)
+            torch.cuda.synchronize()
+            bsa.bsa_device_status(stream)
+            return a.elapsed_time(b_) / n
+
+        # rotary tables (half-split convention, base 10000): understanding positions
+        # 0..P-1 for the prefix keys, generation rows after them
+        inv = 1.0 / (10000.0 ** (torch.arange(0, d, 2, device="cuda", dtype=torch.float64) / d))
+
+        def tables(n, offset):
+            ang = torch.arange(offset, offset + n, device="cuda", dtype=torch.float64)[:, None] * inv[None]
+            ang = torch.cat([ang, ang], dim=1)
+            return ang.cos().float().contiguous(), ang.sin().float().contiguous()
+
+        cq, sq = tables(Sq, P)
+        ck, sk = tables(Skv, 0)
+        q_rot, k_rot = torch.empty_like(q), torch.empty_like(k)
+        r_ms = timed(lambda: bsa.bsa_select_rope(q, k, cq, sq, ck, sk, P, lens, bq, bk, keep, q_out=q_rot,
+                                                 k_out=k_rot, indices=idx, counts=cnt, workspace=ws,
+                                                 stream=stream))
+        s_ms = timed(lambda: bsa.bsa_select(q, k, P, lens, bq, bk, keep, indices=idx, counts=cnt, workspace=ws,
+                                            stream=stream))
+        # Q and K read and their rotations written (bf16), the four tables read (fp32), the block means written
+        r_bytes = (2.0 * (q.numel() + k.numel()) * 2 + 2.0 * (Sq + Skv) * d * 4
+                   + 4.0 * d * (B * Hq * nQb + B * Hkv * nKb))
+        extras["rope_select"] = {
+            "ms": r_ms, "plain_select_ms": s_ms, "bytes": r_bytes, "gb_per_s": r_bytes / (r_ms * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": r_bytes / (r_ms * 1e-3) / 1e9, "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": r_bytes / (r_ms * 1e-3) / 1e9 / pk["hbm"]},
+            "note": "q/k rotated once and pooled in the same pass; score/top-k included in ms"}
+        del q_rot, k_rot
+        # causal self-attention of the understanding stream: this workload's prefix,
+        # and a long one that fills the GPU
+        for pc in sorted({P, 16384}):
+            g = torch.Generator(device="cuda").manual_seed(cfg.seed + pc)
+            qu = torch.randn(B, pc, Hq, d, generator=g, device="cuda").to(torch.bfloat16)
+            ku = torch.randn(B, pc, Hkv, d, generator=g, device="cuda").to(torch.bfloat16)
+            vu = torch.randn(B, pc, Hkv, d, generator=g, device="cuda").to(torch.bfloat16)
+            c_ms = timed(lambda: bsa.bsa_forward_causal(qu, ku, vu, bq, bk, stream=stream))
+            c_flops = 4.0 * d * Hq * B * pc * (pc + 1) / 2      # query row i attends keys 0..i
+            tf = c_flops / (c_ms * 1e-3) / 1e12
+            extras[f"causal_P{pc}"] = {"ms": c_ms, "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16"],
+                                       "flops": c_flops, "rows": pc}
+            del qu, ku, vu
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, idx, cnt)
@@ -606,6 +668,7 @@ def main():
             "clocks": clocks,
             "e2e": e2e,
             **({"backward": bwd} if bwd is not None else {}),
+            **({"extras": extras} if extras is not None else {}),
             "cpu_baseline": cpu,
             "gpu_launches": launches_per_step * args.steps,
         }
