@@ -37,9 +37,6 @@
 #include "bsa_internal.h"
 #include "bsa_ptx.cuh"
 
-#ifndef BSA_SOFTMAX_PACKED
-#define BSA_SOFTMAX_PACKED 1     // packed FFMA2/FADD2 in the softmax
-#endif
 #ifndef BSA_SOFTMAX_MAX3
 #define BSA_SOFTMAX_MAX3 1       // three-input max for the row max
 #endif
@@ -524,42 +521,29 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
         if (grow) m_ref = m_new;
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         // p = 2^(s * scale * log2 e - m): packed FFMA2 for the argument, MUFU
-        // ex2 per element, packed FADD2 row sums in two chains.
-#if BSA_SOFTMAX_PACKED
+        // ex2 per element, packed FADD2 row sums in two chains; P is packed to
+        // bf16 pairs as soon as it is computed and stored over the first BK/2
+        // columns of S_h 64 keys at a time, so the fp32 values do not stay live.
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 nm2 = make_float2(-m_use, -m_use);
         float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < BK; c += 4) {
-          const float2 a = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
-          const float2 b = __ffma2_rn(make_float2(s[c + 2], s[c + 3]), sc2, nm2);
-          s[c] = ex2_approx(a.x);
-          s[c + 1] = ex2_approx(a.y);
-          s[c + 2] = ex2_approx(b.x);
-          s[c + 3] = ex2_approx(b.y);
-          ls0 = __fadd2_rn(ls0, make_float2(s[c], s[c + 1]));
-          ls1 = __fadd2_rn(ls1, make_float2(s[c + 2], s[c + 3]));
-        }
-        const float lsum = (ls0.x + ls0.y) + (ls1.x + ls1.y);
-#else
-        float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-        for (int c = 0; c < BK; c += 2) {
-          s[c] = ex2_approx(fmaf(s[c], p.scale_log2, -m_use));
-          s[c + 1] = ex2_approx(fmaf(s[c + 1], p.scale_log2, -m_use));
-          l0 += s[c];
-          l1 += s[c + 1];
-        }
-        const float lsum = l0 + l1;
-#endif
-        // P (bf16 pairs) over the first BK/2 columns of S_h.
-#pragma unroll
-        for (int c = 0; c < BK / 64; ++c) {
+        for (int cc = 0; cc < BK / 64; ++cc) {
           uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[c * 64 + 2 * i], s[c * 64 + 2 * i + 1]);
-          tmem_st32(s_t + c * 32, pk);
+          for (int c = 0; c < 64; c += 4) {
+            const float2 a = __ffma2_rn(make_float2(s[cc * 64 + c], s[cc * 64 + c + 1]), sc2, nm2);
+            const float2 b = __ffma2_rn(make_float2(s[cc * 64 + c + 2], s[cc * 64 + c + 3]), sc2, nm2);
+            const float2 e0 = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+            const float2 e1 = make_float2(ex2_approx(b.x), ex2_approx(b.y));
+            ls0 = __fadd2_rn(ls0, e0);
+            ls1 = __fadd2_rn(ls1, e1);
+            pk[c / 2] = pack_bf16x2(e0.x, e0.y);
+            pk[c / 2 + 1] = pack_bf16x2(e1.x, e1.y);
+          }
+          tmem_st32(s_t + cc * 32, pk);
         }
+        const float lsum = (ls0.x + ls0.y) + (ls1.x + ls1.y);
         l = l * alpha + lsum;
         // Lazy rescale of O (rare): after P is out of registers, before PV is issued.
         if (__any_sync(0xffffffffu, rescale_o)) {
