@@ -1013,27 +1013,29 @@ struct BwdWorkspace {
   size_t total;
 };
 
+// With base == nullptr only the sizes are computed (pointers stay null).
 BwdWorkspace carve(void* base, int B, int Hq, int Hkv, int Sq, int Skv) {
   const int64_t nQt = cdiv64(Sq, kT), nKt = cdiv64(Skv, kKT), G = Hq / Hkv, words = cdiv64(nKt, 32);
   auto al = [](int64_t x) { return (size_t)((x + 255) & ~(int64_t)255); };
   char* c = static_cast<char*>(base);
   size_t off = 0;
+  auto at = [&](size_t o) -> void* { return c ? static_cast<void*>(c + o) : nullptr; };
   BwdWorkspace w{};
-  w.rowstat = reinterpret_cast<float*>(c + off);
+  w.rowstat = static_cast<float*>(at(off));
   off += al((int64_t)B * Hq * nQt * kRowStat);
-  w.counters = reinterpret_cast<int*>(c + off);
+  w.counters = static_cast<int*>(at(off));
   off += 256;
   w.plane_words = (int64_t)B * Hkv * G * nQt * words;
-  w.planes = reinterpret_cast<uint32_t*>(c + off);
+  w.planes = static_cast<uint32_t*>(at(off));
   w.planes_bytes = al(4 * w.plane_words * 4);
   off += w.planes_bytes;
-  w.dq_list = reinterpret_cast<int32_t*>(c + off);
+  w.dq_list = static_cast<int32_t*>(at(off));
   off += al((int64_t)B * Hq * nQt * nKt * 4);
-  w.dq_cnt = reinterpret_cast<int32_t*>(c + off);
+  w.dq_cnt = static_cast<int32_t*>(at(off));
   off += al((int64_t)B * Hq * nQt * 4);
-  w.inv_cnt = reinterpret_cast<int32_t*>(c + off);
+  w.inv_cnt = static_cast<int32_t*>(at(off));
   off += al((int64_t)B * Hkv * nKt * 4);
-  w.inv_list = reinterpret_cast<int32_t*>(c + off);
+  w.inv_list = static_cast<int32_t*>(at(off));
   off += al((int64_t)B * Hkv * nKt * G * nQt * 4);
   w.total = off;
   return w;
