@@ -416,10 +416,22 @@ static bsa_status launch_topk(const SelectArgs& a, cudaStream_t stream) {
     if (smem > 227 * 1024)
       return set_error(BSA_ERR_UNSUPPORTED, "bsa_select: too many key blocks (nKb=" +
                                                 std::to_string(a.nKb) + ") for one CTA's shared memory");
-    if ((st = cuda_check(cudaFuncSetAttribute(score_topk_kernel,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-                         "cudaFuncSetAttribute(score_topk_kernel)")) != BSA_OK)
-      return st;
+    // The kernel's shared-memory limit is raised once per device and size
+    // (never lowered), so calls captured in a CUDA graph only launch.
+    {
+      static std::mutex mu;
+      static int smem_set[64] = {};
+      int dev = 0;
+      cudaGetDevice(&dev);
+      std::lock_guard<std::mutex> lock(mu);
+      if (dev >= 64 || smem_set[dev] < (int)smem) {
+        if ((st = cuda_check(cudaFuncSetAttribute(score_topk_kernel,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                             "cudaFuncSetAttribute(score_topk_kernel)")) != BSA_OK)
+          return st;
+        if (dev < 64) smem_set[dev] = (int)smem;
+      }
+    }
     dim3 grid((a.nQb + kRows - 1) / kRows, a.Hq, a.B);
     score_topk_kernel<<<grid, kTopkThreads, smem, stream>>>(p);
     if ((st = cuda_check(cudaGetLastError(), "score_topk_kernel launch")) != BSA_OK) return st;

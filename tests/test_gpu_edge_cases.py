@@ -77,7 +77,9 @@ def test_edge_case_select_forward_backward(name):
         assert np.isfinite(gn).all(), name_
         nr = np.linalg.norm(r)
         if nr == 0:
-            assert (gn == 0).all(), name_
+            # exact zero (e.g. a row whose only key gets P = 1, so dS = dP - D = 0): the GPU
+            # forms dP (MMA) and D (its own fp32 sum) in different orders, rounding-level values
+            assert np.abs(gn).max() <= 1e-4, name_
         else:
             assert np.linalg.norm(gn - r) / nr <= 1e-2, (name_, np.linalg.norm(gn - r) / nr)
             assert np.abs(gn - r).max() <= 3e-2 * np.abs(r).max(), name_

@@ -77,7 +77,9 @@ def test_random_geometry(i):
         assert np.isfinite(gn).all(), (cfg, name)
         nr = np.linalg.norm(r)
         if nr == 0:
-            assert (gn == 0).all(), (cfg, name)
+            # exact zero, e.g. a row whose only key gets P = 1 so that dS = dP - D = 0;
+            # the GPU forms dP (MMA) and D (its own fp32 sum) in different orders
+            assert np.abs(gn).max() <= 1e-4, (cfg, name, np.abs(gn).max())
             continue
         rel = np.linalg.norm(gn - r) / nr
         assert rel <= 1e-2 and np.abs(gn - r).max() <= 3e-2 * np.abs(r).max(), (cfg, name, rel)
