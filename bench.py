@@ -500,7 +500,8 @@ def main():
 
         def run_e2e(n):
             loaded = [torch.cuda.Event() for _ in range(n)]
-            computed = [torch.cuda.Event() for _ in range(n)]
+            computed = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+            began = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
             drained = [torch.cuda.Event() for _ in range(n)]
             start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             start.record(h2d_stream)
@@ -517,6 +518,7 @@ def main():
                     stream.wait_event(loaded[i])
                     if i >= 2:
                         stream.wait_event(drained[i - 2])   # its output buffer was read back
+                    began[i].record(stream)
                     bsa.bsa_select(bf["q"], bf["k"], P, lens, bq, bk, keep, indices=bf["idx"], counts=bf["cnt"],
                                    workspace=ws2[i % 2], stream=stream)
                     bsa.bsa_forward(bf["q"], bf["k"], bf["v"], bf["idx"], bf["cnt"], P, lens, bq, bk, out=bf["out"],
@@ -532,16 +534,19 @@ def main():
             d2h_stream.wait_event(drained[n - 1])
             end.record(d2h_stream)
             torch.cuda.synchronize()
-            return start.elapsed_time(end) / n
+            compute = sum(b.elapsed_time(c) for b, c in zip(began, computed)) / n
+            return start.elapsed_time(end) / n, compute
 
         run_e2e(2)
         bsa.bsa_device_status(stream)
-        e_ms = max_over_ranks(run_e2e(n_e2e), device="cuda")
+        e_ms, e_compute_ms = run_e2e(n_e2e)
+        e_ms = max_over_ranks(e_ms, device="cuda")
         bsa.bsa_device_status(stream)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk_, hv))
         d2h = houts[0].numel() * houts[0].element_size() + hlses[0].numel() * hlses[0].element_size()
         e2e = {"value": whole_job_tflops(flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "compute_ms_per_step_during_copies": e_compute_ms,
                "pipelining": "double-buffered device inputs/outputs; H2D and D2H on their own streams "
                              "overlap the neighbouring steps' compute"}
         del bufs[1], ws2[1], fws2[1]
