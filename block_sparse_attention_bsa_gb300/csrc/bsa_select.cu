@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const __grid_c
 
   float* qT = sm;                                                    // [D][kRows]
   uint32_t* keys = reinterpret_cast<uint32_t*>(qT + D * kRows);      // [kRows][nKb]
+  uint32_t* hist_all = keys + kRows * p.nKb;                         // [warps][256]
 
   if (rows_valid > 0 && kh > 0 && kh < N) {
     for (int i = threadIdx.x; i < D * kRows; i += blockDim.x) {
@@ -316,15 +317,54 @@ __global__ void __launch_bounds__(kTopkThreads) score_topk_kernel(const __grid_c
       continue;
     }
     const uint32_t* my_keys = keys + r * p.nKb;
-    // Threshold T = largest key with count(key >= T) >= kh, i.e. the kh-th key.
-    uint32_t T = 0;
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t cand = T | (1u << bit);
-      int cnt = 0;
-      for (int i = lane; i < N; i += 32) cnt += (my_keys[i] >= cand) ? 1 : 0;
+    // Threshold T = the kh-th largest key: most-significant-digit radix
+    // select, 8 bits per pass, on a 256-bin histogram (one per warp) of the
+    // keys whose higher digits equal those already chosen.  `remaining` is
+    // T's rank among those keys.
+    uint32_t* hist = hist_all + warp * 256;
+    uint32_t T = 0, chosen = 0;
+    uint32_t remaining = (uint32_t)kh;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = lane; i < 256; i += 32) hist[i] = 0u;
+      __syncwarp();
+      for (int i = lane; i < N; i += 32) {
+        const uint32_t key = my_keys[i];
+        if ((key & chosen) == T) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      }
+      __syncwarp();
+      // lane l holds digits 8 l .. 8 l + 7; `above` = keys with a larger digit
+      uint32_t c[8], tot = 0;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-      if (cnt >= kh) T = cand;
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[lane * 8 + j];
+        tot += c[j];
+      }
+      uint32_t suf = tot;                 // keys with digit >= 8 lane (inclusive suffix scan)
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += t;
+      }
+      uint32_t above = suf - tot;
+      int found = -1;
+      uint32_t above_found = 0;
+#pragma unroll
+      for (int j = 7; j >= 0; --j) {
+        if (found < 0 && above + c[j] >= remaining) {
+          found = lane * 8 + j;
+          above_found = above;
+        }
+        above += c[j];
+      }
+      // the digit is the largest one with (keys above it) < remaining <=
+      // (keys at or above it): the highest lane that found one
+      const uint32_t ball = __ballot_sync(0xffffffffu, found >= 0);
+      const int src = 31 - __clz(ball);
+      const int digit = __shfl_sync(0xffffffffu, found, src);
+      remaining -= __shfl_sync(0xffffffffu, above_found, src);
+      T |= (uint32_t)digit << shift;
+      chosen |= 255u << shift;
+      __syncwarp();
     }
     int c_gt = 0;
     for (int i = lane; i < N; i += 32) c_gt += (my_keys[i] > T) ? 1 : 0;
@@ -412,7 +452,8 @@ static bsa_status launch_topk(const SelectArgs& a, cudaStream_t stream) {
     for (int b = 0; b < a.B; ++b) p.seq_lens[b] = a.seq_lens ? a.seq_lens[b] : a.Sq;
     for (int h = 0; h < a.Hq; ++h) p.keep[h] = a.keep[h];
     p.indices = a.indices; p.counts = a.counts;
-    const size_t smem = sizeof(float) * (size_t)kRows * a.d + sizeof(uint32_t) * (size_t)kRows * a.nKb;
+    const size_t smem = sizeof(float) * (size_t)kRows * a.d + sizeof(uint32_t) * (size_t)kRows * a.nKb +
+                        sizeof(uint32_t) * 256 * (kTopkThreads / 32);   // q means, keys, radix histograms
     if (smem > 227 * 1024)
       return set_error(BSA_ERR_UNSUPPORTED, "bsa_select: too many key blocks (nKb=" +
                                                 std::to_string(a.nKb) + ") for one CTA's shared memory");
