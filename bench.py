@@ -69,8 +69,8 @@ def peaks():
 # launch, from an ncu capture of the build whose FMHA sources hash to `sha`.
 # When the sources change the figure no longer applies and traffic is null.
 FMHA_TRAFFIC = {
-    "sha": "2da9ecc6859ccccd",
-    "720p_75": 13991214080 + 1763857664,  # profiles/launches_720p_75.md (1-pass capture)
+    "sha": "583341dbae4e2025",
+    "720p_75": 13762209536 + 1723728384,  # profiles/launches_720p_75.md (1-pass capture)
 }
 
 
