@@ -32,8 +32,8 @@
  *    sequence from position 0.  nQb = ceil(Sq/block_q), nKb = ceil(Skv/block_k).
  *    A key block holding any prefix position is a prefix block:
  *    npb = ceil(prefix_len/block_k).
- *  - Supported: d in {64, 128}; (block_q, block_k) in {(64,64), (128,128),
- *    (256,128), (128,64), (256,64)}; Hq % Hkv == 0; bf16 only.  Anything else
+ *  - Supported: d in {64, 128}; block_q in {64, 128, 256} with block_k in
+ *    {64, 128} (all six pairs); Hq % Hkv == 0; bf16 only.  Anything else
  *    returns BSA_ERR_UNSUPPORTED (no fallback path exists).
  *  - Errors: every call validates its arguments on the host before launching
  *    and returns a status; bsa_get_last_error() gives a message naming the
