@@ -71,6 +71,9 @@ def peaks():
 FMHA_TRAFFIC = {
     "sha": "583341dbae4e2025",
     "720p_75": 13762209536 + 1723728384,  # profiles/launches_720p_75.md (1-pass capture)
+    "480p_75": 504095488 + 267694592,     # profiles/fmha_fwd_480p_75.md (full capture)
+    "480p_dense": 511859200 + 268388864,  # profiles/fmha_fwd_480p_dense.md (full capture)
+    "1280x736_ragged": 23763440896 + 2600387328,  # profiles/fmha_traffic_1280x736_ragged.md (1-pass)
 }
 
 
