@@ -69,11 +69,12 @@ def peaks():
 # launch, from an ncu capture of the build whose FMHA sources hash to `sha`.
 # When the sources change the figure no longer applies and traffic is null.
 FMHA_TRAFFIC = {
-    "sha": "583341dbae4e2025",
-    "720p_75": 13762209536 + 1723728384,  # profiles/launches_720p_75.md (1-pass capture)
-    "480p_75": 504095488 + 267694592,     # profiles/fmha_fwd_480p_75.md (full capture)
-    "480p_dense": 511859200 + 268388864,  # profiles/fmha_fwd_480p_dense.md (full capture)
-    "1280x736_ragged": 23763440896 + 2600387328,  # profiles/fmha_traffic_1280x736_ragged.md (1-pass)
+    "sha": "d767523b2f71cede",
+    # 1-pass captures (dram__bytes_read.sum + dram__bytes_write.sum of one launch)
+    "720p_75": 13786234368 + 1723731968,          # profiles/launches_720p_75.md
+    "480p_75": 504559616 + 267785216,             # profiles/fmha_fwd_480p_75.md
+    "480p_dense": 511170560 + 268515584,          # profiles/fmha_fwd_480p_dense.md
+    "1280x736_ragged": 23944224512 + 2601367296,  # profiles/fmha_traffic_1280x736_ragged.md
 }
 
 

@@ -145,6 +145,28 @@ __device__ __forceinline__ TileInfo decode_tile(const FmhaParams& p, int t, int 
   return ti;
 }
 
+// Max of v[LO .. LO + N) in four independent chains of three-input max.
+template <int LO, int N, int M>
+__device__ __forceinline__ float row_max(const float (&v)[M]) {
+  static_assert(LO + N <= M && N % 8 == 0, "row range");
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int c = LO; c < LO + N; c += 8) {
+#if BSA_SOFTMAX_MAX3
+    m0 = max3f(m0, v[c], v[c + 1]);
+    m1 = max3f(m1, v[c + 2], v[c + 3]);
+    m2 = max3f(m2, v[c + 4], v[c + 5]);
+    m3 = max3f(m3, v[c + 6], v[c + 7]);
+#else
+    m0 = fmaxf(fmaxf(m0, v[c]), v[c + 1]);
+    m1 = fmaxf(fmaxf(m1, v[c + 2]), v[c + 3]);
+    m2 = fmaxf(fmaxf(m2, v[c + 4]), v[c + 5]);
+    m3 = fmaxf(fmaxf(m3, v[c + 6]), v[c + 7]);
+#endif
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
 struct Ring {
   uint32_t stage = 0, phase = 0;
   template <int S>
@@ -469,6 +491,22 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       for (int j = 0; j < ti.steps; ++j) {
         const int kb = entry_block(KB < BK ? 2 * j : j);
         const int kb1 = KB < BK ? entry_block(2 * j + 1) : 0;    // second 64-key half of the tile
+        // keys of this block this row may see: the real keys, and in a causal
+        // pass only positions <= the row
+        const int kv_end = p.causal ? min(ti.valid_kv, row + 1) : ti.valid_kv;
+        // Paired 64-key blocks: a half that this row cannot see at all (a block
+        // its own query block did not select in a merged list, or one past the
+        // end) takes no part in the max and is not exponentiated; its P is
+        // stored as zeros.
+        // The test is uniform over a warp except in a causal pass.
+        int kvalid0 = BK, kvalid1 = BK;
+        bool skip0 = false, skip1 = false;
+        if constexpr (KB < BK) {
+          kvalid0 = kv_end - kb * KB;
+          kvalid1 = kv_end - kb1 * KB;
+          skip0 = kvalid0 <= 0;
+          skip1 = kvalid1 <= 0;
+        }
         ok = mbar_wait(smem_u32(s_full + hh), sph & 1u, abort_flag);
         ++sph;
         if (!ok) break;
@@ -477,9 +515,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < BK / 32; ++c) tmem_ld32f(s_t + c * 32, s + c * 32);
         tmem_wait_ld();
-        // keys of this block this row may see: the real keys, and in a causal
-        // pass only positions <= the row
-        const int kv_end = p.causal ? min(ti.valid_kv, row + 1) : ti.valid_kv;
+        float mx;
         if constexpr (KB == BK) {
           const int kvalid = kv_end - kb * BK;
           if (kvalid < BK) {
@@ -487,33 +523,19 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
             for (int c = 0; c < BK; ++c)
               if (c >= kvalid) s[c] = -INFINITY;
           }
+          mx = row_max<0, BK>(s);
         } else {
-          const int kvalid0 = kv_end - kb * KB, kvalid1 = kv_end - kb1 * KB;
-          if (kvalid0 < KB || kvalid1 < KB) {
+          if ((!skip0 && kvalid0 < KB) || (!skip1 && kvalid1 < KB)) {
 #pragma unroll
             for (int c = 0; c < KB; ++c) {
               if (c >= kvalid0) s[c] = -INFINITY;
               if (c >= kvalid1) s[KB + c] = -INFINITY;
             }
           }
+          const float mx_lo = skip0 ? -INFINITY : row_max<0, KB>(s);
+          const float mx_hi = skip1 ? -INFINITY : row_max<KB, KB>(s);
+          mx = fmaxf(mx_lo, mx_hi);
         }
-        // Row max: four independent chains of three-input max.
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < BK; c += 8) {
-#if BSA_SOFTMAX_MAX3
-          mx0 = max3f(mx0, s[c], s[c + 1]);
-          mx1 = max3f(mx1, s[c + 2], s[c + 3]);
-          mx2 = max3f(mx2, s[c + 4], s[c + 5]);
-          mx3 = max3f(mx3, s[c + 6], s[c + 7]);
-#else
-          mx0 = fmaxf(fmaxf(mx0, s[c]), s[c + 1]);
-          mx1 = fmaxf(fmaxf(mx1, s[c + 2]), s[c + 3]);
-          mx2 = fmaxf(fmaxf(mx2, s[c + 4]), s[c + 5]);
-          mx3 = fmaxf(fmaxf(mx3, s[c + 6]), s[c + 7]);
-#endif
-        }
-        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         const float m_new = fmaxf(m_ref, mx * p.scale_log2);
         const bool grow = m_new > m_ref + 8.0f;
         const bool rescale_o = grow && m_ref != -INFINITY;
@@ -530,6 +552,14 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < BK / 64; ++cc) {
           uint32_t pk[32];
+          if constexpr (KB < BK) {           // a skipped 64-key half: P = 0
+            if (cc == 0 ? skip0 : skip1) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) pk[i] = 0u;
+              tmem_st32(s_t + cc * 32, pk);
+              continue;
+            }
+          }
 #pragma unroll
           for (int c = 0; c < 64; c += 4) {
             const float2 a = __ffma2_rn(make_float2(s[cc * 64 + c], s[cc * 64 + c + 1]), sc2, nm2);
