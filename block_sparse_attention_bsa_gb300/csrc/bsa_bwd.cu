@@ -383,6 +383,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         ok = mbar_wait(smem_u32(s_full + buf), (jj >> 1) & 1u, abort_flag);
         if (!ok) break;
         tc_fence_after();
+        if constexpr (!kFull) {
+          if (!pair_ok) {
+            // a pair no query block of these rows listed: P = 0, so dS = 0; it
+            // is stored once this block's dP has landed (the MMA writes those
+            // columns)
+            ok = mbar_wait(smem_u32(dp_full), jj & 1u, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t zk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) zk[i] = 0u;
+            tmem_st16(tl + 256 + grp * 64, zk);
+            tmem_st16(tl + 256 + grp * 64 + 16, zk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(ds_full));
+            continue;
+          }
+        }
         // P = 2^(S scale log2(e) - lse log2(e)), kept in registers
         float pr[64];
 #pragma unroll
@@ -714,6 +733,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         const float* rs = reinterpret_cast<const float*>(qdo_s + st * kStage + 2 * kTile) + grp * 64;
         // this group's query-row half and this warp's key half selected as a pair?
         const bool pair_ok = kFull || ((__ldg(lst + s) >> (24 + grp * 2 + (wq >> 1))) & 1);
+        if constexpr (!kFull) {
+          if (!pair_ok) {
+            // a pair this query block did not list: P^T = 0 and dS^T = 0 for
+            // these keys and rows, stored without exponentials once the MMAs
+            // have written the columns (S^T now, dP^T after its barrier)
+            uint32_t zk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) zk[i] = 0u;
+            tmem_st16(tl + grp * 64, zk);
+            tmem_st16(tl + grp * 64 + 16, zk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(p_full));
+            ok = mbar_wait(smem_u32(dp_full), dc & 1u, abort_flag);
+            ++dc;
+            if (!ok) break;
+            tc_fence_after();
+            tmem_st16(tl + 128 + grp * 64, zk);
+            tmem_st16(tl + 128 + grp * 64 + 16, zk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(ds_full));
+            continue;
+          }
+        }
         const bool need_mask = !(warp_keys_ok && pair_ok);      // warp-uniform
         const float2 km = pair_ok ? km2 : make_float2(0.f, 0.f);
         // P^T = 2^(S^T scale log2(e) - lse log2(e)), kept in registers; bf16 over S^T
