@@ -1,8 +1,9 @@
 """Degenerate inputs through the CUDA selector, forward and backward, each
 against the fp64 oracle on the same bits: an empty request in a batch, a
 sequence shorter than one query block, keep ratio 0 with a protected prefix
-(the lists hold the prefix blocks only), and a prefix that is not a multiple
-of the key block with ragged lengths.  Inputs of the forward and backward
+(the lists hold the prefix blocks only), a prefix that is not a multiple of
+the key block with ragged lengths, and batches of more requests than one
+launch takes (8).  Inputs of the forward and backward
 come from the oracle (its selection, its forward), never from the CUDA path.
 """
 
@@ -26,6 +27,13 @@ CASES = {
                            block_k=128, keep=0.0, recipe="iid", seed=3003),
     "odd_prefix_ragged": Config("odd_prefix_ragged", B=3, Hq=4, Hkv=1, d=64, prefix=100, lens=(333, 64, 1),
                                 block_q=64, block_k=64, keep=0.35, recipe="iid", seed=3004),
+    # more requests than one forward/backward launch takes (8): two launches
+    "batch_11_two_launches": Config("batch_11_two_launches", B=11, Hq=4, Hkv=2, d=64, prefix=64,
+                                    lens=(300, 0, 17, 256, 129, 1, 64, 200, 90, 333, 5), block_q=256,
+                                    block_k=128, keep=0.4, recipe="iid", seed=3005),
+    "batch_10_64x64": Config("batch_10_64x64", B=10, Hq=2, Hkv=1, d=128, prefix=100,
+                             lens=(130, 64, 0, 1, 250, 65, 190, 7, 128, 99), block_q=64, block_k=64, keep=0.3,
+                             recipe="iid", seed=3006),
 }
 
 
