@@ -104,6 +104,25 @@ def test_backward_is_deterministic():
         assert torch.equal(x, y)
 
 
+def test_backward_strided_inputs_match_contiguous():
+    """q, k, v, out and dout as views of packed buffers (16-byte aligned, not
+    contiguous): the same gradient bits as contiguous copies."""
+    inp, idx, cnt, out_bf, lse32, dout, _ = oracle_case("small_gqa")
+    c = inp["cfg"]
+    a = run_backward(inp, idx, cnt, out_bf, lse32, dout)
+    q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    qp = torch.zeros(c.B, c.Sq, 3, c.Hq, c.d, dtype=torch.bfloat16, device="cuda")  # q, out, dout side by side
+    qp[:, :, 0], qp[:, :, 1], qp[:, :, 2] = q, out_bf.cuda(), dout.cuda()
+    kv = torch.stack([k, v], dim=2)
+    views = (qp[:, :, 0], kv[:, :, 0], kv[:, :, 1], qp[:, :, 1], qp[:, :, 2])
+    assert not any(t.is_contiguous() for t in views)
+    b = bsa.bsa_backward(*views, lse32.cuda(), torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda(),
+                         c.prefix, inp["seq_lens"], c.block_q, c.block_k)
+    bsa.bsa_device_status()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
 def test_backward_dense_lists_match_oracle():
     """keep ratio 1: every valid key block of every row (the dense pass's lists)."""
     inp, idx, cnt, out_bf, lse32, dout, (dq_r, dk_r, dv_r) = oracle_case("small_gqa", keep=[1.0])

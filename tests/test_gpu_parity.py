@@ -133,6 +133,21 @@ def test_dropped_blocks_leave_output_bitwise_unchanged():
     assert torch.equal(lse, lse2)
 
 
+@pytest.mark.parametrize("name", ["small_gqa", "small_64x64_d128"])
+def test_forward_without_lse_writes_the_same_output(name):
+    """lse = NULL (return_lse=False): the kernel skips the LSE stores and
+    writes the same output bits."""
+    inp = cuda_inputs(name)
+    c = inp["cfg"]
+    idx, cnt = run_select(inp)
+    out, lse = run_forward(inp, idx, cnt)
+    out2, lse2 = bsa.bsa_forward(inp["q"], inp["k"], inp["v"], idx, cnt, c.prefix, inp["seq_lens"], c.block_q,
+                                 c.block_k, return_lse=False)
+    bsa.bsa_device_status()
+    assert lse2 is None
+    assert torch.equal(out, out2)
+
+
 def test_rows_sum_to_one():
     inp = cuda_inputs("small_gqa")
     idx, cnt = run_select(inp)
