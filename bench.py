@@ -69,12 +69,12 @@ def peaks():
 # launch, from an ncu capture of the build whose FMHA sources hash to `sha`.
 # When the sources change the figure no longer applies and traffic is null.
 FMHA_TRAFFIC = {
-    "sha": "d767523b2f71cede",
+    "sha": "23fc1a5077027a58",
     # 1-pass captures (dram__bytes_read.sum + dram__bytes_write.sum of one launch)
-    "720p_75": 13786234368 + 1723731968,          # profiles/launches_720p_75.md
-    "480p_75": 504559616 + 267785216,             # profiles/fmha_fwd_480p_75.md
-    "480p_dense": 511170560 + 268515584,          # profiles/fmha_fwd_480p_dense.md
-    "1280x736_ragged": 23944224512 + 2601367296,  # profiles/fmha_traffic_1280x736_ragged.md
+    "720p_75": 13786140928 + 1723019008,          # profiles/launches_720p_75.md
+    "480p_75": 503945984 + 268207872,             # profiles/fmha_fwd_480p_75.md
+    "480p_dense": 510417920 + 270237184,          # profiles/fmha_fwd_480p_dense.md
+    "1280x736_ragged": 23890579712 + 2600347136,  # profiles/fmha_traffic_1280x736_ragged.md
 }
 
 

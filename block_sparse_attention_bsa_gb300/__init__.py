@@ -11,6 +11,7 @@ from .api import (  # noqa: F401
     BsaError,
     bsa_backward,
     bsa_backward_workspace_size,
+    bsa_debug_wait_probe,
     bsa_device_status,
     bsa_forward,
     bsa_forward_causal,

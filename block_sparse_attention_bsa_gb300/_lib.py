@@ -58,6 +58,7 @@ SIGNATURES = {
                           _P, _P, _P, _P, _SZ, _P]),
     "bsa_validate_indices": (_I, [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _I32, _I32, _I32, _P, _P]),
     "bsa_device_status": (_I, [_P]),
+    "bsa_debug_wait_probe": (_I, [_I32, ctypes.c_uint64, _P]),
 }
 
 

@@ -308,3 +308,11 @@ def bsa_validate_indices(indices: torch.Tensor, counts: torch.Tensor, B: int, Hq
 def bsa_device_status(stream=None) -> None:
     """Synchronises and raises BsaError if a bounded device wait gave up."""
     _check(_lib.load().bsa_device_status(_stream_ptr(stream)))
+
+
+def bsa_debug_wait_probe(family: int, limit_ns: int, stream=None) -> None:
+    """Enqueues a one-thread kernel whose bounded mbarrier wait (the kernels'
+    wait code, limit ``limit_ns``) runs out on purpose, so that the next
+    ``bsa_device_status`` raises a timeout; ``family`` 0 is the forward side,
+    1 the backward kernels.  For testing the timeout reporting path."""
+    _check(_lib.load().bsa_debug_wait_probe(int(family), int(limit_ns), _stream_ptr(stream)))

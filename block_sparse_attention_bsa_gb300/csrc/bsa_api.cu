@@ -451,10 +451,28 @@ bsa_status bsa_device_status(bsa_stream_t stream) {
   clear_error();
   bsa_status st = cuda_check(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)), "cudaStreamSynchronize");
   if (st != BSA_OK) return st;
-  const unsigned int e = read_and_clear_device_error();
-  if (e == 0xFFFFFFFFu) return set_error(BSA_ERR_CUDA, "bsa_device_status: cannot read the device error word");
-  if (e & 1u) return set_error(BSA_ERR_TIMEOUT, "a bounded device wait gave up (kernel aborted its tiles)");
+  // the forward kernels' and the backward kernels' error words (each read and cleared)
+  const unsigned int ef = read_and_clear_fwd_error();
+  const unsigned int eb = read_and_clear_bwd_error();
+  if (ef == 0xFFFFFFFFu || eb == 0xFFFFFFFFu)
+    return set_error(BSA_ERR_CUDA, "bsa_device_status: cannot read the device error word");
+  if ((ef | eb) & 1u)
+    return set_error(BSA_ERR_TIMEOUT, std::string("a bounded device wait gave up in the ") +
+                                          (ef & 1u ? (eb & 1u ? "forward and backward" : "forward") : "backward") +
+                                          " kernels (the kernel aborted its tiles)");
   return BSA_OK;
+}
+
+bsa_status bsa_debug_wait_probe(int32_t family, uint64_t limit_ns, bsa_stream_t stream) {
+  clear_error();
+  if (family != 0 && family != 1)
+    return set_error(BSA_ERR_INVALID_ARG, "bsa_debug_wait_probe: family " + s(family) +
+                                              " is not 0 (forward kernels) or 1 (backward kernels)");
+  if (limit_ns < 1000000ull || limit_ns > 10000000000ull)
+    return set_error(BSA_ERR_INVALID_ARG, "bsa_debug_wait_probe: limit_ns " + std::to_string(limit_ns) +
+                                              " is outside [1 ms, 10 s]");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return family == 0 ? launch_fwd_wait_probe(limit_ns, st) : launch_bwd_wait_probe(limit_ns, st);
 }
 
 }  // extern "C"

@@ -1200,4 +1200,11 @@ bsa_status launch_backward(const BackwardArgs& a, cudaStream_t stream) {
   return full ? launch_tiles<64, true>(a, w, stream) : launch_tiles<64, false>(a, w, stream);
 }
 
+unsigned int read_and_clear_bwd_error() { return take_error_word(); }
+
+bsa_status launch_bwd_wait_probe(unsigned long long limit_ns, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cuda_check(cudaGetLastError(), "wait_probe_kernel launch (backward)");
+}
+
 }  // namespace bsa

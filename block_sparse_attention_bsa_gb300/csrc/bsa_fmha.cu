@@ -763,11 +763,11 @@ size_t forward_chunk_bytes(int Hq) {
   return 256 + (((size_t)4 * kMaxFwdBatch * Hq + 255) & ~(size_t)255);
 }
 
-unsigned int read_and_clear_device_error() {
-  unsigned int v = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&v, g_bsa_error, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
-  if (v != 0) cudaMemcpyToSymbol(g_bsa_error, &zero, sizeof(zero));
-  return v;
+unsigned int read_and_clear_fwd_error() { return take_error_word(); }
+
+bsa_status launch_fwd_wait_probe(unsigned long long limit_ns, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cuda_check(cudaGetLastError(), "wait_probe_kernel launch (forward)");
 }
 
 // ------------------------------------------------------ merged lists ---

@@ -98,7 +98,11 @@ bsa_status launch_backward(const BackwardArgs& a, cudaStream_t stream);
 
 // Device error word of the current device (0xFFFFFFFF if it cannot be read);
 // cleared after reading.
-unsigned int read_and_clear_device_error();
+// Each translation unit with device waits keeps its own device error word.
+unsigned int read_and_clear_fwd_error();
+unsigned int read_and_clear_bwd_error();
+bsa_status launch_fwd_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
+bsa_status launch_bwd_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
 
 // ---- validation (bsa_api.cu) ----
 size_t select_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int d, int bq, int bk);

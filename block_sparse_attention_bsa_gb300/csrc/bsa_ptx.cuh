@@ -8,9 +8,10 @@
 
 namespace bsa {
 
-// Device error word: bit 0 = a bounded wait gave up.  Read and cleared by
-// bsa_device_status() on the host (through read_and_clear_device_error(), in
-// the one translation unit that includes this header).
+// Device error word: bit 0 = a bounded wait gave up.  Without relocatable
+// device code every translation unit that includes this header has its own
+// copy; each one exports a reader built on take_error_word() below, and
+// bsa_device_status() reads and clears all of them.
 static __device__ unsigned int g_bsa_error = 0;
 
 constexpr unsigned int kErrTimeout = 1u;
@@ -61,22 +62,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits until the phase with parity `parity` of `bar` has completed.  Gives
 // up (returns false) when *abort is set by another role of the CTA or after
-// kWaitTimeoutNs; a timeout sets g_bsa_error and *abort so that every role
-// of the CTA leaves its loop and the CTA can free its TMEM and exit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// limit_ns; a timeout sets g_bsa_error and *abort so that every role of the
+// CTA leaves its loop and the CTA can free its TMEM and exit.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int* abort,
+                                              unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         atomicOr(&g_bsa_error, kErrTimeout);
         *abort = 1;
         return false;
       }
     }
   }
+}
+
+// The kernels' wait: mbar_wait_for with the kWaitTimeoutNs limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return mbar_wait_for(bar, parity, abort, kWaitTimeoutNs);
 }
 
 // Bounded wait that ignores the abort flag, for the way out of a kernel: a
@@ -361,6 +368,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Host: reads and clears this translation unit's copy of the device error
+// word (0xFFFFFFFF if it cannot be read or cleared).
+static inline unsigned int take_error_word() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_bsa_error, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (v != 0 && cudaMemcpyToSymbol(g_bsa_error, &zero, sizeof(zero)) != cudaSuccess) return 0xFFFFFFFFu;
+  return v;
+}
+
+// One thread waits, with the kernels' bounded-wait code and a limit of
+// limit_ns, for phase 0 of an mbarrier that nothing arrives on: the wait
+// gives up, the timeout lands in this translation unit's error word, and the
+// kernel exits.  Used to test that timeouts are reported.
+static __global__ void __launch_bounds__(32, 1) wait_probe_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    mbar_wait_for(smem_u32(&bar), 0u, &abort_flag, limit_ns);
+  }
 }
 
 }  // namespace bsa

@@ -284,6 +284,18 @@ BSA_API bsa_status bsa_validate_indices(const int32_t* indices, const int32_t* c
  * the last call, BSA_ERR_CUDA if the stream reports an error, else BSA_OK. */
 BSA_API bsa_status bsa_device_status(bsa_stream_t stream);
 
+/* Diagnostics for the timeout path above.  Enqueues on `stream` one
+ * single-thread kernel that waits, with the same bounded-wait code the
+ * attention kernels use but a limit of `limit_ns`, for an mbarrier phase that
+ * nothing completes: the wait gives up after limit_ns, records the timeout in
+ * the device error word of the kernel family `family` (0 = selector-side and
+ * forward kernels, 1 = backward kernels) and the kernel exits normally, so
+ * the CUDA context stays usable.  The next bsa_device_status() returns
+ * BSA_ERR_TIMEOUT.  No fault, trap or hang is involved.
+ * Errors: BSA_ERR_INVALID_ARG for another family or a limit outside
+ * [1 ms, 10 s]; BSA_ERR_CUDA if the launch fails. */
+BSA_API bsa_status bsa_debug_wait_probe(int32_t family, uint64_t limit_ns, bsa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,7 @@ def test_header_declares_the_expected_calls():
         "bsa_version", "bsa_get_last_error", "bsa_select_workspace_size", "bsa_select",
         "bsa_forward_workspace_size", "bsa_forward", "bsa_validate_indices", "bsa_device_status",
         "bsa_select_noalloc", "bsa_forward_causal", "bsa_select_rope",
-        "bsa_backward_workspace_size", "bsa_backward",
+        "bsa_backward_workspace_size", "bsa_backward", "bsa_debug_wait_probe",
     ])
 
 
@@ -299,3 +299,10 @@ def test_backward_workspace_size_formula(lib):
     for bq, bk in ((256, 128), (64, 64), (128, 64)):
         assert lib.bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, bq, bk) == want
     assert lib.bsa_backward_workspace_size(B, Hq, 5, Sq, Skv, 256, 128) == 0
+
+
+def test_wait_probe_rejects_bad_arguments(lib):
+    for fam, lim in ((2, 10 ** 8), (-1, 10 ** 8), (0, 999_999), (1, 10 ** 10 + 1)):
+        st = lib.bsa_debug_wait_probe(fam, lim, None)
+        assert st == 1, (fam, lim, st)                      # BSA_ERR_INVALID_ARG, nothing launched
+        assert b"bsa_debug_wait_probe" in lib.bsa_get_last_error()
