@@ -1,11 +1,13 @@
-"""The bounded-wait timeout path on the GPU, without any fault, trap or hang.
+"""Failure detection on the GPU, without any fault, trap or hang: the
+bounded-wait timeout path, and outputs written in bounds only.
 
 A one-thread kernel waits, with the attention kernels' bounded-wait code and a
 short limit, for an mbarrier phase that nothing completes.  The wait gives up,
 records the timeout in the device error word of its kernel family and exits;
 ``bsa_device_status`` must report it once (BSA_ERR_TIMEOUT), clear it, and the
 context must keep working: a select + forward + backward afterwards still
-matches the fp64 oracle.
+matches the fp64 oracle.  Output and workspace buffers placed between
+sentinel margins must come back with the margins unchanged.
 """
 
 import time
@@ -71,3 +73,51 @@ def test_context_keeps_working_after_timeouts():
     compare_attention(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, lens)
     for g in (dq, dk, dv):
         assert torch.isfinite(g.float()).all()
+
+
+def _canary(shape, dtype, fill, pad=4096):
+    """A view of `shape` in the middle of a buffer whose margins hold `fill`."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * pad,), fill, dtype=dtype, device="cuda")
+    return buf, buf[pad:pad + n].view(shape), pad
+
+
+@pytest.mark.parametrize("name", ["small_gqa", "small_64x64_d128"])
+def test_outputs_and_workspaces_are_written_in_bounds_only(name):
+    """Every output and workspace buffer sits between sentinel margins; after
+    select, forward and backward the margins are unchanged."""
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg, "cpu", pad_fill=0.0)
+    lens = inp["seq_lens"]
+    q, k, v = (inp[x].cuda() for x in ("q", "k", "v"))
+    B, Sq, Hq, d = q.shape
+    Skv, Hkv = k.shape[1], k.shape[2]
+    nQb, nKb = -(-Sq // cfg.block_q), -(-Skv // cfg.block_k)
+    u8 = torch.uint8
+    bufs = []
+
+    def make(shape, dtype, fill):
+        buf, view, pad = _canary(shape, dtype, fill)
+        bufs.append((buf, pad, view.numel(), fill))
+        return view
+
+    idx = make((B, Hq, nQb, nKb), torch.int32, 0x7EADBEEF)
+    cnt = make((B, Hq, nQb), torch.int32, 0x7EADBEEF)
+    sws = make((bsa.bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, cfg.block_q, cfg.block_k),), u8, 0xA5)
+    out = make((B, Sq, Hq, d), torch.bfloat16, 1536.0)
+    lse = make((B, Hq, Sq), torch.float32, 4321.0)
+    fws = make((max(16, bsa.bsa_forward_workspace_size(B, Hq, Sq, Skv, cfg.block_q, cfg.block_k)),), u8, 0xA5)
+    dq = make((B, Sq, Hq, d), torch.bfloat16, 1536.0)
+    dk = make((B, Skv, Hkv, d), torch.bfloat16, 1536.0)
+    dv = make((B, Skv, Hkv, d), torch.bfloat16, 1536.0)
+    bws = make((bsa.bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, cfg.block_q, cfg.block_k),), u8, 0xA5)
+    bsa.bsa_select(q, k, cfg.prefix, lens, cfg.block_q, cfg.block_k, inp["keep_ratio"], indices=idx, counts=cnt,
+                   workspace=sws)
+    bsa.bsa_forward(q, k, v, idx, cnt, cfg.prefix, lens, cfg.block_q, cfg.block_k, out=out, lse=lse, workspace=fws)
+    dout = torch.randn(q.shape, generator=torch.Generator(device="cuda").manual_seed(5), device="cuda").bfloat16()
+    bsa.bsa_backward(q, k, v, out, dout, lse, idx, cnt, cfg.prefix, lens, cfg.block_q, cfg.block_k, dq=dq, dk=dk,
+                     dv=dv, workspace=bws)
+    bsa.bsa_device_status()
+    for buf, pad, n, fill in bufs:
+        assert (buf[:pad] == fill).all() and (buf[pad + n:] == fill).all(), (buf.dtype, n)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(dq.float()).all()
