@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <cmath>
 #include <cstdint>
@@ -201,6 +203,43 @@ __global__ void validate_kernel(const __grid_constant__ ValidateParams p) {
   if (bad) atomicAdd(p.bad, 1);
 }
 
+// BSA_DEBUG validation: malformed index-list rows that reached bsa_forward or
+// bsa_backward, counted on the device and reported by bsa_device_status().
+__device__ int g_debug_bad_rows = 0;
+
+bool debug_validation() {
+  const char* e = std::getenv("BSA_DEBUG");
+  return e && *e && std::strcmp(e, "0") != 0;
+}
+
+// Enqueues validate_kernel (no prefix requirement) over the lists of every
+// request, 64 requests per launch, counting malformed rows into
+// g_debug_bad_rows.  Adds no synchronisation.
+bsa_status debug_validate_lists(const int32_t* indices, const int32_t* counts, int B, int Hq, int Sq, int Skv,
+                                int prefix_len, const int32_t* seq_lens, int block_q, int block_k,
+                                cudaStream_t s) {
+  int32_t* bad = nullptr;
+  bsa_status st = cuda_check(cudaGetSymbolAddress(reinterpret_cast<void**>(&bad), g_debug_bad_rows),
+                             "cudaGetSymbolAddress(BSA_DEBUG counter)");
+  if (st != BSA_OK) return st;
+  const int nQb = (int)cdiv64(Sq, block_q), nKb = (int)cdiv64(Skv, block_k);
+  for (int b0 = 0; b0 < B; b0 += kMaxSelectBatch) {
+    ValidateParams p{};
+    const int Bn = B - b0 < kMaxSelectBatch ? B - b0 : kMaxSelectBatch;
+    const int64_t first_row = (int64_t)b0 * Hq * nQb;
+    p.indices = indices + first_row * nKb;
+    p.counts = counts + first_row;
+    p.B = Bn; p.Hq = Hq; p.nQb = nQb; p.nKb = nKb;
+    p.block_q = block_q; p.block_k = block_k; p.prefix_len = prefix_len; p.require_prefix = 0;
+    for (int i = 0; i < Bn; ++i) p.seq_lens[i] = seq_lens ? seq_lens[b0 + i] : Sq;
+    p.bad = bad;
+    const int64_t rows = (int64_t)Bn * Hq * nQb;
+    validate_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(p);
+    if ((st = cuda_check(cudaGetLastError(), "validate_kernel launch (BSA_DEBUG)")) != BSA_OK) return st;
+  }
+  return BSA_OK;
+}
+
 }  // namespace
 }  // namespace bsa
 
@@ -330,6 +369,10 @@ bsa_status bsa_forward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tenso
   a.seq_lens = seq_lens; a.indices = indices; a.counts = counts;
   a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)q->D);
   a.out = out; a.lse = lse; a.workspace = workspace;
+  if (indices && debug_validation() &&
+      (st = debug_validate_lists(indices, counts, a.B, a.Hq, a.Sq, a.Skv, prefix_len, seq_lens, block_q, block_k,
+                                 reinterpret_cast<cudaStream_t>(stream))) != BSA_OK)
+    return st;
   return launch_forward(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -415,6 +458,10 @@ bsa_status bsa_backward(const bsa_tensor* q, const bsa_tensor* k, const bsa_tens
   a.seq_lens = seq_lens; a.indices = indices; a.counts = counts;
   a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)q->D);
   a.dq = dq; a.dk = dk; a.dv = dv; a.workspace = workspace;
+  if (debug_validation() &&
+      (st = debug_validate_lists(indices, counts, a.B, a.Hq, a.Sq, a.Skv, prefix_len, seq_lens, block_q, block_k,
+                                 reinterpret_cast<cudaStream_t>(stream))) != BSA_OK)
+    return st;
   return launch_backward(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -456,6 +503,21 @@ bsa_status bsa_device_status(bsa_stream_t stream) {
   const unsigned int eb = read_and_clear_bwd_error();
   if (ef == 0xFFFFFFFFu || eb == 0xFFFFFFFFu)
     return set_error(BSA_ERR_CUDA, "bsa_device_status: cannot read the device error word");
+  int bad = 0;
+  const int zero = 0;
+  if ((st = cuda_check(cudaMemcpyFromSymbol(&bad, g_debug_bad_rows, sizeof(bad)), "read BSA_DEBUG counter")) !=
+      BSA_OK)
+    return st;
+  if (bad != 0) {
+    if ((st = cuda_check(cudaMemcpyToSymbol(g_debug_bad_rows, &zero, sizeof(zero)), "clear BSA_DEBUG counter")) !=
+        BSA_OK)
+      return st;
+    return set_error(BSA_ERR_INVALID_INDICES,
+                     std::to_string(bad) + " malformed index-list rows reached bsa_forward / bsa_backward "
+                     "(BSA_DEBUG validation: indices in range of the request's real key blocks and strictly "
+                     "ascending, count 0 for query blocks without real rows)" +
+                         (((ef | eb) & 1u) ? "; a bounded device wait also gave up" : ""));
+  }
   if ((ef | eb) & 1u)
     return set_error(BSA_ERR_TIMEOUT, std::string("a bounded device wait gave up in the ") +
                                           (ef & 1u ? (eb & 1u ? "forward and backward" : "forward") : "backward") +

@@ -41,6 +41,14 @@
  *    thread).  Launch failures return BSA_ERR_CUDA.  Device-side waits are
  *    bounded: a wait that gives up sets a device error word that
  *    bsa_device_status() reports as BSA_ERR_TIMEOUT.
+ *  - Debug validation: when the environment variable BSA_DEBUG is set to a
+ *    non-empty value other than "0" at the time of a bsa_forward (with
+ *    lists) or bsa_backward call, the call first enqueues the checks of
+ *    bsa_validate_indices (without the prefix requirement) on its lists;
+ *    malformed rows are counted on the device and the next
+ *    bsa_device_status() returns BSA_ERR_INVALID_INDICES.  No
+ *    synchronisation is added.  Without it the kernels clamp out-of-range
+ *    entries (they read zeros, fully masked) and never read out of bounds.
  */
 #ifndef BSA_H_
 #define BSA_H_
@@ -279,9 +287,10 @@ BSA_API bsa_status bsa_validate_indices(const int32_t* indices, const int32_t* c
                                 int32_t block_q, int32_t block_k, int32_t require_prefix,
                                 int32_t* bad_rows, bsa_stream_t stream);
 
-/* Synchronises `stream`, then reports and clears the device error word of the
- * current device: BSA_ERR_TIMEOUT if a bounded wait in a kernel gave up since
- * the last call, BSA_ERR_CUDA if the stream reports an error, else BSA_OK. */
+/* Synchronises `stream`, then reports and clears the device error words of
+ * the current device: BSA_ERR_INVALID_INDICES if BSA_DEBUG validation found
+ * malformed lists since the last call, BSA_ERR_TIMEOUT if a bounded wait in a
+ * kernel gave up, BSA_ERR_CUDA if the stream reports an error, else BSA_OK. */
 BSA_API bsa_status bsa_device_status(bsa_stream_t stream);
 
 /* Diagnostics for the timeout path above.  Enqueues on `stream` one

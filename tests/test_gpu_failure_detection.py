@@ -7,7 +7,10 @@ records the timeout in the device error word of its kernel family and exits;
 ``bsa_device_status`` must report it once (BSA_ERR_TIMEOUT), clear it, and the
 context must keep working: a select + forward + backward afterwards still
 matches the fp64 oracle.  Output and workspace buffers placed between
-sentinel margins must come back with the margins unchanged.
+sentinel margins must come back with the margins unchanged.  With BSA_DEBUG
+set, malformed index lists given to the forward or the backward are reported
+by ``bsa_device_status`` (BSA_ERR_INVALID_INDICES); without it they are
+clamped and never read out of bounds.
 """
 
 import time
@@ -121,3 +124,54 @@ def test_outputs_and_workspaces_are_written_in_bounds_only(name):
     for buf, pad, n, fill in bufs:
         assert (buf[:pad] == fill).all() and (buf[pad + n:] == fill).all(), (buf.dtype, n)
     assert torch.isfinite(out.float()).all() and torch.isfinite(dq.float()).all()
+
+
+INVALID_INDICES_STATUS = 5   # BSA_ERR_INVALID_INDICES
+
+
+@pytest.fixture
+def debug_env(monkeypatch):
+    monkeypatch.setenv("BSA_DEBUG", "1")
+
+
+def _lists_with_defects(cfg, idx, cnt):
+    """Two malformed rows: one out of order, one with a block past the request's keys."""
+    bad = idx.clone()
+    c0 = int(cnt[0, 0, 0])
+    assert c0 >= 2
+    bad[0, 0, 0, 0], bad[0, 0, 0, 1] = idx[0, 0, 0, 1], idx[0, 0, 0, 0]
+    c1 = int(cnt[0, 1, 0])
+    bad[0, 1, 0, c1 - 1] = -(-cfg.Skv // cfg.block_k) + 5
+    return bad
+
+
+def test_debug_validation_reports_malformed_lists(debug_env):
+    cfg = CONFIGS["small_gqa"]
+    inp = make_inputs(cfg, "cuda", pad_fill=0.0)
+    q, k, v, lens = inp["q"], inp["k"], inp["v"], inp["seq_lens"]
+    idx, cnt = bsa.bsa_select(q, k, cfg.prefix, lens, cfg.block_q, cfg.block_k, inp["keep_ratio"])
+    out, lse = bsa.bsa_forward(q, k, v, idx, cnt, cfg.prefix, lens, cfg.block_q, cfg.block_k)
+    bsa.bsa_device_status()                               # the selector's lists are well formed
+    bad = _lists_with_defects(cfg, idx, cnt)
+    bsa.bsa_forward(q, k, v, bad, cnt, cfg.prefix, lens, cfg.block_q, cfg.block_k)
+    with pytest.raises(bsa.BsaError) as e:
+        bsa.bsa_device_status()
+    assert e.value.status == INVALID_INDICES_STATUS and str(e.value).startswith("BSA_ERR_INVALID_INDICES: 2 ")
+    bsa.bsa_device_status()                               # reported once
+    dout = torch.randn(q.shape, generator=torch.Generator(device="cuda").manual_seed(1), device="cuda").bfloat16()
+    bsa.bsa_backward(q, k, v, out, dout, lse, bad, cnt, cfg.prefix, lens, cfg.block_q, cfg.block_k)
+    with pytest.raises(bsa.BsaError) as e:
+        bsa.bsa_device_status()
+    assert e.value.status == INVALID_INDICES_STATUS
+
+
+def test_without_debug_malformed_lists_are_clamped_silently(monkeypatch):
+    monkeypatch.delenv("BSA_DEBUG", raising=False)
+    cfg = CONFIGS["small_gqa"]
+    inp = make_inputs(cfg, "cuda", pad_fill=0.0)
+    q, k, v, lens = inp["q"], inp["k"], inp["v"], inp["seq_lens"]
+    idx, cnt = bsa.bsa_select(q, k, cfg.prefix, lens, cfg.block_q, cfg.block_k, inp["keep_ratio"])
+    bad = _lists_with_defects(cfg, idx, cnt)
+    out, _ = bsa.bsa_forward(q, k, v, bad, cnt, cfg.prefix, lens, cfg.block_q, cfg.block_k)
+    bsa.bsa_device_status()                               # no validation: no report, no fault
+    assert torch.isfinite(out.float()).all()
