@@ -198,10 +198,14 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(inp, idx, cnt, n_tiles_sample=400, budget_s=20.0):
+def cpu_baseline(inp, idx, cnt, out=None, lse=None, n_tiles_sample=400, budget_s=20.0):
     """The oracle, as it stands, on a bounded sample of the workload: the full
     selector for one query head and the attention of a few work tiles,
-    extrapolated linearly to the whole workload (units: effective TFLOP/s)."""
+    extrapolated linearly to the whole workload (units: effective TFLOP/s).
+
+    The same oracle results are compared, outside the timed oracle calls, with
+    the GPU's selection of that head and the GPU's output/LSE rows of the
+    sampled tiles (given ``out``/``lse``): the line's ``parity`` object."""
     import numpy as np
     import torch
     from oracle import bsa_oracle as O
@@ -214,10 +218,24 @@ def cpu_baseline(inp, idx, cnt, n_tiles_sample=400, budget_s=20.0):
     q1, k1 = t_host(q[:, :, h0:h0 + 1]), t_host(k[:, :, h0 // G:h0 // G + 1])
     keep = inp["keep_ratio"] if len(inp["keep_ratio"]) == 1 else [inp["keep_ratio"][h0]]
     t0 = time.perf_counter()
-    O.select_blocks(q1, k1, c.prefix, inp["seq_lens"], c.block_q, c.block_k, keep)
+    sel = O.select_blocks(q1, k1, c.prefix, inp["seq_lens"], c.block_q, c.block_k, keep)
     t_sel_head = time.perf_counter() - t0
     cnt_np = cnt.cpu().numpy()
     idx_np = idx.cpu().numpy()
+    # selection of head h0: counts exact; index lists exact except at near-ties
+    gi, gc = idx_np[:, h0:h0 + 1], cnt_np[:, h0:h0 + 1]
+    count_mismatch = int((gc != sel["counts"]).sum())
+    list_mismatch = near = near_differ = 0
+    for b, hh, qb in np.argwhere(sel["counts"] > 0):
+        cc = int(sel["counts"][b, hh, qb])
+        same = gc[b, hh, qb] == cc and (gi[b, hh, qb, :cc] == sel["indices"][b, hh, qb, :cc]).all()
+        if sel["near_tie"][b, hh, qb]:
+            near += 1
+            near_differ += int(not same)
+        else:
+            list_mismatch += int(not same)
+    err_max = err_sum = lse_max = 0.0
+    err_n = 0
     rng = np.random.default_rng(0)
     nz = np.argwhere(cnt_np > 0)
     picks = nz[rng.choice(len(nz), size=min(n_tiles_sample, len(nz)), replace=False)]
@@ -233,9 +251,19 @@ def cpu_baseline(inp, idx, cnt, n_tiles_sample=400, budget_s=20.0):
         qh, kh, vh = cache[(b, h)]
         cc = int(cnt_np[b, h, qb])
         t0 = time.perf_counter()
-        O.attention_tile(qh, kh, vh, 0, 0, int(qb), idx_np[b, h, qb, :cc], c.prefix, inp["seq_lens"][b],
-                         c.block_q, c.block_k, 1.0 / math.sqrt(c.d))
+        o_ref, l_ref, r0 = O.attention_tile(qh, kh, vh, 0, 0, int(qb), idx_np[b, h, qb, :cc], c.prefix,
+                                            inp["seq_lens"][b], c.block_q, c.block_k, 1.0 / math.sqrt(c.d))
         t_att += time.perf_counter() - t0
+        if out is not None:
+            nr = max(0, min(len(o_ref), inp["seq_lens"][b] - r0))       # real rows of the tile
+            if nr > 0:
+                og = out[b, r0:r0 + nr, h].float().cpu().numpy().astype(np.float64)
+                e = np.abs(og - o_ref[:nr])
+                err_max, err_sum, err_n = max(err_max, float(e.max())), err_sum + float(e.sum()), err_n + e.size
+                lg = lse[b, h, r0:r0 + nr].cpu().numpy().astype(np.float64)
+                fin = np.isfinite(l_ref[:nr])
+                if fin.any():
+                    lse_max = max(lse_max, float(np.abs(lg[fin] - l_ref[:nr][fin]).max()))
         sampled_pairs += cc
         done += 1
         if t_att + t_sel_head > budget_s:
@@ -253,6 +281,17 @@ def cpu_baseline(inp, idx, cnt, n_tiles_sample=400, budget_s=20.0):
                    f"extrapolated linearly to all heads and all {int(total_pairs)} selected blocks "
                    f"(est. {est_time:.0f} s per step)"),
         "est_seconds_per_step": est_time,
+        "parity": {
+            "selection": {"head": h0, "rows": int(sel["counts"].size), "count_mismatches": count_mismatch,
+                          "list_mismatches_outside_near_ties": list_mismatch, "near_tie_rows": near,
+                          "near_tie_rows_differing": near_differ},
+            "attention": None if out is None or err_n == 0 else {
+                "tiles": done, "elements": err_n, "out_max_abs": err_max, "out_mean_abs": err_sum / err_n,
+                "lse_max_abs": lse_max},
+            "tolerance": {"out_max_abs": 2e-2, "out_mean_abs": 2e-3, "lse_max_abs": 1e-2,
+                          "selection": "bit-exact except near-ties (k-th and (k+1)-th scores within 1e-4 relative)"},
+            "reference": "the fp64 oracle on the same bf16 inputs and the GPU's own lists",
+        },
     }
 
 
@@ -651,7 +690,8 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, idx, cnt)
+        cpu = cpu_baseline(inp, idx, cnt, out, lse)
+    parity = cpu.pop("parity") if cpu else None
 
     if rank == 0:
         line = {
@@ -679,6 +719,7 @@ def main():
             **({"backward": bwd} if bwd is not None else {}),
             **({"extras": extras} if extras is not None else {}),
             "cpu_baseline": cpu,
+            **({"parity": parity} if parity is not None else {}),
             "gpu_launches": launches_per_step * args.steps,
         }
         print(json.dumps(line), flush=True)
