@@ -1,0 +1,89 @@
+"""Host arithmetic of bench.py (CPU): the FLOP and byte counts that the
+reported TFLOP/s and roofline fractions divide by, the schedules' call counts,
+the replica aggregation and the traffic lookup's source check."""
+
+import os
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from bsa_inputs import CONFIGS, make_inputs  # noqa: E402
+from oracle import bsa_oracle as O  # noqa: E402
+
+
+def small_lists(name):
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg, "cpu", pad_fill=0.0)
+    sel = O.select_blocks(inp["q"].float().numpy(), inp["k"].float().numpy(), cfg.prefix, inp["seq_lens"],
+                          cfg.block_q, cfg.block_k, inp["keep_ratio"])
+    return cfg, inp["seq_lens"], sel["indices"], sel["counts"]
+
+
+@pytest.mark.parametrize("name", ["small_gqa", "small_mqa_d64", "tiny"])
+def test_exact_pair_flops_count_real_rows_and_keys(name):
+    """4 d per (real query row, real listed key): counted key by key here."""
+    cfg, lens, idx, cnt = small_lists(name)
+    pairs = 0
+    for b, L in enumerate(lens):
+        real_keys = np.arange(cfg.prefix + L)
+        for h in range(cfg.Hq):
+            for qb in range(cnt.shape[2]):
+                rows = len(range(qb * cfg.block_q, min((qb + 1) * cfg.block_q, L)))
+                listed = set()
+                for kb in idx[b, h, qb, :cnt[b, h, qb]]:
+                    listed.update(range(kb * cfg.block_k, (kb + 1) * cfg.block_k))
+                pairs += rows * len(listed.intersection(real_keys.tolist()))
+    got = bench.valid_pair_flops(cnt, idx, lens, cfg.prefix, cfg.d, cfg.block_q, cfg.block_k)
+    assert got == 4.0 * cfg.d * pairs
+    # the tile-granular count is an upper bound that includes padded rows and keys
+    assert bench.tile_flops(cnt, cfg.d, cfg.block_q, cfg.block_k) >= got
+
+
+def test_tile_flops_and_algorithmic_bytes_of_the_720p_workload():
+    """720p, keep 25 %: 21,600 work tiles x 346 listed blocks; every byte counted once."""
+    cfg = CONFIGS["720p_75"]
+    nQb = -(-cfg.Sq // cfg.block_q)
+    assert (nQb, cfg.Hq) == (675, 32)
+    counts = np.full((1, cfg.Hq, nQb), 346)
+    assert bench.tile_flops(counts, cfg.d, cfg.block_q, cfg.block_k) == 4 * 128 * 256 * 128 * 21_600 * 346
+    q_o = 2 * 172_800 * 32 * 128 * 2               # Q read, O written (bf16)
+    kv = 2 * 173_824 * 8 * 128 * 2                 # K and V read (bf16)
+    lse = 4 * 32 * 172_800                         # fp32 LSE written
+    lists = 4 * 21_600 * 346                       # int32 list entries read
+    assert bench.algorithmic_bytes(cfg, counts) == q_o + kv + lse + lists == 3_595_151_104
+
+
+def test_replicas_aggregate_the_slowest_rank():
+    assert bench.whole_job_tflops(1e12, 1, 1000.0) == pytest.approx(1.0)
+    assert bench.whole_job_tflops(125.0e12, 4, 100.0) == pytest.approx(5000.0)
+
+
+@pytest.mark.parametrize("name,arm,dense,sparse", [
+    ("cosmos3", "dense", 35 * 36, 0),
+    ("cosmos3", "mixed", 10 * 36 + 25 * 8, 25 * 28),      # 10 dense steps, then 28 of 36 layers sparse
+    ("cosmos3", "all_sparse", 0, 35 * 36),
+    ("h3", "dense", 50 * 48, 0),
+    ("h3", "mixed", 20 * 48, 30 * 48),                    # the first 20 of 50 iterations dense
+])
+def test_schedule_arms_call_counts(name, arm, dense, sparse):
+    sch = bench.SCHEDULES[name]
+    is_dense = sch["arms"][arm]
+    calls = [is_dense(s, l) for s in range(sch["steps"]) for l in range(sch["layers"])]
+    assert sum(calls) == dense and len(calls) - sum(calls) == sparse
+
+
+def test_traffic_is_reported_only_for_the_captured_sources(monkeypatch):
+    cfg = CONFIGS["720p_75"]
+    counts = np.zeros((1, 1, 1))
+    monkeypatch.setitem(bench.FMHA_TRAFFIC, "sha", bench.fmha_source_sha())
+    val, src = bench.fmha_traffic(cfg, counts)
+    assert val == float(bench.FMHA_TRAFFIC["720p_75"]) and "ncu capture" in src
+    assert bench.fmha_traffic(CONFIGS["tiny"], counts)[0] is None          # never captured
+    monkeypatch.setitem(bench.FMHA_TRAFFIC, "sha", "0" * 16)
+    val, src = bench.fmha_traffic(cfg, counts)
+    assert val is None and "changed" in src
