@@ -212,9 +212,10 @@ __global__ void __launch_bounds__(kPoolCols* kPoolGroups)
 // mean streams from L2 as float4s; the query means sit transposed in shared
 // memory and are read as broadcast float4s), so each key mean is read once
 // per CTA and each multiply-add needs a fraction of a shared-memory load.
-// Selection: one warp per row; the kh-th largest score key is found bit by
-// bit (32 counting passes), then one pass in ascending block order writes
-// the blocks above it plus the lowest-index blocks equal to it.
+// Selection: one warp per row; the kh-th largest order-preserving score key
+// is found by a radix select (4 passes of 8 bits over a per-warp 256-bin
+// histogram), then one pass in ascending block order writes the blocks above
+// it plus the lowest-index blocks equal to it.
 
 constexpr int kRows = 16;
 constexpr int kTopkThreads = 256;
