@@ -146,6 +146,38 @@ def whole_job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> f
     return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
 
 
+def gpu_local_cpus():
+    """(CPUs on the GPU's NUMA node that this process may use, that node) from
+    sysfs, or (None, None) where the platform does not say."""
+    import torch
+    try:
+        pr = torch.cuda.get_device_properties(torch.cuda.current_device())
+        dev = "/sys/bus/pci/devices/%04x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        cpus = set()
+        for part in open(dev + "/local_cpulist").read().strip().split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return (cpus or None), int(open(dev + "/numa_node").read().strip())
+    except Exception:
+        return None, None
+
+
+def pinned_like(t, local_cpus):
+    """A pinned host buffer of t's shape and dtype, allocated while this thread
+    runs on the GPU's local CPUs (so its pages sit on the GPU's NUMA node);
+    the thread's affinity is restored afterwards."""
+    import torch
+    prev = os.sched_getaffinity(0)
+    if local_cpus:
+        os.sched_setaffinity(0, local_cpus)
+    try:
+        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    finally:
+        if local_cpus:
+            os.sched_setaffinity(0, prev)
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled during the timed region."""
 
@@ -529,10 +561,13 @@ def main():
     # the first H2D to the last D2H.
     e2e = None
     if not args.no_e2e:
-        hq, hk_, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        local_cpus, gpu_node = gpu_local_cpus()
+        hq, hk_, hv = (pinned_like(t, local_cpus) for t in (q, k, v))
+        for h_, t in ((hq, q), (hk_, k), (hv, v)):
+            h_.copy_(t)
         n_e2e = max(3, min(args.steps, 10))
-        houts = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
-        hlses = [torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True) for _ in range(2)]
+        houts = [pinned_like(out, local_cpus) for _ in range(2)]
+        hlses = [pinned_like(lse, local_cpus) for _ in range(2)]
         bufs = [dict(q=q, k=k, v=v, out=out, lse=lse, idx=idx, cnt=cnt)]
         bufs.append(dict(q=torch.empty_like(q), k=torch.empty_like(k), v=torch.empty_like(v),
                          out=torch.empty_like(out), lse=torch.empty_like(lse), idx=torch.empty_like(idx),
@@ -542,10 +577,12 @@ def main():
         h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
 
         def run_e2e(n):
-            loaded = [torch.cuda.Event() for _ in range(n)]
+            loaded = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
             computed = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
             began = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-            drained = [torch.cuda.Event() for _ in range(n)]
+            drained = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+            h2d_go = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+            d2h_go = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
             start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             start.record(h2d_stream)
             for i in range(n + 1):
@@ -553,6 +590,7 @@ def main():
                     bf = bufs[i % 2]
                     if i >= 2:
                         h2d_stream.wait_event(computed[i - 2])
+                    h2d_go[i].record(h2d_stream)
                     with torch.cuda.stream(h2d_stream):
                         bf["q"].copy_(hq, non_blocking=True)
                         bf["k"].copy_(hk_, non_blocking=True)
@@ -570,6 +608,7 @@ def main():
                 if i >= 1:                                  # D2H of step i - 1
                     j = i - 1
                     d2h_stream.wait_event(computed[j])
+                    d2h_go[j].record(d2h_stream)
                     with torch.cuda.stream(d2h_stream):
                         houts[j % 2].copy_(bufs[j % 2]["out"], non_blocking=True)
                         hlses[j % 2].copy_(bufs[j % 2]["lse"], non_blocking=True)
@@ -578,11 +617,13 @@ def main():
             end.record(d2h_stream)
             torch.cuda.synchronize()
             compute = sum(b.elapsed_time(c) for b, c in zip(began, computed)) / n
-            return start.elapsed_time(end) / n, compute
+            h2d_ms = sorted(a.elapsed_time(b) for a, b in zip(h2d_go, loaded))[n // 2]
+            d2h_ms = sorted(a.elapsed_time(b) for a, b in zip(d2h_go, drained))[n // 2]
+            return start.elapsed_time(end) / n, compute, h2d_ms, d2h_ms
 
         run_e2e(2)
         bsa.bsa_device_status(stream)
-        e_ms, e_compute_ms = run_e2e(n_e2e)
+        e_ms, e_compute_ms, h2d_ms, d2h_ms = run_e2e(n_e2e)
         e_ms = max_over_ranks(e_ms, device="cuda")
         bsa.bsa_device_status(stream)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk_, hv))
@@ -590,6 +631,10 @@ def main():
         e2e = {"value": whole_job_tflops(flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "compute_ms_per_step_during_copies": e_compute_ms,
+               "copy_gbs_in_loop": {"h2d": h2d / (h2d_ms * 1e-3) / 1e9, "d2h": d2h / (d2h_ms * 1e-3) / 1e9,
+                                    "note": "median per-step copy time inside the timed loop"},
+               "host_buffers": {"pinned": True, "gpu_numa_node": gpu_node,
+                                "allocated_on_gpu_local_cpus": bool(local_cpus)},
                "pipelining": "double-buffered device inputs/outputs; H2D and D2H on their own streams "
                              "overlap the neighbouring steps' compute"}
         del bufs[1], ws2[1], fws2[1]
