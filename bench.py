@@ -316,10 +316,12 @@ def cpu_baseline(inp, idx, cnt, out=None, lse=None, n_tiles_sample=400, budget_s
         "parity": {
             "selection": {"head": h0, "rows": int(sel["counts"].size), "count_mismatches": count_mismatch,
                           "list_mismatches_outside_near_ties": list_mismatch, "near_tie_rows": near,
-                          "near_tie_rows_differing": near_differ},
+                          "near_tie_rows_differing": near_differ,
+                          "ok": count_mismatch == 0 and list_mismatch == 0},
             "attention": None if out is None or err_n == 0 else {
                 "tiles": done, "elements": err_n, "out_max_abs": err_max, "out_mean_abs": err_sum / err_n,
-                "lse_max_abs": lse_max},
+                "lse_max_abs": lse_max,
+                "ok": err_max <= 2e-2 and err_sum / err_n <= 2e-3 and lse_max <= 1e-2},
             "tolerance": {"out_max_abs": 2e-2, "out_mean_abs": 2e-3, "lse_max_abs": 1e-2,
                           "selection": "bit-exact except near-ties (k-th and (k+1)-th scores within 1e-4 relative)"},
             "reference": "the fp64 oracle on the same bf16 inputs and the GPU's own lists",
