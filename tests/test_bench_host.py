@@ -87,3 +87,29 @@ def test_traffic_is_reported_only_for_the_captured_sources(monkeypatch):
     monkeypatch.setitem(bench.FMHA_TRAFFIC, "sha", "0" * 16)
     val, src = bench.fmha_traffic(cfg, counts)
     assert val is None and "changed" in src
+
+
+def test_bench_parity_verdicts_catch_planted_defects():
+    """The CPU-baseline leg's comparison: the oracle's own bf16-stored results
+    pass; a swapped list entry and a shifted output tile each fail."""
+    import torch
+    cfg = CONFIGS["small_gqa"]
+    inp = make_inputs(cfg, "cpu", pad_fill=0.0)
+    q, k, v = (inp[x].float().numpy().astype(np.float64) for x in ("q", "k", "v"))
+    sel = O.select_blocks(inp["q"].float().numpy(), inp["k"].float().numpy(), cfg.prefix, inp["seq_lens"],
+                          cfg.block_q, cfg.block_k, inp["keep_ratio"])
+    idx = torch.from_numpy(sel["indices"].astype(np.int32))
+    cnt = torch.from_numpy(sel["counts"].astype(np.int32))
+    o, l = O.attention(q, k, v, sel["indices"], sel["counts"], cfg.prefix, inp["seq_lens"], cfg.block_q,
+                       cfg.block_k)
+    out = torch.from_numpy(np.nan_to_num(o)).bfloat16()
+    lse = torch.from_numpy(np.where(np.isnan(l), -np.inf, l)).float()
+    good = bench.cpu_baseline(inp, idx, cnt, out, lse, n_tiles_sample=64, budget_s=10)["parity"]
+    assert good["selection"]["ok"] and good["attention"]["ok"], good
+    bad_idx = idx.clone()
+    bad_idx[0, 0, 1, 2], bad_idx[0, 0, 1, 3] = idx[0, 0, 1, 3], idx[0, 0, 1, 2]
+    bad_out = out.clone()
+    bad_out[0, :10, 0, :] += 0.5
+    bad = bench.cpu_baseline(inp, bad_idx, cnt, bad_out, lse, n_tiles_sample=64, budget_s=10)["parity"]
+    assert not bad["selection"]["ok"] and bad["selection"]["list_mismatches_outside_near_ties"] == 1
+    assert not bad["attention"]["ok"]
