@@ -1,6 +1,7 @@
-"""Host arithmetic of bench.py (CPU): the FLOP and byte counts that the
-reported TFLOP/s and roofline fractions divide by, the schedules' call counts,
-the replica aggregation and the traffic lookup's source check."""
+"""Host logic of bench.py (CPU): the FLOP and byte counts that the reported
+TFLOP/s and roofline fractions divide by, the schedules' call counts, the
+replica aggregation, the traffic lookup's source check and the verdicts of
+the line's parity comparison."""
 
 import os
 import sys
