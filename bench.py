@@ -621,11 +621,16 @@ def main():
             compute = sum(b.elapsed_time(c) for b, c in zip(began, computed)) / n
             h2d_ms = sorted(a.elapsed_time(b) for a, b in zip(h2d_go, loaded))[n // 2]
             d2h_ms = sorted(a.elapsed_time(b) for a, b in zip(d2h_go, drained))[n // 2]
-            return start.elapsed_time(end) / n, compute, h2d_ms, d2h_ms
+            # where the rest of the region goes: before the first compute, between
+            # consecutive computes (waits on copies), after the last compute
+            timeline = {"fill_ms": start.elapsed_time(began[0]),
+                        "gap_ms_between_computes": [computed[i - 1].elapsed_time(began[i]) for i in range(1, n)],
+                        "drain_ms": computed[n - 1].elapsed_time(end)}
+            return start.elapsed_time(end) / n, compute, h2d_ms, d2h_ms, timeline
 
         run_e2e(2)
         bsa.bsa_device_status(stream)
-        e_ms, e_compute_ms, h2d_ms, d2h_ms = run_e2e(n_e2e)
+        e_ms, e_compute_ms, h2d_ms, d2h_ms, e_timeline = run_e2e(n_e2e)
         e_ms = max_over_ranks(e_ms, device="cuda")
         bsa.bsa_device_status(stream)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk_, hv))
@@ -635,6 +640,7 @@ def main():
                "compute_ms_per_step_during_copies": e_compute_ms,
                "copy_gbs_in_loop": {"h2d": h2d / (h2d_ms * 1e-3) / 1e9, "d2h": d2h / (d2h_ms * 1e-3) / 1e9,
                                     "note": "median per-step copy time inside the timed loop"},
+               "timeline": e_timeline,
                "host_buffers": {"pinned": True, "gpu_numa_node": gpu_node,
                                 "allocated_on_gpu_local_cpus": bool(local_cpus)},
                "pipelining": "double-buffered device inputs/outputs; H2D and D2H on their own streams "
