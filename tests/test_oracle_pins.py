@@ -608,3 +608,46 @@ def test_backward_finite_difference_tiny():
             args[name] = xm
             lm = (w * O.attention(args["q"], args["k"], args["v"], idx, cnt, P, [Sq], bq, bk)[0]).sum()
             assert abs((lp - lm) / (2 * eps) - g[i]) < 1e-6, (name, i)
+
+
+# ------------------------------------------- planted mistakes, backward ---
+# Each mutation is a plausible slip in the oracle's backward (a sign, a
+# dropped scale, a wrong operand or head mapping, a transposed product); the
+# mutant is built from the function's own source and must fail the torch
+# autograd pin above.
+BACKWARD_MUTATIONS = [
+    ("ds = p_ * (gg @ vv.T - D)", "ds = p_ * (gg @ vv.T + D)"),
+    ("dq[b, r0:r1, h] += scale * ds @ kk", "dq[b, r0:r1, h] += ds @ kk"),
+    ("dk[b, pos, hk] += scale * ds.T @ qq", "dk[b, pos, hk] += ds.T @ qq"),
+    ("dv[b, pos, hk] += p_.T @ gg", "dv[b, pos, hk] += p_.T @ oo"),
+    ("dk[b, pos, hk] += scale * ds.T @ qq", "dk[b, pos, hk] += scale * ds.T @ gg"),
+    ("hk = h // G", "hk = h % Hkv"),
+    ("p_ = np.exp((qq @ kk.T) * scale - lse[b, h, r0:r1, None])", "p_ = np.exp((qq @ kk.T) - lse[b, h, r0:r1, None])"),
+    ("dq[b, r0:r1, h] += scale * ds @ kk", "dq[b, r0:r1, h] += scale * (p_ * (gg @ vv.T)) @ kk"),  # D dropped in dQ
+]
+
+
+@pytest.mark.parametrize("old,new", BACKWARD_MUTATIONS)
+def test_planted_backward_mistake_is_caught(old, new):
+    import inspect
+    src = inspect.getsource(O.attention_backward)
+    assert old in src, old
+    ns = dict(vars(O))
+    exec(compile(src.replace(old, new), "<mutant>", "exec"), ns)
+    mutant = ns["attention_backward"]
+    inp, q, k, v = _tiny("small_gqa")
+    c = inp["cfg"]
+    q, k, v = (np.nan_to_num(x) for x in (q, k, v))
+    sel = O.select_blocks(q, k, c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    out, lse = O.attention(q, k, v, sel["indices"], sel["counts"], c.prefix, inp["seq_lens"], c.block_q, c.block_k)
+    dout = np.random.default_rng(23).standard_normal(out.shape)
+    for b, L in enumerate(inp["seq_lens"]):
+        dout[b, L:] = 0.0
+    grads = mutant(q, k, v, out, dout, lse, sel["indices"], sel["counts"], c.prefix, inp["seq_lens"], c.block_q,
+                   c.block_k)
+    qt, kt, vt = (torch.from_numpy(x).requires_grad_(True) for x in (q, k, v))
+    ot = _torch_selected_attention(qt, kt, vt, sel["indices"], sel["counts"], c.prefix, inp["seq_lens"],
+                                   c.block_q, c.block_k, 1 / math.sqrt(c.d))
+    ot.backward(torch.from_numpy(dout))
+    worst = max(np.abs(g - t.grad.numpy()).max() for g, t in zip(grads, (qt, kt, vt)))
+    assert worst > 1e-6, (new, worst)
