@@ -651,3 +651,97 @@ def test_planted_backward_mistake_is_caught(old, new):
     ot.backward(torch.from_numpy(dout))
     worst = max(np.abs(g - t.grad.numpy()).max() for g, t in zip(grads, (qt, kt, vt)))
     assert worst > 1e-6, (new, worst)
+
+
+# -------------------------------------- planted mistakes, forward and selector ---
+# Source mutations of the oracle's building blocks, each paired with the
+# independent check that must expose it (the check passes on the unmodified
+# oracle: see test_forward_mutation_checks_pass_on_the_oracle).
+
+def _check_golden_attention():
+    e = json.load(open(GOLDEN))["attention"]
+    out, lse = O.attention_rows(np.array([e["q"]]), np.array(e["keys"]), np.array(e["vals"]), e["scale"])
+    return not (np.allclose(out[0], e["expect_out"], rtol=1e-14, atol=0)
+                and abs(lse[0] - e["expect_lse"]) <= 1e-14 * abs(e["expect_lse"]))
+
+
+def _check_dense_sdpa_with_nan_padding():
+    inp, q, k, v = _tiny("small_gqa")
+    c = inp["cfg"]
+    idx, cnt = O.dense_indices(c.prefix, inp["seq_lens"], c.Sq, c.Skv, c.block_q, c.block_k, c.Hq)
+    out, lse = O.attention(q, k, v, idx, cnt, c.prefix, inp["seq_lens"], c.block_q, c.block_k)
+    ro, rl = _sdpa_dense(q, k, v, c.prefix, inp["seq_lens"], 1 / math.sqrt(c.d))
+    real = ~np.isnan(ro)
+    for b, L in enumerate(inp["seq_lens"]):
+        real[b, L:] = False
+    return not (np.allclose(out[real], ro[real], rtol=0, atol=1e-12))
+
+
+def _check_pool_ramp_with_padding():
+    S, H, d, blk, nv = 11, 2, 3, 4, 9
+    x = np.repeat(np.arange(S, dtype=np.float64)[:, None, None], H, 1).repeat(d, 2)
+    x[nv:] = np.nan
+    m = O.pool_means(x, nv, blk)
+    return not (np.array_equal(m[:, 0], np.full((H, d), 1.5)) and np.array_equal(m[:, 2], np.full((H, d), 8.0)))
+
+
+def _check_keep_count_closed_form():
+    return O.keep_count(np.float32(0.25), 378) != 95 or O.keep_count(np.float32(0.25), 1350) != 338
+
+
+def _check_lists_ascending_and_golden():
+    g = json.load(open(GOLDEN))["selection"]
+    sel = O.select_blocks(np.array(g["q"], float), np.array(g["k"], float), g["prefix_len"], g["seq_lens"],
+                          g["block_q"], g["block_k"], [np.float32(x) for x in g["keep_ratio"]])
+    bad = not np.array_equal(sel["indices"][..., :3], g["expect_indices"])
+    rng = np.random.default_rng(5)
+    scores = rng.permutation(40).astype(float)
+    got = O.topk_lowest_index(scores, 10)
+    return bad or not np.array_equal(got, np.sort(np.argsort(-scores)[:10]))
+
+
+def _check_gqa_selection_equals_repeated_kv():
+    inp, q, k, v = _tiny("small_gqa")
+    c = inp["cfg"]
+    G = c.Hq // c.Hkv
+    a = O.select_blocks(q, k, c.prefix, inp["seq_lens"], c.block_q, c.block_k, inp["keep_ratio"])
+    bsel = O.select_blocks(q, np.repeat(k, G, axis=2), c.prefix, inp["seq_lens"], c.block_q, c.block_k,
+                           inp["keep_ratio"])
+    return not (np.array_equal(a["counts"], bsel["counts"]) and np.array_equal(a["indices"], bsel["indices"]))
+
+
+FORWARD_MUTATIONS = [
+    ("attention_rows", "lse = (m + np.log(l))[:, 0]", "lse = (m + np.log2(l))[:, 0]", _check_golden_attention),
+    ("attention_rows", "out = (p @ vals) / l", "out = (p @ vals)", _check_golden_attention),
+    ("attention_rows", "p = np.exp(z - m)", "p = np.exp(z)", _check_golden_attention),
+    ("tile_keys", "r1 = min((int(kb) + 1) * block_k, n_valid_keys)", "r1 = (int(kb) + 1) * block_k",
+     _check_dense_sdpa_with_nan_padding),
+    ("pool_means", "r1 = min((j + 1) * block, n_valid, S)", "r1 = min((j + 1) * block, S)",
+     _check_pool_ramp_with_padding),
+    ("keep_count", "math.ceil(r * float(n_candidates))", "math.floor(r * float(n_candidates))",
+     _check_keep_count_closed_form),
+    ("topk_lowest_index", "return np.sort(order[:k]).astype(np.int64)", "return order[:k].astype(np.int64)",
+     _check_lists_ascending_and_golden),
+    ("select_blocks", "hk = h // G ", "hk = h % Hkv ", _check_gqa_selection_equals_repeated_kv),
+]
+
+
+def test_forward_mutation_checks_pass_on_the_oracle():
+    for _, _, _, check in FORWARD_MUTATIONS:
+        assert not check(), check.__name__
+
+
+@pytest.mark.parametrize("fname,old,new,check", FORWARD_MUTATIONS,
+                         ids=[f"{m[0]}:{i}" for i, m in enumerate(FORWARD_MUTATIONS)])
+def test_planted_forward_mistake_is_caught(monkeypatch, fname, old, new, check):
+    import inspect
+    src = inspect.getsource(getattr(O, fname))
+    assert old in src, old
+    ns = dict(vars(O))
+    exec(compile(src.replace(old, new), "<mutant>", "exec"), ns)
+    monkeypatch.setattr(O, fname, ns[fname])
+    try:
+        caught = check()
+    except (IndexError, ValueError, FloatingPointError):
+        caught = True                       # the pin's run breaks down: caught as well
+    assert caught, (fname, new)
