@@ -33,8 +33,11 @@
  *    A key block holding any prefix position is a prefix block:
  *    npb = ceil(prefix_len/block_k).
  *  - Supported: d in {64, 128}; block_q in {64, 128, 256} with block_k in
- *    {64, 128} (all six pairs); Hq % Hkv == 0; bf16 only.  Anything else
- *    returns BSA_ERR_UNSUPPORTED (no fallback path exists).
+ *    {64, 128} (all six pairs); Hq % Hkv == 0; Hq <= 256; bf16 only.  Batch:
+ *    B <= 64 for the selector calls, bsa_backward and bsa_validate_indices;
+ *    bsa_forward and bsa_forward_causal take larger batches (they launch 8
+ *    requests at a time).  Anything else returns BSA_ERR_UNSUPPORTED (no
+ *    fallback path exists).
  *  - Errors: every call validates its arguments on the host before launching
  *    and returns a status; bsa_get_last_error() gives a message naming the
  *    argument and value (thread-local, valid until the next call on the
