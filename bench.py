@@ -102,7 +102,7 @@ def fmha_traffic(cfg, counts):
         return None, "forward kernel changed since the last ncu capture"
     if cfg.name in FMHA_TRAFFIC:
         return float(FMHA_TRAFFIC[cfg.name]), f"ncu capture of {cfg.name}"
-    return None, f"no ncu capture of {cfg.name} for this build"
+    return None, f"no ncu capture of {cfg.name} for these forward sources"
 
 
 def tile_flops(counts, d, bq, bk) -> float:
