@@ -306,3 +306,21 @@ def test_wait_probe_rejects_bad_arguments(lib):
         st = lib.bsa_debug_wait_probe(fam, lim, None)
         assert st == 1, (fam, lim, st)                      # BSA_ERR_INVALID_ARG, nothing launched
         assert b"bsa_debug_wait_probe" in lib.bsa_get_last_error()
+
+
+def test_product_package_never_touches_the_oracle():
+    """The library and its binding import nothing from oracle/ (only the tests,
+    the smoke check and the bench's CPU-baseline arm may)."""
+    import subprocess
+    import sys
+    code = ("import sys, block_sparse_attention_bsa_gb300 as b; b.build(); "
+            "from block_sparse_attention_bsa_gb300 import _lib; _lib.load(); "
+            "print(any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules))")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, timeout=600)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip().splitlines()[-1] == "False"
+    pkg = os.path.join(ROOT, "block_sparse_attention_bsa_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                assert "oracle" not in open(os.path.join(dirpath, f)).read(), f
