@@ -53,6 +53,8 @@ def parse():
                          "understanding-stream pass, each against its roofline")
     ap.add_argument("--schedule", choices=["cosmos3", "h3"], default=None,
                     help="time the dense pass and the sparse step and report a dense->sparse schedule")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the dense pass and the other workloads (480p, 1280x736) after the timed step")
     return ap.parse_args()
 
 
@@ -66,15 +68,15 @@ def peaks():
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one forward
-# launch, from an ncu capture of the build whose FMHA sources hash to `sha`.
-# When the sources change the figure no longer applies and traffic is null.
+# launch, from a 1-pass ncu capture of the build whose FMHA sources hash to
+# `sha`.  When the sources change the figure no longer applies and traffic is
+# null.
 FMHA_TRAFFIC = {
     "sha": "23fc1a5077027a58",
-    # 1-pass captures (dram__bytes_read.sum + dram__bytes_write.sum of one launch)
-    "720p_75": 13786140928 + 1723019008,          # profiles/launches_720p_75.md
-    "480p_75": 503945984 + 268207872,             # profiles/fmha_fwd_480p_75.md
-    "480p_dense": 510417920 + 270237184,          # profiles/fmha_fwd_480p_dense.md
-    "1280x736_ragged": 23890579712 + 2600347136,  # profiles/fmha_traffic_1280x736_ragged.md
+    "720p_75": 13786140928 + 1723019008,
+    "480p_75": 503945984 + 268207872,
+    "480p_dense": 510417920 + 270237184,
+    "1280x736_ragged": 23890579712 + 2600347136,
 }
 
 
@@ -103,6 +105,26 @@ def fmha_traffic(cfg, counts):
     if cfg.name in FMHA_TRAFFIC:
         return float(FMHA_TRAFFIC[cfg.name]), f"ncu capture of {cfg.name}"
     return None, f"no ncu capture of {cfg.name} for these forward sources"
+
+
+def dense_tiles(lens, prefix, Hq, bq, bk) -> int:
+    """(work tile, key block) pairs of the dense pass: every real query block
+    of every head against every key block holding a real key."""
+    return sum(-(-(prefix + L) // bk) * -(-L // bq) for L in lens) * Hq
+
+
+def schedule_arms(name: str, t_dense_ms: float, t_sparse_ms: float) -> dict:
+    """Attention time of one generation under a schedule of SCHEDULES, from
+    the time of one dense call and one sparse call (select + forward)."""
+    sch = SCHEDULES[name]
+    arms = {}
+    for arm, is_dense in sch["arms"].items():
+        n_d = sum(1 for st in range(sch["steps"]) for l in range(sch["layers"]) if is_dense(st, l))
+        n_s = sch["steps"] * sch["layers"] - n_d
+        arms[arm] = dict(dense_calls=n_d, sparse_calls=n_s, attention_s=(n_d * t_dense_ms + n_s * t_sparse_ms) / 1e3)
+    for arm in arms:
+        arms[arm]["speedup_vs_dense"] = arms["dense"]["attention_s"] / arms[arm]["attention_s"]
+    return {"arms": arms, "pages_end_to_end_speedups": sch["published"]}
 
 
 def tile_flops(counts, d, bq, bk) -> float:
@@ -230,7 +252,46 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(inp, idx, cnt, out=None, lse=None, n_tiles_sample=400, budget_s=20.0):
+def _tiny_oracle_run(reps: int = 5) -> None:
+    """Child-process body of tiny_oracle_timing: the oracle's full selector and
+    attention on the tiny workload, `reps` times; prints the median seconds."""
+    import numpy as np
+    from bsa_inputs import CONFIGS, make_inputs
+    from oracle import bsa_oracle as O
+    cfg = CONFIGS["tiny"]
+    inp = make_inputs(cfg, "cpu", pad_fill=0.0)
+    q, k, v = (inp[x].float().numpy().astype(np.float64) for x in ("q", "k", "v"))
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        sel = O.select_blocks(q, k, cfg.prefix, inp["seq_lens"], cfg.block_q, cfg.block_k, inp["keep_ratio"])
+        O.attention(q, k, v, sel["indices"], sel["counts"], cfg.prefix, inp["seq_lens"], cfg.block_q, cfg.block_k)
+        times.append(time.perf_counter() - t0)
+    print(json.dumps({"seconds": sorted(times)[reps // 2], "flops": tile_flops(sel["counts"], cfg.d, cfg.block_q,
+                                                                                cfg.block_k)}))
+
+
+def tiny_oracle_timing():
+    """The tiny workload timed in full through the oracle, in fresh processes
+    whose BLAS / OpenMP thread pools are set to one thread and to every host
+    core (environment variables read when numpy loads)."""
+    res = {}
+    for label, n in (("one_core", 1), ("all_cores", os.cpu_count() or 1)):
+        env = dict(os.environ)
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[var] = str(n)
+        try:
+            r = subprocess.run([sys.executable, "-c", "import bench; bench._tiny_oracle_run()"], cwd=ROOT, env=env,
+                               capture_output=True, text=True, timeout=300)
+            d = json.loads(r.stdout.strip().splitlines()[-1])
+            res[label] = {"threads": n, "seconds": d["seconds"], "tflops": d["flops"] / d["seconds"] / 1e12}
+        except Exception as e:          # the timing is informative only
+            res[label] = {"threads": n, "error": repr(e)[:200]}
+    res["note"] = "tiny workload (B1 Hq4 Hkv2 d64, 256 + 1,024 tokens, 64x64 blocks) in full, median of 5"
+    return res
+
+
+def cpu_baseline(inp, idx, cnt, out=None, lse=None, n_tiles_sample=400, budget_s=20.0, tiny=True):
     """The oracle, as it stands, on a bounded sample of the workload: the full
     selector for one query head and the attention of a few work tiles,
     extrapolated linearly to the whole workload (units: effective TFLOP/s).
@@ -313,6 +374,7 @@ def cpu_baseline(inp, idx, cnt, out=None, lse=None, n_tiles_sample=400, budget_s
                    f"extrapolated linearly to all heads and all {int(total_pairs)} selected blocks "
                    f"(est. {est_time:.0f} s per step)"),
         "est_seconds_per_step": est_time,
+        **({"tiny_in_full": tiny_oracle_timing()} if tiny else {}),
         "parity": {
             "selection": {"head": h0, "rows": int(sel["counts"].size), "count_mismatches": count_mismatch,
                           "list_mismatches_outside_near_ties": list_mismatch, "near_tie_rows": near,
@@ -383,18 +445,95 @@ def run_schedule(args):
     t_dense = timed(lambda: bsa.bsa_forward(q, k, v, None, None, P, lens, bq, bk, return_lse=False),
                     max(3, args.steps))
     bsa.bsa_device_status()
-    sch = SCHEDULES[args.schedule]
-    totals = {}
-    for arm, is_dense in sch["arms"].items():
-        n_d = sum(1 for s in range(sch["steps"]) for l in range(sch["layers"]) if is_dense(s, l))
-        n_s = sch["steps"] * sch["layers"] - n_d
-        totals[arm] = dict(dense_calls=n_d, sparse_calls=n_s, attention_s=(n_d * t_dense + n_s * t_sparse) / 1e3)
-    base = totals["dense"]["attention_s"]
-    for arm in totals:
-        totals[arm]["speedup_vs_dense"] = base / totals[arm]["attention_s"]
     print(json.dumps({"schedule": args.schedule, "workload": args.config, "dense_call_ms": t_dense,
-                      "sparse_call_ms": t_sparse, "per_call_speedup": t_dense / t_sparse, "arms": totals,
-                      "pages_end_to_end_speedups": sch["published"]}), flush=True)
+                      "sparse_call_ms": t_sparse, "per_call_speedup": t_dense / t_sparse,
+                      **schedule_arms(args.schedule, t_dense, t_sparse)}), flush=True)
+
+
+def time_calls(fn, n: int, stream, warm: int = 2):
+    """Median and all per-call times (ms) of n back-to-back calls, each between
+    its own CUDA events on `stream`, after `warm` untimed calls."""
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    return sorted(ms)[len(ms) // 2], ms
+
+
+def other_workloads(bsa, pk, stream, step_inputs, step_fwd_ms, step_ms, step_sparsity):
+    """Forward time of the dense pass on the step's own inputs (the north
+    star's 'speedup over this library's own dense pass'), and the forward of
+    the other video-latent workloads (480p at 75 %, 480p dense, the ragged
+    1280x736 batch, with its dense pass); plus the pages' dense->sparse
+    schedules evaluated from those call times.  Outside the timed step."""
+    import torch
+    from bsa_inputs import CONFIGS, make_inputs
+    res = {}
+    q, k, v, c = step_inputs["q"], step_inputs["k"], step_inputs["v"], step_inputs["cfg"]
+    lens = step_inputs["seq_lens"]
+    out = torch.empty_like(q)
+    fws = torch.empty(max(256, bsa.bsa_forward_workspace_size(c.B, c.Hq, c.Sq, c.Skv, c.block_q, c.block_k)),
+                      dtype=torch.uint8, device="cuda")
+    d_ms, d_all = time_calls(lambda: bsa.bsa_forward(q, k, v, None, None, c.prefix, lens, c.block_q, c.block_k,
+                                                     out=out, return_lse=False, workspace=fws, stream=stream),
+                             3, stream, warm=1)
+    bsa.bsa_device_status(stream)
+    d_flops = 4.0 * c.d * c.block_q * c.block_k * dense_tiles(lens, c.prefix, c.Hq, c.block_q, c.block_k)
+    res[c.name] = {"dense_fwd_ms": d_ms, "dense_fwd_ms_all": d_all,
+                   "dense_tflops": d_flops / (d_ms * 1e-3) / 1e12,
+                   "dense_over_sparse_fwd": d_ms / step_fwd_ms,
+                   "dense_over_sparse_ideal": 1.0 / (1.0 - step_sparsity),
+                   "note": "ideal = 1 / (1 - tile sparsity): the sparse forward's share of the dense work"}
+    schedules = {"cosmos3_on_" + c.name: {"dense_call_ms": d_ms, "sparse_call_ms": step_ms,
+                                          **schedule_arms("cosmos3", d_ms, step_ms)}}
+    del out, fws
+    for name, n in (("480p_75", 5), ("480p_dense", 5), ("1280x736_ragged", 3)):
+        cfg = CONFIGS[name]
+        inp = make_inputs(cfg, "cuda", pad_fill=0.0)
+        q2, k2, v2, L2 = inp["q"], inp["k"], inp["v"], inp["seq_lens"]
+        o2 = torch.empty_like(q2)
+        P2, bq, bk = cfg.prefix, cfg.block_q, cfg.block_k
+        fw = torch.empty(max(256, bsa.bsa_forward_workspace_size(cfg.B, cfg.Hq, cfg.Sq, cfg.Skv, bq, bk)),
+                         dtype=torch.uint8, device="cuda")
+        dense = cfg.keep == 1.0
+        row = {}
+        if dense:
+            idx = cnt = None
+            flops = 4.0 * cfg.d * bq * bk * dense_tiles(L2, P2, cfg.Hq, bq, bk)
+            sparsity = 0.0
+        else:
+            sel_ms, _ = time_calls(lambda: bsa.bsa_select(q2, k2, P2, L2, bq, bk, inp["keep_ratio"]), 3, stream)
+            idx, cnt = bsa.bsa_select(q2, k2, P2, L2, bq, bk, inp["keep_ratio"])
+            flops = tile_flops(cnt, cfg.d, bq, bk)
+            sparsity = 1.0 - float(cnt.sum()) / dense_tiles(L2, P2, cfg.Hq, bq, bk)
+            row["select_ms"] = sel_ms
+        f_ms, f_all = time_calls(lambda: bsa.bsa_forward(q2, k2, v2, idx, cnt, P2, L2, bq, bk, out=o2,
+                                                         return_lse=False, workspace=fw, stream=stream), n, stream)
+        bsa.bsa_device_status(stream)
+        tf = flops / (f_ms * 1e-3) / 1e12
+        row.update({"fwd_ms": f_ms, "fwd_ms_all": f_all, "tflops_effective": tf, "frac_of_bf16_peak": tf / pk["bf16"],
+                    "tile_sparsity": sparsity, "dense_pass": dense, "calls": n})
+        if name == "1280x736_ragged":
+            dd_ms, dd_all = time_calls(lambda: bsa.bsa_forward(q2, k2, v2, None, None, P2, L2, bq, bk, out=o2,
+                                                               return_lse=False, workspace=fw, stream=stream),
+                                       3, stream, warm=1)
+            bsa.bsa_device_status(stream)
+            row.update({"dense_fwd_ms": dd_ms, "dense_fwd_ms_all": dd_all, "dense_over_sparse_fwd": dd_ms / f_ms,
+                        "dense_over_sparse_ideal": 1.0 / (1.0 - sparsity)})
+            sparse_step = row["select_ms"] + f_ms
+            schedules["h3_on_" + name] = {"dense_call_ms": dd_ms, "sparse_call_ms": sparse_step,
+                                          **schedule_arms("h3", dd_ms, sparse_step)}
+        res[name] = row
+        del q2, k2, v2, o2, fw, idx, cnt, inp
+        torch.cuda.empty_cache()
+    return res, schedules
 
 
 def run_reference(args, rank, world):
@@ -457,11 +596,17 @@ def run_reference(args, rank, world):
     value = steps_flops_est[0] / est_mean / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": est_mean * 1e3,
+        "steps": args.steps, "warmup": args.warmup,
+        # measured: host wall time of the sampled oracle work of one step
+        "ms_per_step": wall / args.steps * 1e3,
+        # not measured: that sample scaled to the whole workload; `value` divides the
+        # workload's effective FLOPs by this estimate
+        "est_ms_per_step_extrapolated": est_mean * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": args.config, "sample": "per step: full selector of one "
-                                        "random query head + attention of one random work tile, "
-                                        "extrapolated to the whole workload"},
+                                        "random query head + attention of one random work tile; value = the "
+                                        "workload's effective FLOPs / that sample extrapolated to the whole "
+                                        "workload (est_ms_per_step_extrapolated)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
                          "sample": f"{args.steps} steps, {wall:.1f} s of measured oracle work"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -647,6 +792,11 @@ def main():
                              "overlap the neighbouring steps' compute"}
         del bufs[1], ws2[1], fws2[1]
 
+    # ---- the dense pass on the same inputs and the other workloads ----
+    workloads = schedules = None
+    if not args.no_workloads:
+        workloads, schedules = other_workloads(bsa, pk, stream, inp, fwd_mean, ms_step, tile_sparsity)
+
     # ---- backward pass (dQ, dK, dV) over the same lists, outputs and LSE ----
     bwd = None
     if args.backward:
@@ -768,6 +918,10 @@ def main():
                          "algorithmic_bytes": algorithmic_bytes(cfg, cnt_np),
                          "algorithmic_flops": flops},
             "clocks": clocks,
+            **({"dense_fwd_ms": workloads[args.config]["dense_fwd_ms"],
+                "dense_over_sparse": workloads[args.config]["dense_over_sparse_fwd"],
+                "dense_over_sparse_ideal": workloads[args.config]["dense_over_sparse_ideal"],
+                "workloads": workloads, "schedules": schedules} if workloads else {}),
             "e2e": e2e,
             **({"backward": bwd} if bwd is not None else {}),
             **({"extras": extras} if extras is not None else {}),

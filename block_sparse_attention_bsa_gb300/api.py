@@ -64,6 +64,31 @@ def _cdiv(a: int, b: int) -> int:
     return -(-a // b)
 
 
+def _check_buffer(name: str, t, shape, dtype, device) -> None:
+    """Raises ValueError unless ``t`` is a contiguous tensor of exactly
+    ``shape`` and ``dtype`` on ``device``.  The C ABI receives bare pointers
+    and cannot see a buffer's size, so every caller-passed input list and
+    output buffer is checked here, before anything is launched."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if (t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous()
+            or t.device != torch.device(device)):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device} "
+                         f"(got {t.dtype}, {tuple(t.shape)}, contiguous={t.is_contiguous()}, {t.device})")
+
+
+def _lists(indices, counts, B, Hq, nQb, nKb, device):
+    """Index/count buffers for a selector call: new ones (indices start at -1)
+    or the caller's, checked."""
+    if indices is None:
+        indices = torch.full((B, Hq, nQb, nKb), -1, dtype=torch.int32, device=device)
+    if counts is None:
+        counts = torch.empty((B, Hq, nQb), dtype=torch.int32, device=device)
+    _check_buffer("indices", indices, (B, Hq, nQb, nKb), torch.int32, device)
+    _check_buffer("counts", counts, (B, Hq, nQb), torch.int32, device)
+    return indices, counts
+
+
 def bsa_version() -> int:
     return _lib.load().bsa_version()
 
@@ -106,13 +131,7 @@ def bsa_select(q: torch.Tensor, k: torch.Tensor, prefix_len: int, seq_lens: Opti
     if isinstance(keep_ratio, (int, float)):
         keep_ratio = [float(keep_ratio)]
     keep = (ctypes.c_float * len(keep_ratio))(*[float(x) for x in keep_ratio])
-    if indices is None:
-        indices = torch.full((B, Hq, nQb, nKb), -1, dtype=torch.int32, device=q.device)
-    if counts is None:
-        counts = torch.empty((B, Hq, nQb), dtype=torch.int32, device=q.device)
-    for name, t, shape in (("indices", indices, (B, Hq, nQb, nKb)), ("counts", counts, (B, Hq, nQb))):
-        if t.dtype != torch.int32 or tuple(t.shape) != shape or not t.is_contiguous() or t.device != q.device:
-            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of shape {shape}")
+    indices, counts = _lists(indices, counts, B, Hq, nQb, nKb, q.device)
     need = bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, block_q, block_k)
     ws = _workspace(need, q.device, workspace)
     lib = _lib.load()
@@ -144,10 +163,9 @@ def bsa_select_rope(q: torch.Tensor, k: torch.Tensor, cos_q: torch.Tensor, sin_q
     keep = (ctypes.c_float * len(keep_ratio))(*[float(x) for x in keep_ratio])
     q_out = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device=q.device) if q_out is None else q_out
     k_out = torch.empty((B, Skv, Hkv, d), dtype=torch.bfloat16, device=q.device) if k_out is None else k_out
-    if indices is None:
-        indices = torch.full((B, Hq, nQb, nKb), -1, dtype=torch.int32, device=q.device)
-    if counts is None:
-        counts = torch.empty((B, Hq, nQb), dtype=torch.int32, device=q.device)
+    _check_buffer("q_out", q_out, (B, Sq, Hq, d), torch.bfloat16, q.device)
+    _check_buffer("k_out", k_out, (B, Skv, Hkv, d), torch.bfloat16, q.device)
+    indices, counts = _lists(indices, counts, B, Hq, nQb, nKb, q.device)
     need = bsa_select_workspace_size(B, Hq, Hkv, Sq, Skv, d, block_q, block_k)
     ws = _workspace(need, q.device, workspace)
     st = _lib.load().bsa_select_rope(ctypes.byref(qd), ctypes.byref(kd), cos_q.data_ptr(), sin_q.data_ptr(),
@@ -172,10 +190,7 @@ def bsa_select_noalloc(q: torch.Tensor, k: torch.Tensor, prefix_len: int, seq_le
     if isinstance(keep_ratio, (int, float)):
         keep_ratio = [float(keep_ratio)]
     keep = (ctypes.c_float * len(keep_ratio))(*[float(x) for x in keep_ratio])
-    if indices is None:
-        indices = torch.full((B, Hq, nQb, nKb), -1, dtype=torch.int32, device=q.device)
-    if counts is None:
-        counts = torch.empty((B, Hq, nQb), dtype=torch.int32, device=q.device)
+    indices, counts = _lists(indices, counts, B, Hq, nQb, nKb, q.device)
     st = _lib.load().bsa_select_noalloc(ctypes.byref(qd), ctypes.byref(kd), int(prefix_len),
                                         _i32_array(seq_lens), int(block_q), int(block_k), keep,
                                         len(keep_ratio), indices.data_ptr(), counts.data_ptr(),
@@ -197,16 +212,17 @@ def bsa_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, indices: Opti
     B, Sq, Hq, d = q.shape
     if out is None:
         out = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device=q.device)
-    if tuple(out.shape) != (B, Sq, Hq, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
-        raise ValueError("out must be a contiguous bf16 tensor [B, Sq, Hq, d]")
+    _check_buffer("out", out, (B, Sq, Hq, d), torch.bfloat16, q.device)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
-    if lse is not None and (tuple(lse.shape) != (B, Hq, Sq) or lse.dtype != torch.float32
-                            or not lse.is_contiguous()):
-        raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, Sq]")
-    for name, t in (("indices", indices), ("counts", counts)):
-        if t is not None and (t.dtype != torch.int32 or not t.is_contiguous() or t.device != q.device):
-            raise ValueError(f"{name} must be a contiguous int32 tensor on {q.device}")
+    if lse is not None:
+        _check_buffer("lse", lse, (B, Hq, Sq), torch.float32, q.device)
+    if (indices is None) != (counts is None):
+        raise ValueError("indices and counts are given together (both None: the dense pass)")
+    if indices is not None:
+        _check_buffer("indices", indices, (B, Hq, _cdiv(Sq, block_q), _cdiv(k.shape[1], block_k)), torch.int32,
+                      q.device)
+        _check_buffer("counts", counts, (B, Hq, _cdiv(Sq, block_q)), torch.int32, q.device)
     need = bsa_forward_workspace_size(B, Hq, Sq, k.shape[1], block_q, block_k)
     ws = _workspace(need, q.device, workspace)
     lib = _lib.load()
@@ -233,10 +249,11 @@ def bsa_forward_causal(q_und: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bl
     B, P, Hq, d = q_und.shape
     if out is None:
         out = torch.empty((B, P, Hq, d), dtype=torch.bfloat16, device=q_und.device)
-    if tuple(out.shape) != (B, P, Hq, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
-        raise ValueError("out must be a contiguous bf16 tensor [B, P, Hq, d]")
+    _check_buffer("out", out, (B, P, Hq, d), torch.bfloat16, q_und.device)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq, P), dtype=torch.float32, device=q_und.device)
+    if lse is not None:
+        _check_buffer("lse", lse, (B, Hq, P), torch.float32, q_und.device)
     need = bsa_forward_workspace_size(B, Hq, P, k.shape[1], block_q, block_k)
     ws = _workspace(need, q_und.device, workspace)
     st = _lib.load().bsa_forward_causal(ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), int(block_q),
@@ -273,13 +290,10 @@ def bsa_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.T
     if dv is None:
         dv = torch.empty((B, Skv, Hkv, d), dtype=torch.bfloat16, device=q.device)
     for name, t, shape in (("dq", dq, (B, Sq, Hq, d)), ("dk", dk, (B, Skv, Hkv, d)), ("dv", dv, (B, Skv, Hkv, d))):
-        if tuple(t.shape) != shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous bf16 tensor {list(shape)}")
-    if tuple(lse.shape) != (B, Hq, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 tensor [B, Hq, Sq]")
-    for name, t in (("indices", indices), ("counts", counts)):
-        if t.dtype != torch.int32 or not t.is_contiguous() or t.device != q.device:
-            raise ValueError(f"{name} must be a contiguous int32 tensor on {q.device}")
+        _check_buffer(name, t, shape, torch.bfloat16, q.device)
+    _check_buffer("lse", lse, (B, Hq, Sq), torch.float32, q.device)
+    _check_buffer("indices", indices, (B, Hq, _cdiv(Sq, block_q), _cdiv(Skv, block_k)), torch.int32, q.device)
+    _check_buffer("counts", counts, (B, Hq, _cdiv(Sq, block_q)), torch.int32, q.device)
     need = bsa_backward_workspace_size(B, Hq, Hkv, Sq, Skv, block_q, block_k)
     ws = _workspace(need, q.device, workspace)
     st = _lib.load().bsa_backward(ctypes.byref(qd), ctypes.byref(kd), ctypes.byref(vd), ctypes.byref(od),

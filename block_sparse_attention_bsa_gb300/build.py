@@ -29,17 +29,17 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found (set NVCC or put the CUDA toolkit on PATH)")
 
 
-def _flags(verbose_ptxas: bool, defines=()):
-    f = [f"-D{d}" for d in defines] + ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
+def _flags(verbose_ptxas: bool):
+    f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
                 "-I", os.path.join(ROOT, "include"), "-DNDEBUG"]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
     return f
 
 
-def _compile(src: str, verbose_ptxas: bool, build_dir: str = BUILD, defines=()) -> tuple:
-    obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj] + _flags(verbose_ptxas, defines)
+def _compile(src: str, verbose_ptxas: bool) -> tuple:
+    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+    cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj] + _flags(verbose_ptxas)
     r = subprocess.run(cmd, capture_output=True, text=True)
     return src, obj, r.returncode, r.stdout + r.stderr
 
@@ -53,17 +53,13 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = False,
-          out: str = None, defines=()) -> str:
-    """Compiles the library if a source is newer than it; returns its path.
-    ``out``/``defines`` build a variant with extra -D tuning macros elsewhere."""
-    lib = out or LIB
-    if out is None and not force and not _stale():
+def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = False) -> str:
+    """Compiles the library if a source is newer than it; returns its path."""
+    if not force and not _stale():
         return LIB
-    build_dir = BUILD if out is None else out + ".objs"
-    os.makedirs(build_dir, exist_ok=True)
+    os.makedirs(BUILD, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(lambda s: _compile(s, verbose_ptxas, build_dir, defines), SOURCES))
+        results = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
     failed = [r for r in results if r[2] != 0]
     for src, _, rc, log in results:
         if log.strip() and (verbose_ptxas or rc != 0) and not quiet:
@@ -71,13 +67,13 @@ def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = False,
     if failed:
         raise RuntimeError("nvcc failed for " + ", ".join(r[0] for r in failed) + ":\n" +
                            "\n".join(r[3] for r in failed))
-    tmp = lib + ".tmp"
+    tmp = LIB + ".tmp"
     cmd = [nvcc(), "-shared", "-o", tmp] + [r[1] for r in results] + ARCH + ["-Xcompiler", "-fPIC"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
-    os.replace(tmp, lib)
-    return lib
+    os.replace(tmp, LIB)
+    return LIB
 
 
 if __name__ == "__main__":

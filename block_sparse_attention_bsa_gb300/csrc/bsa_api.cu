@@ -258,13 +258,14 @@ size_t bsa_select_workspace_size(int B, int Hq, int Hkv, int Sq, int Skv, int d,
 
 }  // extern "C"
 
-namespace {
-// Shared body of bsa_select and bsa_select_rope (`rope` carries the tables and
-// rotated outputs, or is NULL).
+namespace bsa {
+// Shared body of bsa_select, bsa_select_rope and bsa_select_noalloc (`rope`
+// carries the tables and rotated outputs, or is NULL; `static_scratch`, when
+// given, supplies the workspace after every argument has been checked).
 bsa_status select_impl(const char* fn, const bsa_tensor* q, const bsa_tensor* k, int32_t prefix_len,
                        const int32_t* seq_lens, int32_t block_q, int32_t block_k, const float* keep_ratio,
                        int32_t n_keep, int32_t* indices, int32_t* counts, void* workspace, size_t ws_bytes,
-                       bsa_stream_t stream, const SelectArgs* rope) {
+                       bsa_stream_t stream, const SelectArgs* rope, StaticScratchFn static_scratch) {
   bsa_status st = check_common(fn, q, k, prefix_len, seq_lens, block_q, block_k, kMaxSelectBatch);
   if (st != BSA_OK) return st;
   if (!keep_ratio) return set_error(BSA_ERR_INVALID_ARG, std::string(fn) + ": keep_ratio is NULL");
@@ -283,6 +284,9 @@ bsa_status select_impl(const char* fn, const bsa_tensor* q, const bsa_tensor* k,
   if (!counts) return set_error(BSA_ERR_INVALID_ARG, std::string(fn) + ": counts is NULL");
   const size_t need = select_workspace_bytes((int)q->B, (int)q->H, (int)k->H, (int)q->S, (int)k->S, (int)q->D,
                                              block_q, block_k);
+  if (static_scratch) {
+    if ((st = static_scratch(fn, need, &workspace, &ws_bytes)) != BSA_OK) return st;
+  }
   if ((st = check_workspace(fn, workspace, ws_bytes, need)) != BSA_OK) return st;
   SelectArgs a{};
   a.q = q->ptr; a.q_sb = q->stride_b; a.q_ss = q->stride_s; a.q_sh = q->stride_h;
@@ -302,7 +306,7 @@ bsa_status select_impl(const char* fn, const bsa_tensor* q, const bsa_tensor* k,
   a.kbar = reinterpret_cast<float*>(static_cast<char*>(workspace) + qbar_bytes);
   return launch_select(a, reinterpret_cast<cudaStream_t>(stream));
 }
-}  // namespace
+}  // namespace bsa
 
 extern "C" {
 
@@ -312,7 +316,7 @@ bsa_status bsa_select(const bsa_tensor* q, const bsa_tensor* k, int32_t prefix_l
                       bsa_stream_t stream) {
   clear_error();
   return select_impl("bsa_select", q, k, prefix_len, seq_lens, block_q, block_k, keep_ratio, n_keep, indices,
-                     counts, workspace, ws_bytes, stream, nullptr);
+                     counts, workspace, ws_bytes, stream, nullptr, nullptr);
 }
 
 bsa_status bsa_select_rope(const bsa_tensor* q, const bsa_tensor* k, const float* cos_q, const float* sin_q,
@@ -331,7 +335,7 @@ bsa_status bsa_select_rope(const bsa_tensor* q, const bsa_tensor* k, const float
   SelectArgs r{};
   r.cos_q = cos_q; r.sin_q = sin_q; r.cos_k = cos_k; r.sin_k = sin_k; r.q_out = q_out; r.k_out = k_out;
   return select_impl("bsa_select_rope", q, k, prefix_len, seq_lens, block_q, block_k, keep_ratio, n_keep,
-                     indices, counts, workspace, ws_bytes, stream, &r);
+                     indices, counts, workspace, ws_bytes, stream, &r, nullptr);
 }
 
 size_t bsa_forward_workspace_size(int B, int Hq, int Sq, int Skv, int block_q, int block_k) {

@@ -37,13 +37,6 @@
 #include "bsa_internal.h"
 #include "bsa_ptx.cuh"
 
-#ifndef BSA_SOFTMAX_MAX3
-#define BSA_SOFTMAX_MAX3 1       // three-input max for the row max
-#endif
-#ifndef BSA_REG_CONTROL
-#define BSA_REG_CONTROL 0        // registers of the control warpgroup (0: no split; measured faster)
-#endif
-
 namespace bsa {
 
 namespace {
@@ -83,14 +76,6 @@ struct Cfg {
   static constexpr int kSmemBytes = kQBytes + kStages * kStageBytes + kBarBytes + kAlignSlack;
   static constexpr int kThreads = 128 + 128 * NH;
   static constexpr uint32_t kTmemCols = NH == 2 ? 512 : 256;
-  // Register split for NH == 2 (launched with 168 per thread x 384 threads
-  // = 64,512): control warpgroup 56, each softmax warpgroup 224
-  // (56*128 + 224*256 = 64,512).
-  static constexpr uint32_t kRegsLaunch = 168;
-  static constexpr uint32_t kRegsControl = BSA_REG_CONTROL;
-  static constexpr uint32_t kRegsSoftmax = ((kRegsLaunch * kThreads - BSA_REG_CONTROL * 128) / 256) / 8 * 8;
-  static_assert(NH != 2 || kRegsControl * 128 + kRegsSoftmax * 256 <= kRegsLaunch * kThreads,
-                "register split exceeds the launch budget");
   static constexpr uint32_t kOCol = NH * 128;             // O_h at kOCol + 128 h
   static_assert(kStages >= 2, "not enough shared memory for a K/V ring");
   static_assert(D == 64 || D == 128, "head dim");
@@ -152,17 +137,10 @@ __device__ __forceinline__ float row_max(const float (&v)[M]) {
   float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
   for (int c = LO; c < LO + N; c += 8) {
-#if BSA_SOFTMAX_MAX3
     m0 = max3f(m0, v[c], v[c + 1]);
     m1 = max3f(m1, v[c + 2], v[c + 3]);
     m2 = max3f(m2, v[c + 4], v[c + 5]);
     m3 = max3f(m3, v[c + 6], v[c + 7]);
-#else
-    m0 = fmaxf(fmaxf(m0, v[c]), v[c + 1]);
-    m1 = fmaxf(fmaxf(m1, v[c + 2]), v[c + 3]);
-    m2 = fmaxf(fmaxf(m2, v[c + 4]), v[c + 5]);
-    m3 = fmaxf(fmaxf(m3, v[c + 6]), v[c + 7]);
-#endif
   }
   return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
@@ -260,7 +238,6 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-  if constexpr (NH == 2 && BSA_REG_CONTROL > 0) regs_dec<C::kRegsControl>();
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer ---
     Ring ring;
@@ -443,7 +420,6 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
     __syncwarp();
   }
   } else {
-    if constexpr (NH == 2 && BSA_REG_CONTROL > 0) regs_inc<C::kRegsSoftmax>();
     // --------------------------------------------------- softmax + epilogue ---
     const int hh = (warp - 4) / 4;
     const int wq = warp % 4;

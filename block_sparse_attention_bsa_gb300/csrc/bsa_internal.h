@@ -53,6 +53,18 @@ struct SelectArgs {
 };
 bsa_status launch_select(const SelectArgs& a, cudaStream_t stream);
 
+// Supplies a selector workspace that the caller did not pass (the static
+// scratch of bsa_select_noalloc): given the bytes needed, sets *ws and
+// *ws_bytes or returns an error naming `fn`.
+using StaticScratchFn = bsa_status (*)(const char* fn, size_t need, void** ws, size_t* ws_bytes);
+// The selector entry points' common body (bsa_api.cu): checks every argument
+// under the name `fn`, then launches.  `rope` is NULL for the plain selector;
+// `static_scratch` is NULL when the caller passes the workspace.
+bsa_status select_impl(const char* fn, const bsa_tensor* q, const bsa_tensor* k, int32_t prefix_len,
+                       const int32_t* seq_lens, int32_t block_q, int32_t block_k, const float* keep_ratio,
+                       int32_t n_keep, int32_t* indices, int32_t* counts, void* workspace, size_t ws_bytes,
+                       bsa_stream_t stream, const SelectArgs* rope, StaticScratchFn static_scratch);
+
 // ---- forward (bsa_fmha.cu) ----
 struct ForwardArgs {
   const void* q; int64_t q_sb, q_ss, q_sh;

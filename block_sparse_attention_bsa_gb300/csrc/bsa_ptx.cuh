@@ -345,18 +345,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Per-warpgroup register budget changes (all warps of a warpgroup execute
-// the same one).  The amounts must add up to at most the registers the block
-// was launched with.
-template <uint32_t N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // max of three floats (sm_100+ three-input form).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;

@@ -494,25 +494,73 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[BSA_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (the host-side symbol is only a stand-in, never a device address).
-bsa_status noalloc_scratch_address(void** out) {
+// Device address of g_noalloc_scratch, looked up with cudaGetSymbolAddress
+// the first time a device is used (the host-side symbol is only a stand-in,
+// never a device address).  The unique ID of the context it was looked up in
+// is kept with it: after cudaDeviceReset the module is loaded again in a new
+// primary context, where the array may sit elsewhere, so a call made in a
+// different context looks the address up again.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename F>
+F driver_fn(const char* name) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<F>(f);
+  return nullptr;
+}
+
+// ID of the calling thread's current context; 0 when none is current yet.
+bsa_status current_context_id(const char* fn, unsigned long long* id) {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_ctx = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    get_ctx = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  });
+  if (!get_ctx || !get_id)
+    return set_error(BSA_ERR_CUDA, std::string(fn) + ": cuCtxGetCurrent / cuCtxGetId are not available");
+  CUcontext ctx = nullptr;
+  *id = 0;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return set_error(BSA_ERR_CUDA, std::string(fn) + ": cuCtxGetCurrent failed");
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS)
+    return set_error(BSA_ERR_CUDA, std::string(fn) + ": cuCtxGetId failed");
+  return BSA_OK;
+}
+
+bsa_status noalloc_scratch(const char* fn, size_t need, void** ws, size_t* ws_bytes) {
+  if (need > BSA_NOALLOC_SCRATCH_BYTES)
+    return set_error(BSA_ERR_UNSUPPORTED, std::string(fn) + ": the block means need " + std::to_string(need) +
+                                              " bytes, above the static scratch of " +
+                                              std::to_string((size_t)BSA_NOALLOC_SCRATCH_BYTES) +
+                                              " bytes; use bsa_select");
   static std::mutex mu;
   static void* addr[64] = {nullptr};
+  static unsigned long long ctx_id[64] = {0};
   int dev = 0;
   bsa_status st = cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
   if (st != BSA_OK) return st;
   if (dev < 0 || dev >= 64)
-    return set_error(BSA_ERR_UNSUPPORTED, "bsa_select_noalloc: device ordinal " + std::to_string(dev) +
+    return set_error(BSA_ERR_UNSUPPORTED, std::string(fn) + ": device ordinal " + std::to_string(dev) +
                                               " above the 64 devices it tracks");
+  unsigned long long id = 0;
+  if ((st = current_context_id(fn, &id)) != BSA_OK) return st;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || id == 0 || ctx_id[dev] != id) {
     void* p = nullptr;
+    // also makes the device's primary context current if none was
     st = cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)");
     if (st != BSA_OK) return st;
+    if ((st = current_context_id(fn, &id)) != BSA_OK) return st;
     addr[dev] = p;
+    ctx_id[dev] = id;
   }
-  *out = addr[dev];
+  *ws = addr[dev];
+  *ws_bytes = BSA_NOALLOC_SCRATCH_BYTES;
   return BSA_OK;
 }
 
@@ -525,19 +573,6 @@ extern "C" bsa_status bsa_select_noalloc(const bsa_tensor* q, const bsa_tensor* 
                                          int32_t* counts, bsa_stream_t stream) {
   using namespace bsa;
   clear_error();
-  if (q && k && q->B > 0 && q->H > 0 && k->H > 0 && q->S > 0 && k->S > 0 && q->D > 0 && block_q > 0 &&
-      block_k > 0) {
-    const size_t need = select_workspace_bytes((int)q->B, (int)q->H, (int)k->H, (int)q->S, (int)k->S,
-                                               (int)q->D, block_q, block_k);
-    if (need > BSA_NOALLOC_SCRATCH_BYTES)
-      return set_error(BSA_ERR_UNSUPPORTED,
-                       "bsa_select_noalloc: the block means need " + std::to_string(need) +
-                           " bytes, above the static scratch of " +
-                           std::to_string((size_t)BSA_NOALLOC_SCRATCH_BYTES) + " bytes; use bsa_select");
-  }
-  void* scratch = nullptr;
-  const bsa_status st = noalloc_scratch_address(&scratch);
-  if (st != BSA_OK) return st;
-  return bsa_select(q, k, prefix_len, seq_lens, block_q, block_k, keep_ratio, n_keep, indices, counts,
-                    scratch, BSA_NOALLOC_SCRATCH_BYTES, stream);
+  return select_impl("bsa_select_noalloc", q, k, prefix_len, seq_lens, block_q, block_k, keep_ratio, n_keep,
+                     indices, counts, nullptr, 0, stream, nullptr, noalloc_scratch);
 }

@@ -105,12 +105,33 @@ def test_bench_parity_verdicts_catch_planted_defects():
                        cfg.block_k)
     out = torch.from_numpy(np.nan_to_num(o)).bfloat16()
     lse = torch.from_numpy(np.where(np.isnan(l), -np.inf, l)).float()
-    good = bench.cpu_baseline(inp, idx, cnt, out, lse, n_tiles_sample=64, budget_s=10)["parity"]
+    good = bench.cpu_baseline(inp, idx, cnt, out, lse, n_tiles_sample=64, budget_s=10, tiny=False)["parity"]
     assert good["selection"]["ok"] and good["attention"]["ok"], good
     bad_idx = idx.clone()
     bad_idx[0, 0, 1, 2], bad_idx[0, 0, 1, 3] = idx[0, 0, 1, 3], idx[0, 0, 1, 2]
     bad_out = out.clone()
     bad_out[0, :10, 0, :] += 0.5
-    bad = bench.cpu_baseline(inp, bad_idx, cnt, bad_out, lse, n_tiles_sample=64, budget_s=10)["parity"]
+    bad = bench.cpu_baseline(inp, bad_idx, cnt, bad_out, lse, n_tiles_sample=64, budget_s=10, tiny=False)["parity"]
     assert not bad["selection"]["ok"] and bad["selection"]["list_mismatches_outside_near_ties"] == 1
     assert not bad["attention"]["ok"]
+
+
+def test_dense_tiles_and_schedule_arms():
+    """Dense work counts every real query block against every key block with a
+    real key; a schedule's attention time is its call counts x call times."""
+    cfg = CONFIGS["480p_dense"]
+    # 189 query blocks x 382 key blocks x 24 heads (the last blocks ragged)
+    assert bench.dense_tiles(cfg.lens, cfg.prefix, cfg.Hq, cfg.block_q, cfg.block_k) == 189 * 382 * 24
+    r = CONFIGS["1280x736_ragged"]
+    assert bench.dense_tiles(r.lens, r.prefix, r.Hq, 256, 128) == (690 * 1384 + 586 * 1176) * 24
+    arms = bench.schedule_arms("cosmos3", 4.0, 1.0)["arms"]
+    assert arms["dense"]["attention_s"] == pytest.approx(35 * 36 * 4.0 / 1e3)
+    assert arms["all_sparse"]["speedup_vs_dense"] == pytest.approx(4.0)
+    mixed = (10 * 36 + 25 * 8) * 4.0 + 25 * 28 * 1.0
+    assert arms["mixed"]["speedup_vs_dense"] == pytest.approx(35 * 36 * 4.0 / mixed)
+
+
+def test_tiny_oracle_timing_runs_in_child_processes():
+    t = bench.tiny_oracle_timing()
+    assert t["one_core"]["threads"] == 1 and t["one_core"]["seconds"] > 0
+    assert t["all_cores"]["threads"] == (os.cpu_count() or 1) and t["all_cores"]["tflops"] > 0

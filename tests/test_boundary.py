@@ -209,6 +209,32 @@ def test_python_binding_refuses_cpu_tensors():
         bsa.bsa_forward(q, q, q, None, None, 0, None, 64, 64)
 
 
+def test_binding_checks_caller_buffers_before_any_launch():
+    """The C ABI sees bare pointers, so the binding checks every buffer a caller
+    passes (shape, dtype, contiguity, device) on the host; a wrong one raises
+    ValueError before anything is launched."""
+    import torch
+    from block_sparse_attention_bsa_gb300 import api
+    dev = torch.device("cpu")
+    good_i = torch.full((1, 4, 2, 6), -1, dtype=torch.int32)
+    good_c = torch.zeros((1, 4, 2), dtype=torch.int32)
+    i, c = api._lists(good_i, good_c, 1, 4, 2, 6, dev)
+    assert i is good_i and c is good_c
+    bad_lists = [torch.full((1, 4, 2, 5), -1, dtype=torch.int32),                 # row capacity short
+                 good_i.to(torch.int64),                                           # wrong dtype
+                 torch.full((1, 4, 6, 2), -1, dtype=torch.int32).transpose(2, 3)]  # not contiguous
+    for bad in bad_lists:
+        with pytest.raises(ValueError, match="indices"):
+            api._lists(bad, good_c, 1, 4, 2, 6, dev)
+    with pytest.raises(ValueError, match="counts"):
+        api._lists(good_i, torch.zeros((1, 4, 3), dtype=torch.int32), 1, 4, 2, 6, dev)
+    with pytest.raises(ValueError, match="q_out"):
+        api._check_buffer("q_out", torch.zeros(1, 8, 4, 64, dtype=torch.float16), (1, 8, 4, 64), torch.bfloat16, dev)
+    with pytest.raises(ValueError, match="on meta"):
+        api._check_buffer("out", torch.zeros(1, 8, 4, 64, dtype=torch.bfloat16), (1, 8, 4, 64), torch.bfloat16,
+                          torch.device("meta"))
+
+
 def test_causal_rejects_bad_arguments(lib):
     q, k, v = T(H=4, S=512), T(H=2, S=400), T(H=2, S=400)
     st = lib.bsa_forward_causal(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 256, 128, 0.0, FAKE, None,
@@ -324,3 +350,15 @@ def test_product_package_never_touches_the_oracle():
         for f in files:
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 assert "oracle" not in open(os.path.join(dirpath, f)).read(), f
+
+
+def test_noalloc_reports_argument_errors_under_its_own_name(lib):
+    """bsa_select_noalloc checks its arguments (under its own name) before it
+    looks at the static scratch: an unsupported geometry is reported as such,
+    not as a size problem."""
+    q, k = T(H=4), T(H=2, S=768)
+    keep = (ctypes.c_float * 1)(0.25)
+    st = lib.bsa_select_noalloc(ctypes.byref(q), ctypes.byref(k), 256, None, 100, 128, keep, 1, FAKE, FAKE, None)
+    assert st == 2 and err(lib).startswith("bsa_select_noalloc: block geometry")
+    st = lib.bsa_select_noalloc(ctypes.byref(q), ctypes.byref(k), 256, None, 256, 128, keep, 1, None, FAKE, None)
+    assert st == 1 and err(lib) == "bsa_select_noalloc: indices is NULL"

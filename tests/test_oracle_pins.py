@@ -508,6 +508,42 @@ def test_rope_preserves_pair_norms():
     np.testing.assert_allclose(O.apply_rope(x, np.zeros((11, 32)), np.ones((11, 32))), O.rotate_half(x), rtol=0)
 
 
+def test_rope_rotates_basis_vectors_counterclockwise():
+    # Closed form of the half-split rotation by theta (channel i paired with
+    # channel i + d/2): e_0 -> cos(t) e_0 + sin(t) e_{d/2} and
+    # e_{d/2} -> -sin(t) e_0 + cos(t) e_{d/2}, i.e. (x1, x2) ->
+    # (x1 cos - x2 sin, x2 cos + x1 sin), the direction of x*cos + rotate_half(x)*sin.
+    d, t = 8, 0.3
+    cos, sin = np.full((1, d), math.cos(t)), np.full((1, d), math.sin(t))
+    for src, want in ((0, {0: math.cos(t), d // 2: math.sin(t)}),
+                      (d // 2, {0: -math.sin(t), d // 2: math.cos(t)})):
+        x = np.zeros((1, 1, 1, d))
+        x[..., src] = 1.0
+        expect = np.zeros(d)
+        for ch, val in want.items():
+            expect[ch] = val
+        np.testing.assert_allclose(O.apply_rope(x, cos, sin)[0, 0, 0], expect, rtol=0, atol=1e-15)
+
+
+def _check_rope_complex_rotation():
+    """Half-split RoPE equals multiplying z = x1 + i*x2 (first half real, second
+    half imaginary) by exp(i*theta) per channel pair: an identity of complex
+    arithmetic, computed here with numpy's complex multiply."""
+    rng = np.random.default_rng(31)
+    S, d = 7, 16
+    x = rng.standard_normal((1, S, 2, d))
+    theta = rng.uniform(-np.pi, np.pi, (S, d // 2))
+    cos = np.concatenate([np.cos(theta)] * 2, axis=1)
+    sin = np.concatenate([np.sin(theta)] * 2, axis=1)
+    w = (x[..., : d // 2] + 1j * x[..., d // 2:]) * np.exp(1j * theta)[None, :, None, :]
+    want = np.concatenate([w.real, w.imag], axis=-1)
+    return not np.allclose(O.apply_rope(x, cos, sin), want, rtol=0, atol=1e-12)
+
+
+def test_rope_equals_complex_multiplication():
+    assert not _check_rope_complex_rotation()
+
+
 def test_rope_scores_depend_on_relative_position_only():
     rng = np.random.default_rng(16)
     d = 64
@@ -723,6 +759,11 @@ FORWARD_MUTATIONS = [
     ("topk_lowest_index", "return np.sort(order[:k]).astype(np.int64)", "return order[:k].astype(np.int64)",
      _check_lists_ascending_and_golden),
     ("select_blocks", "hk = h // G ", "hk = h % Hkv ", _check_gqa_selection_equals_repeated_kv),
+    # rotation direction: rotate_half turned the other way, and the sin term subtracted
+    ("rotate_half", "return np.concatenate([-x[..., d // 2:], x[..., : d // 2]], axis=-1)",
+     "return np.concatenate([x[..., d // 2:], -x[..., : d // 2]], axis=-1)", _check_rope_complex_rotation),
+    ("apply_rope", "return x * c + rotate_half(x) * s", "return x * c - rotate_half(x) * s",
+     _check_rope_complex_rotation),
 ]
 
 

@@ -28,10 +28,12 @@ def _desc(t):
     return _lib.BsaTensor(t.data_ptr(), B, S, H, D, sb, ss, sh)
 
 
-def _noalloc(lib, q, k, cfg, lens, keep):
+def _noalloc(lib, q, k, cfg, lens, keep, idx=None, cnt=None):
     nQb, nKb = -(-q.shape[1] // cfg.block_q), -(-k.shape[1] // cfg.block_k)
-    idx = torch.full((q.shape[0], q.shape[2], nQb, nKb), -7, dtype=torch.int32, device="cuda")
-    cnt = torch.full((q.shape[0], q.shape[2], nQb), -7, dtype=torch.int32, device="cuda")
+    if idx is None:
+        idx = torch.full((q.shape[0], q.shape[2], nQb, nKb), -7, dtype=torch.int32, device="cuda")
+    if cnt is None:
+        cnt = torch.full((q.shape[0], q.shape[2], nQb), -7, dtype=torch.int32, device="cuda")
     qd, kd = _desc(q), _desc(k)
     keep_arr = (ctypes.c_float * len(keep))(*keep)
     lens_arr = (ctypes.c_int32 * len(lens))(*lens)
@@ -72,3 +74,25 @@ def test_noalloc_rejects_problems_above_the_static_scratch():
     st = lib.bsa_select_noalloc(ctypes.byref(q), ctypes.byref(k), 0, None, 64, 64, keep, 1, fake, fake, None)
     assert st == 2
     assert "static scratch" in lib.bsa_get_last_error().decode()
+
+
+def test_noalloc_call_allocates_no_device_memory():
+    """The defining property: once the first call on the device has looked up
+    the scratch address, a call with the caller's buffers changes neither
+    torch's allocator nor the device's free memory."""
+    bsa.build()
+    lib = _lib.load()
+    cfg = CONFIGS["small_gqa"]
+    inp = make_inputs(cfg, "cuda", pad_fill=float("nan"))
+    q, k = inp["q"], inp["k"]
+    idx, cnt = _noalloc(lib, q, k, cfg, inp["seq_lens"], inp["keep_ratio"])     # warm-up call
+    # buffers for the second call exist before the measurement starts
+    idx2, cnt2 = torch.full_like(idx, -7), torch.full_like(cnt, -7)
+    torch.cuda.synchronize()
+    allocated, free = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
+    _noalloc(lib, q, k, cfg, inp["seq_lens"], inp["keep_ratio"], idx=idx2, cnt=cnt2)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == allocated
+    assert torch.cuda.mem_get_info()[0] == free
+    bsa.bsa_device_status()
+    assert torch.equal(cnt2, cnt) and torch.equal(idx2, idx)
