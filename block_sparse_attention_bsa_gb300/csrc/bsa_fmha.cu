@@ -32,6 +32,7 @@
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "bsa_internal.h"
@@ -601,6 +602,521 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------ CTA pairs ---
+// The same attention for head dim 128, with one 256-row query block per
+// cluster of two CTAs (the two SMs of a TPC).  CTA rank r owns query rows
+// r*128 .. r*128+127 of the block, so both CTAs attend the block's one list.
+// One thread of the even CTA issues M = 256 tcgen05 MMAs (cta_group::2) for
+// both: S = Q K^T into each CTA's TMEM (128 lanes x 128 keys), O += P V with
+// P read from each CTA's TMEM.  B operands are split across the pair: for S
+// each CTA holds 64 of the tile's 128 keys (all 128 dims), for P V all 128
+// keys and 64 of the 128 value dims.  Per SM, an S MMA therefore reads 6 KB
+// of shared memory instead of 8 KB, and every key block costs 16 MMA
+// instructions for 256 rows instead of 32.  TMEM per CTA: two S buffers
+// (S of step j+1 is computed while the softmax works on step j) and O.
+//
+// Synchronisation across the pair (barriers at the same offsets in both
+// CTAs): the even CTA's producer takes work tiles from the global counter
+// and writes each id into both CTAs' tile rings (remote store, then a
+// cluster-scope release arrive; consumers acquire at cluster scope); each
+// CTA's producer loads its own halves with completion counted on the even
+// CTA's full barriers (TMA .cta_group::2); the MMA thread's commits are
+// multicast to both CTAs (S ready, a P V finished, stage and Q buffer free);
+// each softmax warp arrives once per step on the even CTA's P barrier.  The
+// per-step hand-offs carry TMEM or TMA data only, ordered by the tcgen05 and
+// transaction-count rules, so they use CTA-scope waits and a relaxed remote
+// arrive (a cluster-scope release costs ~1,000 cycles per step).
+constexpr int kPairSBufs = 3;   // S buffers of the CTA-pair kernel
+
+template <int NS>
+struct PairCfg {
+  static constexpr int D = 128;
+  static constexpr int kSBufs = NS;                 // S buffers in TMEM (128 columns each)
+  static constexpr int kQBytes = 128 * 128 * 2;     // 128 rows x 128 dims: two 64-dim chunks of 16 KB
+  static constexpr int kQBufs = 2;
+  static constexpr int kKBytes = 64 * 128 * 2;      // 64 keys x 128 dims: two chunks of 8 KB
+  static constexpr int kVBytes = 128 * 64 * 2;      // 128 keys x 64 dims: one chunk
+  static constexpr int kStageBytes = kKBytes + kVBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kAlignSlack = 1024;
+  static constexpr int kSmemMax = 232448;
+  static constexpr int kStagesFit = (kSmemMax - kQBufs * kQBytes - kBarBytes - kAlignSlack) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+  static constexpr int kSmemBytes = kQBufs * kQBytes + kStages * kStageBytes + kBarBytes + kAlignSlack;
+  static constexpr int kThreads = 256;              // warp 0 TMA, warp 1 MMA/TMEM, warps 4..7 softmax
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kOCol = 128 * NS;       // S buffers at 0, 128, ..., O after them
+  static constexpr int kTileEmptyCount = 10;        // MMA thread + 4 softmax warps + peer producer + 4 peer warps
+  static constexpr int kPFullCount = 8;             // 4 softmax warps per CTA
+  static_assert(kStages >= 3, "not enough shared memory for a K/V ring");
+  static_assert(NS >= 2 && 128 * NS + 128 <= 512, "TMEM columns");
+  static constexpr int kNumBars = 9 + 3 * NS + 2 * kStages;
+  static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier block");
+};
+
+template <int KB, int NS>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<NS>::kThreads, 1)
+    fmha_fwd_pair_kernel(const __grid_constant__ FmhaParams p) {
+  static_assert(KB == 128 || KB == 64, "key block");
+  using C = PairCfg<NS>;
+  constexpr int BK = 128;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* q_smem = smem;
+  uint8_t* kv_smem = smem + C::kQBufs * C::kQBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(kv_smem + S * C::kStageBytes);
+  uint64_t* q_full = bars + 0;             // [2] even CTA: both halves of a Q buffer landed
+  uint64_t* q_empty = bars + 2;            // [2] both: the tile's last S MMA finished
+  uint64_t* mma_done = bars + 4;           // both: the MMA thread's last commit (exit)
+  uint64_t* tile_full = bars + 5;          // [2] both: tile id published
+  uint64_t* tile_empty = bars + 7;         // [2] even CTA: every consumer of both CTAs read the id
+  uint64_t* s_full = bars + 9;             // [NS] both: S buffer b holds this step's scores
+  uint64_t* p_full = bars + 9 + NS;        // [NS] even CTA: P of S buffer b written by both CTAs
+  uint64_t* pv_done = bars + 9 + 2 * NS;   // [NS] both: the P V reading S buffer b finished
+  uint64_t* kv_full = bars + 9 + 3 * NS;   // [S] even CTA: both halves of a K/V stage landed
+  uint64_t* kv_empty = kv_full + S;        // [S] both: the stage's P V finished
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* tile_ids = reinterpret_cast<volatile int*>(tmem_slot + 2);   // [2]
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(q_full + i), 1);
+      mbar_init(smem_u32(q_empty + i), 1);
+      mbar_init(smem_u32(tile_full + i), 1);
+      mbar_init(smem_u32(tile_empty + i), C::kTileEmptyCount);
+    }
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(s_full + i), 1);
+      mbar_init(smem_u32(p_full + i), C::kPFullCount);
+      mbar_init(smem_u32(pv_done + i), 1);
+    }
+    mbar_init(smem_u32(mma_done), 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(smem_u32(kv_full + i), 1);
+      mbar_init(smem_u32(kv_empty + i), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < p.Bn; ++i) {
+      tma_prefetch_desc(&p.tq[i]);
+      tma_prefetch_desc(&p.tk[i]);
+      tma_prefetch_desc(&p.tv[i]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();   // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // shared::cluster addresses in the even CTA (or in the peer)
+  auto at_leader = [&](const void* x) { return cluster_addr(smem_u32(x), 0u); };
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer ---
+    Ring ring;
+    uint32_t qi = 0;
+    const uint32_t q_base = smem_u32(q_smem);
+    const uint32_t kv_base = smem_u32(kv_smem);
+    const uint64_t q_policy = l2_policy_evict_first();
+    bool ok = true;
+    TileRing tr;
+    while (ok) {
+      int t = -1;
+      if (lane == 0) {
+        if (leader) {
+          // take the next tile and publish its id in both CTAs' rings
+          t = atomicAdd(p.counter, 1);
+          if (t >= p.n_tiles) t = -1;
+          ok = mbar_wait_cl(smem_u32(tile_empty + tr.slot), tr.phase ^ 1u, abort_flag);
+          if (ok) {
+            tile_ids[tr.slot] = t;
+            st_cluster_u32(cluster_addr(smem_u32(const_cast<int*>(tile_ids + tr.slot)), 1u), (uint32_t)t);
+            mbar_arrive(smem_u32(tile_full + tr.slot));
+            mbar_arrive_remote(cluster_addr(smem_u32(tile_full + tr.slot), 1u));
+          }
+        } else {
+          ok = mbar_wait_cl(smem_u32(tile_full + tr.slot), tr.phase, abort_flag);
+          t = ok ? tile_ids[tr.slot] : -1;
+          if (ok) mbar_arrive_remote(at_leader(tile_empty + tr.slot));
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      tr.next();
+      if (!ok || t < 0) break;
+      const TileInfo ti = decode_tile(p, t, KB, BK);
+      if (ti.n == 0) continue;
+      if (lane == 0) {
+        const uint32_t qs = qi & 1u;
+        ok = mbar_wait(smem_u32(q_empty + qs), ((qi >> 1) & 1u) ^ 1u, abort_flag);
+        if (ok) {
+          if (leader) mbar_arrive_expect_tx(smem_u32(q_full + qs), 2 * C::kQBytes);
+          const uint32_t fb = at_leader(q_full + qs);
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d_pair_hint(q_base + qs * C::kQBytes + c * 16384, &p.tq[ti.bl], fb, c * 64,
+                                  ti.qb * p.block_q + (int)rank * 128, ti.h, q_policy);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ++qi;
+      for (int j0 = 0; j0 < ti.n && ok; j0 += 32) {
+        int my_kb = ti.idx ? (j0 + lane < ti.n ? __ldg(ti.idx + j0 + lane) : 0) : j0 + lane;
+        if (p.masked) my_kb &= kEntryBlockMask;
+        const int m = min(32, ti.n - j0);
+        for (int jj = 0; jj < m && ok; jj += BK / KB) {
+          int kb = __shfl_sync(0xffffffffu, my_kb, jj);
+          if (kb < 0 || kb >= p.nKb) kb = p.nKb;   // out of range: rows past the end read zeros
+          int kb1 = p.nKb;                          // second 64-key block of the tile
+          if constexpr (KB < BK) {
+            const int t1 = __shfl_sync(0xffffffffu, my_kb, (jj + 1) & 31);
+            if (jj + 1 < m && t1 >= 0 && t1 < p.nKb) kb1 = t1;
+          }
+          if (lane == 0) {
+            ok = mbar_wait(smem_u32(kv_empty + ring.stage), ring.phase ^ 1u, abort_flag);
+            if (ok) {
+              if (leader) mbar_arrive_expect_tx(smem_u32(kv_full + ring.stage), 2 * C::kStageBytes);
+              const uint32_t fb = at_leader(kv_full + ring.stage);
+              const uint32_t kd = kv_base + ring.stage * C::kStageBytes;
+              const uint32_t vd = kd + C::kKBytes;
+              // K: this CTA's 64 keys of the tile, all 128 dims (two chunks)
+              const int krow = KB == BK ? kb * BK + (int)rank * 64 : (rank == 0 ? kb : kb1) * KB;
+              for (int c = 0; c < 2; ++c) tma_load_3d_pair(kd + c * 8192, &p.tk[ti.bl], fb, c * 64, krow, ti.hk);
+              // V: all 128 keys of the tile, this CTA's 64 dims
+              if constexpr (KB == BK) {
+                tma_load_3d_pair(vd, &p.tv[ti.bl], fb, (int)rank * 64, kb * BK, ti.hk);
+              } else {
+                tma_load_3d_pair(vd, &p.tv[ti.bl], fb, (int)rank * 64, kb * KB, ti.hk);
+                tma_load_3d_pair(vd + KB * 128, &p.tv[ti.bl], fb, (int)rank * 64, kb1 * KB, ti.hk);
+              }
+              ring.next<S>();
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+      }
+    }
+    __syncwarp();
+    // On an abort, copies of this CTA may still be in flight: give them time
+    // to land (they complete in microseconds) before the CTA can exit.
+    if (*abort_flag && lane == 0) {
+      const unsigned long long t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 20000000ull) {
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer ---
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(256, BK, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(256, C::D, true);
+      const uint64_t qdesc0 = sdesc_sw128(smem_u32(q_smem), 16, 1024);
+      const uint64_t kdesc0 = sdesc_sw128(smem_u32(kv_smem), 16, 1024);
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(kv_smem) + C::kKBytes, 16, 1024);
+      constexpr uint16_t kBoth = 3;
+      // S_b = Q_qs K_stage^T (K = 128 dims in 8 steps of 16)
+      auto issue_s = [&](uint32_t qs, uint32_t b, uint32_t stage) {
+        const uint32_t d_t = tmem + b * 128;
+        const uint64_t a0 = qdesc0 + (uint64_t)((qs * C::kQBytes) >> 4);
+        const uint64_t b0 = kdesc0 + (uint64_t)((stage * C::kStageBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < C::D / 16; ++kk) {
+          const uint64_t a = a0 + (uint64_t)((kk / 4) * (16384 >> 4) + (kk % 4) * 2);
+          const uint64_t bb = b0 + (uint64_t)((kk / 4) * (8192 >> 4) + (kk % 4) * 2);
+          if (kk == 0) mma2_ss_acc<0>(d_t, a, bb, idesc_s);
+          else mma2_ss_acc<1>(d_t, a, bb, idesc_s);
+        }
+      };
+      // O += P_b V_stage (K = 128 keys in 8 steps of 16; P bf16 packed in S_b)
+      auto issue_pv = [&](uint32_t b, uint32_t stage, bool acc) {
+        const uint32_t d_t = tmem + C::kOCol;
+        const uint32_t a_t = tmem + b * 128;
+        const uint64_t bs = vdesc0 + (uint64_t)((stage * C::kStageBytes) >> 4);
+        if (acc) mma2_ts_acc<1>(d_t, a_t, bs, idesc_o);
+        else mma2_ts_acc<0>(d_t, a_t, bs, idesc_o);
+#pragma unroll
+        for (int kk = 1; kk < BK / 16; ++kk)
+          mma2_ts_acc<1>(d_t, a_t + kk * 8, bs + (uint64_t)(kk * ((16 * 128) >> 4)), idesc_o);
+      };
+      Ring ring;
+      uint32_t qi = 0;
+      uint32_t b0 = 0;                  // S buffer of the next step (steps rotate over the NS buffers)
+      // Per-buffer state packed in registers (runtime-indexed arrays would
+      // live in local memory, on the issue path): bit b of pph = phase of
+      // p_full[b] to wait for; bits 4b..4b+3 of st_of = K/V stage of the
+      // step whose S sits in buffer b.
+      uint32_t pph = 0u, st_of = 0u;
+      static_assert(S <= 16 && NS <= 8, "packed per-buffer state");
+      auto stage_of = [&](uint32_t b) { return (st_of >> (4u * b)) & 15u; };
+      auto set_stage = [&](uint32_t b, uint32_t st) { st_of = (st_of & ~(15u << (4u * b))) | (st << (4u * b)); };
+      bool ok = true;
+      TileRing tr;
+      auto next_buf = [](uint32_t b) { return b + 1 == (uint32_t)NS ? 0u : b + 1; };
+      while (ok) {
+        ok = mbar_wait_cl(smem_u32(tile_full + tr.slot), tr.phase, abort_flag);
+        const int t = ok ? tile_ids[tr.slot] : -1;
+        if (ok) mbar_arrive(smem_u32(tile_empty + tr.slot));
+        tr.next();
+        if (t < 0) break;
+        const TileInfo ti = decode_tile(p, t, KB, BK);
+        const int n = ti.steps;
+        if (n == 0) continue;
+        const uint32_t qs = qi & 1u;
+        ok = mbar_wait(smem_u32(q_full + qs), (qi >> 1) & 1u, abort_flag);
+        ++qi;
+        if (!ok) break;
+        // S of the first min(n, NS) steps, one per buffer
+        uint32_t bs = b0;
+        for (int j = 0; j < n && j < NS && ok; ++j) {
+          const uint32_t st = ring.stage;
+          set_stage(bs, st);
+          ok = mbar_wait(smem_u32(kv_full + st), ring.phase, abort_flag);
+          ring.next<S>();
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(qs, bs, st);
+          mma2_commit_mc(smem_u32(s_full + bs), kBoth);
+          bs = next_buf(bs);
+        }
+        if (!ok) break;
+        if (n <= NS) mma2_commit_mc(smem_u32(q_empty + qs), kBoth);
+        uint32_t b = b0;
+        for (int j = 0; j < n && ok; ++j) {
+          ok = mbar_wait(smem_u32(p_full + b), (pph >> b) & 1u, abort_flag);
+          pph ^= 1u << b;
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t stj = stage_of(b);
+          issue_pv(b, stj, j > 0);
+          mma2_commit_mc(smem_u32(pv_done + b), kBoth);
+          mma2_commit_mc(smem_u32(kv_empty + stj), kBoth);
+          if (j + NS < n) {
+            // S of step j + NS into the buffer P V (j) just read (MMAs run in order)
+            const uint32_t st = ring.stage;
+            set_stage(b, st);
+            ok = mbar_wait(smem_u32(kv_full + st), ring.phase, abort_flag);
+            ring.next<S>();
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(qs, b, st);
+            mma2_commit_mc(smem_u32(s_full + b), kBoth);
+            if (j + NS + 1 == n) mma2_commit_mc(smem_u32(q_empty + qs), kBoth);
+          }
+          b = next_buf(b);
+        }
+        b0 = b;
+      }
+      // every MMA issued has finished before either CTA frees its TMEM
+      mma2_commit_mc(smem_u32(mma_done), kBoth);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_drain_cl(smem_u32(mma_done), 0u, kWaitTimeoutNs);
+    __syncwarp();
+  } else if (warp >= 4) {
+    // --------------------------------------------------- softmax + epilogue ---
+    const int wq = warp - 4;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t o_t = tmem + lane_base + C::kOCol;
+    const uint32_t p_full_cl0 = at_leader(p_full);   // p_full + b at p_full_cl0 + 8 b
+    const uint32_t tile_empty_cl[2] = {at_leader(tile_empty), at_leader(tile_empty + 1)};
+    uint32_t b = 0;                   // S buffer of the next step
+    // Bit b of sph: phase of s_full[b] to wait for next.  Bit b of pvph:
+    // parity of the phase of pv_done[b] that the next P V on buffer b will
+    // complete (it flips when this thread hands a P of buffer b over).  Waiting for the
+    // P V of the previous step, on buffer bp, is unambiguous whenever it is
+    // needed: the one before it on bp finished before S(this step) was
+    // computed, and the one after it needs a P this thread has not made.
+    // bit b of sph / pvph (packed in registers, not runtime-indexed arrays)
+    uint32_t sph = 0u, pvph = 0u;
+    bool ok = true;
+    TileRing tr;
+    while (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait_cl(smem_u32(tile_full + tr.slot), tr.phase, abort_flag));
+      const int t = ok ? tile_ids[tr.slot] : -1;
+      __syncwarp();
+      if (ok && lane == 0) {
+        if (leader) mbar_arrive(smem_u32(tile_empty + tr.slot));
+        else mbar_arrive_remote(tile_empty_cl[tr.slot]);
+      }
+      tr.next();
+      if (t < 0) break;
+      const TileInfo ti = decode_tile(p, t, KB, BK);
+      const int row_in_blk = (int)rank * 128 + r;
+      const int row = ti.qb * p.block_q + row_in_blk;
+      const bool row_exists = row_in_blk < p.block_q && row < p.Sq;
+      const bool row_ok = row_exists && row < ti.L;
+      __nv_bfloat16* orow = p.out + (((int64_t)ti.b * p.Sq + row) * p.Hq + ti.h) * C::D;
+      float* lrow = p.lse ? p.lse + ((int64_t)ti.b * p.Hq + ti.h) * p.Sq + row : nullptr;
+      if (ti.n == 0) {
+        if (row_exists) {
+          uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int i = 0; i < C::D / 8; ++i) reinterpret_cast<uint4*>(orow)[i] = z;
+          if (lrow) *lrow = -INFINITY;
+        }
+        continue;
+      }
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      auto entry_block = [&](int e) {
+        if (e >= ti.n) return p.nKb;
+        const int entry = ti.idx ? __ldg(ti.idx + e) : e;
+        int kb = (ti.idx && p.masked) ? (entry & kEntryBlockMask) : entry;
+        if (kb < 0 || kb >= p.nKb) kb = p.nKb;
+        if (p.masked && !((entry >> (kEntryGroupShift + row_in_blk / p.group_rows)) & 1)) kb = p.nKb;
+        return kb;
+      };
+      for (int j = 0; j < ti.steps; ++j, b = b + 1 == (uint32_t)NS ? 0u : b + 1) {
+        const uint32_t s_t = tmem + lane_base + b * 128;
+        const int kb = entry_block(KB < BK ? 2 * j : j);
+        const int kb1 = KB < BK ? entry_block(2 * j + 1) : 0;
+        const int kv_end = p.causal ? min(ti.valid_kv, row + 1) : ti.valid_kv;
+        int kvalid0 = BK, kvalid1 = BK;
+        bool skip0 = false, skip1 = false;
+        if constexpr (KB < BK) {
+          kvalid0 = kv_end - kb * KB;
+          kvalid1 = kv_end - kb1 * KB;
+          skip0 = kvalid0 <= 0;
+          skip1 = kvalid1 <= 0;
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(s_full + b), (sph >> b) & 1u, abort_flag));
+        sph ^= 1u << b;
+        if (!ok) break;
+        tc_fence_after();
+        float sv[BK];
+#pragma unroll
+        for (int c = 0; c < BK / 32; ++c) tmem_ld32f(s_t + c * 32, sv + c * 32);
+        tmem_wait_ld();
+        float mx;
+        if constexpr (KB == BK) {
+          const int kvalid = kv_end - kb * BK;
+          if (kvalid < BK) {
+#pragma unroll
+            for (int c = 0; c < BK; ++c)
+              if (c >= kvalid) sv[c] = -INFINITY;
+          }
+          mx = row_max<0, BK>(sv);
+        } else {
+          if ((!skip0 && kvalid0 < KB) || (!skip1 && kvalid1 < KB)) {
+#pragma unroll
+            for (int c = 0; c < KB; ++c) {
+              if (c >= kvalid0) sv[c] = -INFINITY;
+              if (c >= kvalid1) sv[KB + c] = -INFINITY;
+            }
+          }
+          const float mx_lo = skip0 ? -INFINITY : row_max<0, KB>(sv);
+          const float mx_hi = skip1 ? -INFINITY : row_max<KB, KB>(sv);
+          mx = fmaxf(mx_lo, mx_hi);
+        }
+        const float m_new = fmaxf(m_ref, mx * p.scale_log2);
+        const bool grow = m_new > m_ref + 8.0f;
+        const bool rescale_o = grow && m_ref != -INFINITY;
+        const float alpha = rescale_o ? ex2_approx(m_ref - m_new) : 1.f;
+        if (grow) m_ref = m_new;
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nm2 = make_float2(-m_use, -m_use);
+        float2 ls0 = make_float2(0.f, 0.f), ls1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int cc = 0; cc < BK / 64; ++cc) {
+          uint32_t pk[32];
+          if constexpr (KB < BK) {
+            if (cc == 0 ? skip0 : skip1) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) pk[i] = 0u;
+              tmem_st32(s_t + cc * 32, pk);
+              continue;
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            const float2 a = __ffma2_rn(make_float2(sv[cc * 64 + c], sv[cc * 64 + c + 1]), sc2, nm2);
+            const float2 bq = __ffma2_rn(make_float2(sv[cc * 64 + c + 2], sv[cc * 64 + c + 3]), sc2, nm2);
+            const float2 e0 = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+            const float2 e1 = make_float2(ex2_approx(bq.x), ex2_approx(bq.y));
+            ls0 = __fadd2_rn(ls0, e0);
+            ls1 = __fadd2_rn(ls1, e1);
+            pk[c / 2] = pack_bf16x2(e0.x, e0.y);
+            pk[c / 2 + 1] = pack_bf16x2(e1.x, e1.y);
+          }
+          tmem_st32(s_t + cc * 32, pk);
+        }
+        const float lsum = (ls0.x + ls0.y) + (ls1.x + ls1.y);
+        l = l * alpha + lsum;
+        // O is rescaled (rare) only after the P V of the previous step finished.
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          const uint32_t bp = b == 0 ? (uint32_t)NS - 1 : b - 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(pv_done + bp), ((pvph >> bp) & 1u) ^ 1u, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < C::D / 32; ++c) {
+            float o[32];
+            tmem_ld32f(o_t + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32f(o_t + c * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(smem_u32(p_full + b));
+          else mbar_arrive_remote_relaxed(p_full_cl0 + 8u * b);
+        }
+        pvph ^= 1u << b;
+      }
+      if (!ok) break;
+      {  // the tile's last P V (on the buffer before b)
+        const uint32_t bl = b == 0 ? (uint32_t)NS - 1 : b - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(pv_done + bl), ((pvph >> bl) & 1u) ^ 1u, abort_flag));
+      }
+      if (!ok) break;
+      tc_fence_after();
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < C::D / 32; ++c) {
+        float o[32];
+        tmem_ld32f(o_t + c * 32, o);
+        tmem_wait_ld();
+        if (row_exists) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = row_ok ? pack_bf16x2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l) : 0u;
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (row_exists && lrow)
+        *lrow = (row_ok && l > 0.f) ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      tc_fence_before();
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();   // no arrival, store or MMA of either CTA targets the other after this
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------- scheduling ---
 // One CTA: total selected work of every (request, KV head) group (query rows
 // x listed blocks, summed over the group's query heads and query blocks),
@@ -733,6 +1249,96 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
   return BSA_OK;
 }
 
+// CTA-pair launch: the same per-chunk parameters, tensor maps whose K box is
+// 64 rows (each CTA loads half of a key tile) and a grid of as many 2-CTA
+// clusters as can be resident at once.
+template <int KB, int NS>
+bsa_status launch_pair(const ForwardArgs& a, cudaStream_t stream) {
+  using C = PairCfg<NS>;
+  static std::atomic<int> clusters[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  bsa_status st;
+  int max_clusters = dev < 64 ? clusters[dev].load(std::memory_order_acquire) : 0;
+  if (max_clusters <= 0) {
+    if ((st = cuda_check(cudaFuncSetAttribute(fmha_fwd_pair_kernel<KB, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              C::kSmemBytes),
+                         "cudaFuncSetAttribute(fmha_fwd_pair_kernel)")) != BSA_OK)
+      return st;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (unsigned)(num_sms() / 2), 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if ((st = cuda_check(cudaOccupancyMaxActiveClusters(&max_clusters, fmha_fwd_pair_kernel<KB, NS>, &cfg),
+                         "cudaOccupancyMaxActiveClusters(fmha_fwd_pair_kernel)")) != BSA_OK)
+      return st;
+    if (max_clusters <= 0) return set_error(BSA_ERR_UNSUPPORTED, "bsa_forward: no CTA pair fits on this device");
+    if (dev < 64) clusters[dev].store(max_clusters, std::memory_order_release);
+  }
+  for (int b0 = 0; b0 < a.B; b0 += kMaxFwdBatch) {
+    const int Bn = std::min(kMaxFwdBatch, a.B - b0);
+    FmhaParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int i = 0; i < Bn; ++i) {
+      const int b = b0 + i;
+      const int L = a.seq_lens ? a.seq_lens[b] : a.Sq;
+      p.seq_lens[i] = L;
+      const char* qb = static_cast<const char*>(a.q) + (int64_t)b * a.q_sb * 2;
+      const char* kb = static_cast<const char*>(a.k) + (int64_t)b * a.k_sb * 2;
+      const char* vb = static_cast<const char*>(a.v) + (int64_t)b * a.v_sb * 2;
+      if ((st = encode_tensor_map(&p.tq[i], qb, L, a.Hq, 128, a.q_ss, a.q_sh, 128, "Q")) != BSA_OK) return st;
+      if ((st = encode_tensor_map(&p.tk[i], kb, a.prefix_len + L, a.Hkv, 128, a.k_ss, a.k_sh, 64, "K")) != BSA_OK)
+        return st;
+      if ((st = encode_tensor_map(&p.tv[i], vb, a.prefix_len + L, a.Hkv, 128, a.v_ss, a.v_sh, KB, "V")) != BSA_OK)
+        return st;
+    }
+    p.b0 = b0;
+    p.Bn = Bn;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = a.Hq / a.Hkv;
+    p.Sq = a.Sq;
+    p.nQb = a.nQb;
+    p.nKb = a.nKb;
+    p.block_q = a.block_q;
+    p.prefix_len = a.prefix_len;
+    p.n_tiles = Bn * a.nQb * a.Hq;
+    p.indices = a.indices;
+    p.counts = a.counts;
+    p.causal = a.causal ? 1 : 0;
+    p.masked = a.masked ? 1 : 0;
+    p.group_rows = a.group_rows > 0 ? a.group_rows : a.block_q;
+    char* cws = static_cast<char*>(a.workspace) + (size_t)(b0 / kMaxFwdBatch) * forward_chunk_bytes(a.Hq);
+    p.counter = reinterpret_cast<int*>(cws);
+    p.group_order = reinterpret_cast<const int*>(cws + 256);
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.lse = a.lse;
+    const int n_clusters = std::min(p.n_tiles, max_clusters);
+    if (n_clusters <= 0) continue;
+    ScheduleParams sp{};
+    sp.counts = a.indices ? a.counts : nullptr;
+    sp.causal = a.causal ? 1 : 0;
+    sp.b0 = b0; sp.Bn = Bn; sp.Hq = a.Hq; sp.Hkv = a.Hkv; sp.G = a.Hq / a.Hkv;
+    sp.nQb = a.nQb; sp.nKb = a.nKb; sp.block_q = a.block_q; sp.block_k = KB; sp.prefix_len = a.prefix_len;
+    for (int i = 0; i < Bn; ++i) sp.seq_lens[i] = p.seq_lens[i];
+    sp.counter = p.counter;
+    sp.order = const_cast<int*>(p.group_order);
+    schedule_kernel<<<1, 1024, 0, stream>>>(sp);
+    if ((st = cuda_check(cudaGetLastError(), "schedule_kernel launch")) != BSA_OK) return st;
+    fmha_fwd_pair_kernel<KB, NS><<<2 * n_clusters, C::kThreads, C::kSmemBytes, stream>>>(p);
+    if ((st = cuda_check(cudaGetLastError(), "fmha_fwd_pair_kernel launch")) != BSA_OK) return st;
+  }
+  return BSA_OK;
+}
+
 }  // namespace
 
 size_t forward_chunk_bytes(int Hq) {
@@ -841,6 +1447,14 @@ bsa_status launch_forward(const ForwardArgs& a_in, cudaStream_t stream) {
     a.group_rows = a.block_q;
     a.block_q = 256;
     a.nQb = nSb;
+  }
+  static const bool pair = [] {
+    const char* e = std::getenv("BSA_FWD_PAIR");
+    return e && *e && std::strcmp(e, "0") != 0;
+  }();
+  if (pair) {
+    if (a.d == 128 && a.block_k == 128) return launch_pair<128, kPairSBufs>(a, stream);
+    if (a.d == 128 && a.block_k == 64) return launch_pair<64, kPairSBufs>(a, stream);
   }
   if (a.d == 128 && a.block_k == 128) return launch_t<128, 128, 2>(a, stream);
   if (a.d == 128 && a.block_k == 64) return launch_t<128, 128, 2, 64>(a, stream);   // paired 64-key blocks

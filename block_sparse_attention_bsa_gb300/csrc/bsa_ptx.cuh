@@ -310,6 +310,160 @@ __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* r) {
       : "memory");
 }
 
+// ------------------------------------------------- CTA pairs (clusters of 2) ---
+// A cluster of two CTAs on the two SMs of a TPC runs one M = 256 MMA per
+// instruction (cta_group::2): each CTA holds 128 rows of A and of the
+// accumulator, and half of B's N columns, at the same shared-memory and TMEM
+// offsets.  The even CTA of the pair issues the MMAs for both.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address, in the shared::cluster window, of the variable at shared::cta
+// address `addr` in the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of any CTA of the cluster (release at cluster scope:
+// the caller's earlier memory operations are visible to a cluster-scope
+// acquire of the completed phase).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
+}
+
+// Remote arrive without a memory-model release (no cluster-scope fence).
+// Enough where the only data handed over lives in TMEM: its writes are
+// ordered by tcgen05.wait::st and tcgen05.fence::before_thread_sync, which
+// the caller executes first.  A cluster-scope release costs ~1,000 cycles.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t cl_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cl_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait with cluster-scope acquire (phases completed by the peer CTA's
+// arrivals or by multicast commits).  Same limit and abort handling.
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort,
+                                             unsigned long long limit_ns = kWaitTimeoutNs) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        atomicOr(&g_bsa_error, kErrTimeout);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait on the way out (ignores the abort flag, like mbar_drain).
+__device__ __forceinline__ void mbar_drain_cl(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  if (mbar_try_wait_cl(bar, parity)) return;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait_cl(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) {
+      atomicOr(&g_bsa_error, kErrTimeout);
+      return;
+    }
+  }
+}
+
+// All threads of both CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMA tile load into this CTA's shared memory whose completion (transaction
+// bytes) is signalled on an mbarrier of this CTA or of its pair peer
+// (`bar_cl` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap, uint32_t bar_cl,
+                                                 int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cl), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void* tmap, uint32_t bar_cl,
+                                                      int32_t c0, int32_t c1, int32_t c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cl), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
+// TMEM allocation for a CTA pair: one warp of each CTA executes it; both get
+// the same columns.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// M = 256 MMAs over the pair, issued by one thread of the even CTA.
+template <int ACC>
+__device__ __forceinline__ void mma2_ss_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+
+template <int ACC>
+__device__ __forceinline__ void mma2_ts_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at shared::cta address `bar` of every CTA in
+// `cta_mask` when all pair MMAs this thread issued so far have completed.
+__device__ __forceinline__ void mma2_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // ------------------------------------------------------------ descriptors ---
 
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B and fp32 D.
