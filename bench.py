@@ -911,7 +911,7 @@ def main():
             "tile_sparsity": tile_sparsity,
             "exact_pair_tflop_per_step": exact_flops / 1e12,
             "effective_tflop_per_step": flops / 1e12,
-            "roofline": {"bound": "tensor", "kernel": "fmha_fwd_kernel<128,128,2>", "achieved": fwd_tflops,
+            "roofline": {"bound": "tensor", "kernel": "fmha_fwd_pair_kernel<128,3>", "achieved": fwd_tflops,
                          "peak": pk["bf16"], "unit": "TFLOP/s", "frac": fwd_tflops / pk["bf16"],
                          "peak_source": f"{pk['source']} bf16 burst (of measured)",
                          "traffic": traffic, "traffic_source": traffic_src,

@@ -6,24 +6,30 @@
 // protected prefix, suffix padding masked, no dense fallback) and by
 // cosmos_parallel.py (cosmos3_cp_attention: non-causal attention of
 // generation queries over cat(und, gen); build_gen_key_mask: padded keys
-// never contribute).  The FA4 kernel the pages run is prior art; this is a
-// fresh design for GB300:
+// never contribute).  The FA4 kernel the pages run is prior art; these are
+// fresh designs for GB300.  Two kernels share the work-tile scheduler and the
+// softmax/epilogue arithmetic:
 //
-//  * Persistent CTAs (one per SM) walk work tiles (b, query block, head),
-//    heads innermost so GQA siblings run together and share K/V in L2.
-//  * Warp 0 is the TMA producer: Q tile once per work tile, then K and V
-//    tiles of the listed blocks, gathered by index (row = index * block_k),
-//    into a ring of shared-memory stages.  Per-request tensor maps bound the
-//    rows at prefix + L_b, so padded keys/values load as zeros.
-//  * Warp 1 issues tcgen05.mma (one thread): S_h = Q_h K^T into TMEM for
-//    each 128-row half h of the query block, then O_h += P_h V with P_h read
-//    from TMEM (bf16, written over S_h by the softmax), ping-ponging the two
-//    halves so one half's softmax overlaps the other half's MMAs.
-//  * Warps 4.. are one softmax warpgroup per half: thread r owns query row r
-//    (TMEM lane r): tcgen05.ld of its S row, key mask, online softmax in the
-//    log2 domain with a lazy rescale (O is rescaled in TMEM only when the
-//    running max grows by more than 2^8), P back to TMEM, and the epilogue
-//    (O / l to bf16, LSE = ln-sum-exp of the scaled logits).
+//  * fmha_fwd_pair_kernel (head dim 128): a cluster of two CTAs on the two
+//    SMs of a TPC attends one 256-row query block, 128 rows per CTA, with
+//    M = 256 MMAs (cta_group::2) issued by two threads of the even CTA (one
+//    for S = Q K^T, one for O += P V).  See the comment above the kernel.
+//  * fmha_fwd_kernel (head dim 64): one persistent CTA per SM and 256-row
+//    query block, the two 128-row halves ping-ponged by one MMA thread.
+//
+// Common to both:
+//  * Persistent CTAs walk work tiles (b, query block, head) in (request, KV
+//    head) groups, GQA siblings innermost, so the running CTAs share one KV
+//    head's K/V in L2.
+//  * Warp 0 is the TMA producer: Q once per work tile, then K and V tiles of
+//    the listed blocks, gathered by index (row = index * block_k), into a
+//    ring of shared-memory stages.  Per-request tensor maps bound the rows at
+//    prefix + L_b, so padded keys/values load as zeros.
+//  * Softmax warps: thread r owns query row r (TMEM lane r): tcgen05.ld of
+//    its S row, key mask, online softmax in the log2 domain with a lazy
+//    rescale (O is rescaled in TMEM only when the running max grows by more
+//    than 2^8), P (bf16) back to TMEM over S, and the epilogue (O / l to
+//    bf16, LSE = ln-sum-exp of the scaled logits).
 //  * Every mbarrier wait is bounded (see mbar_wait); a CTA that gives up
 //    raises the device error word, leaves its loops and frees its TMEM.
 #include <cuda_bf16.h>
@@ -32,7 +38,6 @@
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 
 #include "bsa_internal.h"
@@ -631,7 +636,6 @@ constexpr int kPairSBufs = 3;   // S buffers of the CTA-pair kernel
 template <int NS>
 struct PairCfg {
   static constexpr int D = 128;
-  static constexpr int kSBufs = NS;                 // S buffers in TMEM (128 columns each)
   static constexpr int kQBytes = 128 * 128 * 2;     // 128 rows x 128 dims: two 64-dim chunks of 16 KB
   static constexpr int kQBufs = 2;
   static constexpr int kKBytes = 64 * 128 * 2;      // 64 keys x 128 dims: two chunks of 8 KB
@@ -643,10 +647,10 @@ struct PairCfg {
   static constexpr int kStagesFit = (kSmemMax - kQBufs * kQBytes - kBarBytes - kAlignSlack) / kStageBytes;
   static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
   static constexpr int kSmemBytes = kQBufs * kQBytes + kStages * kStageBytes + kBarBytes + kAlignSlack;
-  static constexpr int kThreads = 256;              // warp 0 TMA, warp 1 MMA/TMEM, warps 4..7 softmax
+  static constexpr int kThreads = 256;              // warp 0 TMA, warp 1 S MMAs + TMEM, warp 2 P V MMAs, warps 4..7 softmax
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOCol = 128 * NS;       // S buffers at 0, 128, ..., O after them
-  static constexpr int kTileEmptyCount = 10;        // MMA thread + 4 softmax warps + peer producer + 4 peer warps
+  static constexpr int kTileEmptyCount = 11;        // 2 MMA threads + 4 softmax warps + peer producer + 4 peer warps
   static constexpr int kPFullCount = 8;             // 4 softmax warps per CTA
   static_assert(kStages >= 3, "not enough shared memory for a K/V ring");
   static_assert(NS >= 2 && 128 * NS + 128 <= 512, "TMEM columns");
@@ -669,7 +673,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<NS>::kThread
   uint64_t* bars = reinterpret_cast<uint64_t*>(kv_smem + S * C::kStageBytes);
   uint64_t* q_full = bars + 0;             // [2] even CTA: both halves of a Q buffer landed
   uint64_t* q_empty = bars + 2;            // [2] both: the tile's last S MMA finished
-  uint64_t* mma_done = bars + 4;           // both: the MMA thread's last commit (exit)
+  uint64_t* mma_done = bars + 4;           // both: the MMA threads' last commits (exit)
   uint64_t* tile_full = bars + 5;          // [2] both: tile id published
   uint64_t* tile_empty = bars + 7;         // [2] even CTA: every consumer of both CTAs read the id
   uint64_t* s_full = bars + 9;             // [NS] both: S buffer b holds this step's scores
@@ -698,7 +702,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<NS>::kThread
       mbar_init(smem_u32(p_full + i), C::kPFullCount);
       mbar_init(smem_u32(pv_done + i), 1);
     }
-    mbar_init(smem_u32(mma_done), 1);
+    mbar_init(smem_u32(mma_done), 2);
     for (int i = 0; i < S; ++i) {
       mbar_init(smem_u32(kv_full + i), 1);
       mbar_init(smem_u32(kv_empty + i), 1);
@@ -817,8 +821,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<NS>::kThread
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------- MMA issuer ---
+  } else if (warp == 1 || warp == 2) {
+    // ----------------------------------------------------- MMA issuers ---
+    // Two threads of the even CTA issue the pair's MMAs: warp 1 the S MMAs,
+    // warp 2 the P V MMAs.  Each one's barrier waits and commits overlap the
+    // other's MMAs, so the tensor pipe is fed while one of them waits.  They
+    // follow the same step, buffer and K/V stage rotation; their
+    // dependencies go through barriers: S into buffer b waits for the P V
+    // that last read b (pv_done[b]); P V (j) waits for P (j), which implies
+    // S (j), and so K/V (j), complete.
     if (leader && lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(256, BK, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(256, C::D, true);
@@ -826,44 +837,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<NS>::kThread
       const uint64_t kdesc0 = sdesc_sw128(smem_u32(kv_smem), 16, 1024);
       const uint64_t vdesc0 = sdesc_sw128(smem_u32(kv_smem) + C::kKBytes, 16, 1024);
       constexpr uint16_t kBoth = 3;
-      // S_b = Q_qs K_stage^T (K = 128 dims in 8 steps of 16)
-      auto issue_s = [&](uint32_t qs, uint32_t b, uint32_t stage) {
-        const uint32_t d_t = tmem + b * 128;
-        const uint64_t a0 = qdesc0 + (uint64_t)((qs * C::kQBytes) >> 4);
-        const uint64_t b0 = kdesc0 + (uint64_t)((stage * C::kStageBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < C::D / 16; ++kk) {
-          const uint64_t a = a0 + (uint64_t)((kk / 4) * (16384 >> 4) + (kk % 4) * 2);
-          const uint64_t bb = b0 + (uint64_t)((kk / 4) * (8192 >> 4) + (kk % 4) * 2);
-          if (kk == 0) mma2_ss_acc<0>(d_t, a, bb, idesc_s);
-          else mma2_ss_acc<1>(d_t, a, bb, idesc_s);
-        }
-      };
-      // O += P_b V_stage (K = 128 keys in 8 steps of 16; P bf16 packed in S_b)
-      auto issue_pv = [&](uint32_t b, uint32_t stage, bool acc) {
-        const uint32_t d_t = tmem + C::kOCol;
-        const uint32_t a_t = tmem + b * 128;
-        const uint64_t bs = vdesc0 + (uint64_t)((stage * C::kStageBytes) >> 4);
-        if (acc) mma2_ts_acc<1>(d_t, a_t, bs, idesc_o);
-        else mma2_ts_acc<0>(d_t, a_t, bs, idesc_o);
-#pragma unroll
-        for (int kk = 1; kk < BK / 16; ++kk)
-          mma2_ts_acc<1>(d_t, a_t + kk * 8, bs + (uint64_t)(kk * ((16 * 128) >> 4)), idesc_o);
-      };
+      const bool s_role = warp == 1;
       Ring ring;
       uint32_t qi = 0;
-      uint32_t b0 = 0;                  // S buffer of the next step (steps rotate over the NS buffers)
-      // Per-buffer state packed in registers (runtime-indexed arrays would
-      // live in local memory, on the issue path): bit b of pph = phase of
-      // p_full[b] to wait for; bits 4b..4b+3 of st_of = K/V stage of the
-      // step whose S sits in buffer b.
-      uint32_t pph = 0u, st_of = 0u;
-      static_assert(S <= 16 && NS <= 8, "packed per-buffer state");
-      auto stage_of = [&](uint32_t b) { return (st_of >> (4u * b)) & 15u; };
-      auto set_stage = [&](uint32_t b, uint32_t st) { st_of = (st_of & ~(15u << (4u * b))) | (st << (4u * b)); };
+      uint32_t b = 0;                   // S buffer of the next step (steps rotate over the NS buffers)
+      // Per-buffer phase bits packed in registers: bit b of ph = parity of
+      // the next phase to wait for (p_full[b] for the P V thread; pv_done[b]
+      // for the S thread); bit b of used = buffer b has held an S before.
+      uint32_t ph = 0u, used = 0u;
       bool ok = true;
       TileRing tr;
-      auto next_buf = [](uint32_t b) { return b + 1 == (uint32_t)NS ? 0u : b + 1; };
       while (ok) {
         ok = mbar_wait_cl(smem_u32(tile_full + tr.slot), tr.phase, abort_flag);
         const int t = ok ? tile_ids[tr.slot] : -1;
@@ -873,56 +856,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<NS>::kThread
         const TileInfo ti = decode_tile(p, t, KB, BK);
         const int n = ti.steps;
         if (n == 0) continue;
-        const uint32_t qs = qi & 1u;
-        ok = mbar_wait(smem_u32(q_full + qs), (qi >> 1) & 1u, abort_flag);
-        ++qi;
-        if (!ok) break;
-        // S of the first min(n, NS) steps, one per buffer
-        uint32_t bs = b0;
-        for (int j = 0; j < n && j < NS && ok; ++j) {
-          const uint32_t st = ring.stage;
-          set_stage(bs, st);
-          ok = mbar_wait(smem_u32(kv_full + st), ring.phase, abort_flag);
-          ring.next<S>();
+        if (s_role) {
+          const uint32_t qs = qi & 1u;
+          ok = mbar_wait(smem_u32(q_full + qs), (qi >> 1) & 1u, abort_flag);
+          ++qi;
           if (!ok) break;
-          tc_fence_after();
-          issue_s(qs, bs, st);
-          mma2_commit_mc(smem_u32(s_full + bs), kBoth);
-          bs = next_buf(bs);
-        }
-        if (!ok) break;
-        if (n <= NS) mma2_commit_mc(smem_u32(q_empty + qs), kBoth);
-        uint32_t b = b0;
-        for (int j = 0; j < n && ok; ++j) {
-          ok = mbar_wait(smem_u32(p_full + b), (pph >> b) & 1u, abort_flag);
-          pph ^= 1u << b;
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t stj = stage_of(b);
-          issue_pv(b, stj, j > 0);
-          mma2_commit_mc(smem_u32(pv_done + b), kBoth);
-          mma2_commit_mc(smem_u32(kv_empty + stj), kBoth);
-          if (j + NS < n) {
-            // S of step j + NS into the buffer P V (j) just read (MMAs run in order)
+          const uint64_t a0 = qdesc0 + (uint64_t)((qs * C::kQBytes) >> 4);
+          for (int j = 0; j < n && ok; ++j) {
             const uint32_t st = ring.stage;
-            set_stage(b, st);
             ok = mbar_wait(smem_u32(kv_full + st), ring.phase, abort_flag);
             ring.next<S>();
+            if (ok && ((used >> b) & 1u)) {
+              ok = mbar_wait(smem_u32(pv_done + b), (ph >> b) & 1u, abort_flag);
+              ph ^= 1u << b;
+            }
+            if (!ok) break;
+            used |= 1u << b;
+            tc_fence_after();
+            // S_b = Q K_st^T (K = 128 dims in 8 steps of 16)
+            const uint32_t d_t = tmem + b * 128;
+            const uint64_t b0 = kdesc0 + (uint64_t)((st * C::kStageBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < C::D / 16; ++kk) {
+              const uint64_t a = a0 + (uint64_t)((kk / 4) * (16384 >> 4) + (kk % 4) * 2);
+              const uint64_t bb = b0 + (uint64_t)((kk / 4) * (8192 >> 4) + (kk % 4) * 2);
+              if (kk == 0) mma2_ss_acc<0>(d_t, a, bb, idesc_s);
+              else mma2_ss_acc<1>(d_t, a, bb, idesc_s);
+            }
+            mma2_commit_mc(smem_u32(s_full + b), kBoth);
+            if (j + 1 == n) mma2_commit_mc(smem_u32(q_empty + qs), kBoth);
+            b = b + 1 == (uint32_t)NS ? 0u : b + 1;
+          }
+        } else {
+          for (int j = 0; j < n && ok; ++j) {
+            const uint32_t st = ring.stage;
+            ring.next<S>();
+            ok = mbar_wait(smem_u32(p_full + b), (ph >> b) & 1u, abort_flag);
+            ph ^= 1u << b;
             if (!ok) break;
             tc_fence_after();
-            issue_s(qs, b, st);
-            mma2_commit_mc(smem_u32(s_full + b), kBoth);
-            if (j + NS + 1 == n) mma2_commit_mc(smem_u32(q_empty + qs), kBoth);
+            // O += P_b V_st (K = 128 keys in 8 steps of 16; P bf16 packed in S_b)
+            const uint32_t d_t = tmem + C::kOCol;
+            const uint32_t a_t = tmem + b * 128;
+            const uint64_t bs = vdesc0 + (uint64_t)((st * C::kStageBytes) >> 4);
+            if (j > 0) mma2_ts_acc<1>(d_t, a_t, bs, idesc_o);
+            else mma2_ts_acc<0>(d_t, a_t, bs, idesc_o);
+#pragma unroll
+            for (int kk = 1; kk < BK / 16; ++kk)
+              mma2_ts_acc<1>(d_t, a_t + kk * 8, bs + (uint64_t)(kk * ((16 * 128) >> 4)), idesc_o);
+            mma2_commit_mc(smem_u32(pv_done + b), kBoth);
+            mma2_commit_mc(smem_u32(kv_empty + st), kBoth);
+            b = b + 1 == (uint32_t)NS ? 0u : b + 1;
           }
-          b = next_buf(b);
         }
-        b0 = b;
       }
       // every MMA issued has finished before either CTA frees its TMEM
       mma2_commit_mc(smem_u32(mma_done), kBoth);
     }
     __syncwarp();
-    if (lane == 0) mbar_drain_cl(smem_u32(mma_done), 0u, kWaitTimeoutNs);
+    if (warp == 1 && lane == 0) mbar_drain_cl(smem_u32(mma_done), 0u, kWaitTimeoutNs);
     __syncwarp();
   } else if (warp >= 4) {
     // --------------------------------------------------- softmax + epilogue ---
@@ -1448,16 +1440,9 @@ bsa_status launch_forward(const ForwardArgs& a_in, cudaStream_t stream) {
     a.block_q = 256;
     a.nQb = nSb;
   }
-  static const bool pair = [] {
-    const char* e = std::getenv("BSA_FWD_PAIR");
-    return e && *e && std::strcmp(e, "0") != 0;
-  }();
-  if (pair) {
-    if (a.d == 128 && a.block_k == 128) return launch_pair<128, kPairSBufs>(a, stream);
-    if (a.d == 128 && a.block_k == 64) return launch_pair<64, kPairSBufs>(a, stream);
-  }
-  if (a.d == 128 && a.block_k == 128) return launch_t<128, 128, 2>(a, stream);
-  if (a.d == 128 && a.block_k == 64) return launch_t<128, 128, 2, 64>(a, stream);   // paired 64-key blocks
+  // head dim 128: CTA pairs (M = 256 MMAs); head dim 64: one CTA per 256 rows
+  if (a.d == 128 && a.block_k == 128) return launch_pair<128, kPairSBufs>(a, stream);
+  if (a.d == 128 && a.block_k == 64) return launch_pair<64, kPairSBufs>(a, stream);   // paired 64-key blocks
   if (a.d == 64 && a.block_k == 128) return launch_t<64, 128, 2>(a, stream);
   if (a.d == 64 && a.block_k == 64) return launch_t<64, 128, 2, 64>(a, stream);
   return set_error(BSA_ERR_UNSUPPORTED, "bsa_forward: unsupported (d, block_k)");
