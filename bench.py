@@ -72,11 +72,8 @@ def peaks():
 # `sha`.  When the sources change the figure no longer applies and traffic is
 # null.
 FMHA_TRAFFIC = {
-    "sha": "23fc1a5077027a58",
-    "720p_75": 13786140928 + 1723019008,
-    "480p_75": 503945984 + 268207872,
-    "480p_dense": 510417920 + 270237184,
-    "1280x736_ragged": 23890579712 + 2600347136,
+    "sha": "dec5531165c80383",
+    "720p_75": 21691810560 + 1439451904,
 }
 
 

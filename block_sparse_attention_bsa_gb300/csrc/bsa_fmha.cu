@@ -1440,9 +1440,12 @@ bsa_status launch_forward(const ForwardArgs& a_in, cudaStream_t stream) {
     a.block_q = 256;
     a.nQb = nSb;
   }
-  // head dim 128: CTA pairs (M = 256 MMAs); head dim 64: one CTA per 256 rows
+  // head dim 128 with 128-key blocks: CTA pairs (M = 256 MMAs).  64-key
+  // blocks (two list entries per 128-key tile) run faster on the single-CTA
+  // kernel, which skips a row's unselected 64-key halves (measured at 480p:
+  // 9.0 ms against 10.1 ms); so does head dim 64.
   if (a.d == 128 && a.block_k == 128) return launch_pair<128, kPairSBufs>(a, stream);
-  if (a.d == 128 && a.block_k == 64) return launch_pair<64, kPairSBufs>(a, stream);   // paired 64-key blocks
+  if (a.d == 128 && a.block_k == 64) return launch_t<128, 128, 2, 64>(a, stream);   // paired 64-key blocks
   if (a.d == 64 && a.block_k == 128) return launch_t<64, 128, 2>(a, stream);
   if (a.d == 64 && a.block_k == 64) return launch_t<64, 128, 2, 64>(a, stream);
   return set_error(BSA_ERR_UNSUPPORTED, "bsa_forward: unsupported (d, block_k)");
