@@ -72,8 +72,8 @@ def peaks():
 # `sha`.  When the sources change the figure no longer applies and traffic is
 # null.
 FMHA_TRAFFIC = {
-    "sha": "dec5531165c80383",
-    "720p_75": 21691810560 + 1439451904,
+    "sha": "43c163fd0d8cd03b",
+    "720p_75": 21705600512 + 1439234816,
 }
 
 
