@@ -15,7 +15,9 @@ skip) divided by the step time.
 --impl reference times the fp64 CPU oracle (the only other implementation of
 the method here) on a bounded sample of the same workload, extrapolated to
 the full workload.  Under torchrun every rank runs its own replica (weak
-scaling, no collective on the data path); rank 0 prints the JSON line.
+scaling), or with --split kv-heads each rank takes an equal share of the KV
+heads and their query heads (strong scaling); there is no collective on the
+data path in either mode, and rank 0 prints the JSON line.
 """
 
 from __future__ import annotations
@@ -55,6 +57,9 @@ def parse():
                     help="time the dense pass and the sparse step and report a dense->sparse schedule")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the dense pass and the other workloads (480p, 1280x736) after the timed step")
+    ap.add_argument("--split", choices=["replicas", "kv-heads"], default="replicas",
+                    help="under torchrun: every rank runs the whole step (replicas, weak scaling), or rank r "
+                         "runs KV heads [r Hkv/N, (r+1) Hkv/N) and their query heads (kv-heads, strong scaling)")
     return ap.parse_args()
 
 
@@ -156,6 +161,31 @@ def max_over_ranks(value: float, device=None) -> float:
         return value
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def head_partition(Hq: int, Hkv: int, world: int, rank: int):
+    """KV heads [hk0, hk1) of `rank` when the KV heads are split evenly over
+    `world` ranks, and the query heads [hq0, hq1) that read them (query head h
+    reads KV head h // (Hq / Hkv), so a KV-head range carries a contiguous
+    query-head range).  Returns (hq0, hq1, hk0, hk1)."""
+    if Hkv % world:
+        raise ValueError(f"{Hkv} KV heads do not split evenly over {world} ranks")
+    per = Hkv // world
+    G = Hq // Hkv
+    hk0, hk1 = rank * per, (rank + 1) * per
+    return hk0 * G, hk1 * G, hk0, hk1
+
+
+def sum_over_ranks(value: float, device=None) -> float:
+    """Sum of a per-rank scalar over the process group (identity without one).
+    Bookkeeping only: the data path exchanges nothing between ranks."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
 
 
@@ -638,6 +668,17 @@ def main():
     inp = make_inputs(cfg, "cuda", pad_fill=0.0)
     q, k, v = inp["q"], inp["k"], inp["v"]
     P, lens, bq, bk, keep = cfg.prefix, inp["seq_lens"], cfg.block_q, cfg.block_k, inp["keep_ratio"]
+    split = args.split == "kv-heads" and world > 1
+    heads = None
+    if split:
+        # this rank's KV heads and their query heads, as strided head views of
+        # the whole workload (no copy; the library takes the head stride)
+        hq0, hq1, hk0, hk1 = head_partition(cfg.Hq, cfg.Hkv, world, rank)
+        q, k, v = q[:, :, hq0:hq1], k[:, :, hk0:hk1], v[:, :, hk0:hk1]
+        keep = keep if len(keep) == 1 else keep[hq0:hq1]
+        inp = dict(inp, q=q, k=k, v=v, keep_ratio=keep)
+        heads = {"query_heads": [hq0, hq1], "kv_heads": [hk0, hk1]}
+        args.no_workloads = True      # the other workloads would run whole on every rank
     B, Sq, Hq, d = q.shape
     Skv, Hkv = k.shape[1], k.shape[2]
     nQb, nKb = -(-Sq // bq), -(-Skv // bk)
@@ -687,7 +728,12 @@ def main():
     if world > 1:
         dist.barrier()
     ms_step = total_ms / args.steps
-    value = whole_job_tflops(flops, world, ms_step)
+    if split:
+        job_flops = sum_over_ranks(flops, device="cuda")        # every head once over all ranks
+        value = job_flops / (ms_step * 1e-3) / 1e12
+    else:
+        job_flops = world * flops
+        value = whole_job_tflops(flops, world, ms_step)
     pk = peaks()
     fwd_mean = sum(fwd_ms) / len(fwd_ms)
     fwd_tflops = flops / (fwd_mean * 1e-3) / 1e12
@@ -777,7 +823,7 @@ def main():
         bsa.bsa_device_status(stream)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk_, hv))
         d2h = houts[0].numel() * houts[0].element_size() + hlses[0].numel() * hlses[0].element_size()
-        e2e = {"value": whole_job_tflops(flops, world, e_ms), "unit": UNIT, "ms_per_step": e_ms,
+        e2e = {"value": job_flops / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "compute_ms_per_step_during_copies": e_compute_ms,
                "copy_gbs_in_loop": {"h2d": h2d / (h2d_ms * 1e-3) / 1e9, "d2h": d2h / (d2h_ms * 1e-3) / 1e9,
@@ -897,10 +943,12 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.config, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "prefix": P,
+            "scaling": "strong" if split else "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.config, "B": B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "d": d, "prefix": P,
                        "seq_lens": lens, "block_q": bq, "block_k": bk, "keep_ratio": keep[:4],
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "parallelism": (f"KV-head split x{world}" if split else f"replicas x{world}")
+                       if world > 1 else "single GPU",
+                       **({"rank0_heads": heads} if heads else {}),
                        "l2": f"inputs larger than L2 ({(q.numel() + k.numel() + v.numel()) * 2 / 1e9:.2f} GB)"},
             "select_ms": sum(sel_ms) / len(sel_ms),
             "fwd_ms": fwd_mean,
@@ -908,6 +956,7 @@ def main():
             "tile_sparsity": tile_sparsity,
             "exact_pair_tflop_per_step": exact_flops / 1e12,
             "effective_tflop_per_step": flops / 1e12,
+            "job_effective_tflop_per_step": job_flops / 1e12,
             "roofline": {"bound": "tensor", "kernel": "fmha_fwd_pair_kernel<128,3>", "achieved": fwd_tflops,
                          "peak": pk["bf16"], "unit": "TFLOP/s", "frac": fwd_tflops / pk["bf16"],
                          "peak_source": f"{pk['source']} bf16 burst (of measured)",
