@@ -206,3 +206,63 @@ def test_backward_480p_identities_and_sampled_dq(name):
         rel = np.linalg.norm(g - r) / np.linalg.norm(r)
         print("tile", h, qb, "rel_fro", rel, "max err / bound", float(excess.max()))
         assert excess.max() <= 1.0, (h, qb, rel, float(excess.max()))
+
+
+def elementwise_bounds(q, k, v, out, dout, lse, indices, counts, prefix_len, seq_lens, block_q, block_k):
+    """Per-element bounds on |grad_gpu - grad_exact| from the kernels' roundings,
+    accumulated tile by tile like the oracle's backward but over magnitudes:
+      * dS (dQ, dK) and P^T (dV) rounded to bf16 before their MMAs:
+        2^-8 sum |dS| |k| (dQ), 2^-8 scale sum |dS| |q| (dK), 2^-8 sum P |dO| (dV);
+      * dP and D accumulated in fp32 over d <= 128 products (and the exponent
+        argument likewise): 2^-16 per unit of sum_c |dO_c| (|v_c| + |O_c|), carried
+        through P into dQ and dK;
+      * the result stored in bf16: 2^-8 |grad|, added by the caller.
+    Returns (bq, bk, bv) shaped like dq, dk, dv."""
+    B, Sq, Hq, d = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    scale = O.default_scale(d)
+    bq, bk, bv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    nQb = -(-Sq // block_q)
+    for b in range(B):
+        L = int(seq_lens[b])
+        for h in range(Hq):
+            hk = h // G
+            for qb in range(nQb):
+                r0, r1 = qb * block_q, min((qb + 1) * block_q, L)
+                if r1 <= r0:
+                    continue
+                c = int(counts[b, h, qb])
+                pos = O.tile_keys(indices[b, h, qb, :c], prefix_len + L, block_k)
+                if pos.size == 0:
+                    continue
+                qq, oo, gg = q[b, r0:r1, h], out[b, r0:r1, h], dout[b, r0:r1, h]
+                kk, vv = k[b, pos, hk], v[b, pos, hk]
+                p_ = np.exp((qq @ kk.T) * scale - lse[b, h, r0:r1, None])
+                D = (gg * oo).sum(axis=1, keepdims=True)
+                ds = np.abs(p_ * (gg @ vv.T - D))
+                w = p_ * (np.abs(gg) @ np.abs(vv).T + np.abs(gg * oo).sum(axis=1, keepdims=True))
+                bq[b, r0:r1, h] += scale * (2.0 ** -8 * ds + 2.0 ** -16 * w) @ np.abs(kk)
+                bk[b, pos, hk] += scale * (2.0 ** -8 * ds + 2.0 ** -16 * w).T @ np.abs(qq)
+                bv[b, pos, hk] += 2.0 ** -8 * p_.T @ np.abs(gg)
+    return bq, bk, bv
+
+
+@pytest.mark.parametrize("name", ["small_gqa", "small_mha_perhead", "tiny", "small_mqa_d64", "small_64x64_d128"])
+def test_backward_small_every_element_within_its_rounding_bound(name):
+    """Every element of dQ, dK and dV on the small configurations lies within
+    the bound its roundings allow (not only relative to the tensor's largest
+    value), including the entries whose exact gradient is zero."""
+    inp, idx, cnt, out_bf, lse32, dout, grads_r = oracle_case(name)
+    c = inp["cfg"]
+    grads = run_backward(inp, idx, cnt, out_bf, lse32, dout)
+    q, k, v = (np.nan_to_num(to_f32_np(inp[x]).astype(np.float64)) for x in ("q", "k", "v"))
+    bounds = elementwise_bounds(q, k, v, to_f32_np(out_bf).astype(np.float64),
+                                np.nan_to_num(to_f32_np(dout).astype(np.float64)), lse32.numpy().astype(np.float64),
+                                idx, cnt, c.prefix, inp["seq_lens"], c.block_q, c.block_k)
+    for n, g, r, bnd in zip(("dq", "dk", "dv"), grads, grads_r, bounds):
+        gn = g.float().cpu().numpy().astype(np.float64)
+        tol = bnd + 2.0 ** -8 * np.abs(r) + 1e-7
+        excess = np.abs(gn - r) / tol
+        print(name, n, "max err / bound", float(excess.max()))
+        assert excess.max() <= 1.0, (name, n, float(excess.max()), np.unravel_index(excess.argmax(), excess.shape))
