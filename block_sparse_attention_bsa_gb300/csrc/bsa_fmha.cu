@@ -39,6 +39,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include "bsa_internal.h"
 #include "bsa_ptx.cuh"
@@ -58,8 +59,10 @@ struct FmhaParams {   // CUtensorMap members make it 128-byte aligned
   int causal;              // 1: query row i sees key positions 0..i only (dense pass)
   int group_rows;          // merged lists: rows per original query block (64 or 128)
   int masked;              // 1: list entries are kb | membership << 24 (merged lists)
+  int list_stride;         // entries per list row (nKb, or the merged lists' row length)
   const int32_t* indices;  // NULL = dense pass
   const int32_t* counts;
+  const int32_t* classes;  // merged lists: per row, steps only half 0 / only half 1 attends
   int* counter;            // next work tile (zeroed by the schedule kernel)
   const int* group_order;  // (request, KV head) groups, heaviest first
   float scale_log2;        // softmax scale * log2(e)
@@ -73,17 +76,19 @@ struct Cfg {
   static constexpr int kQHalfBytes = 128 * 128 * kChunks; // 128 rows x D bf16
   static constexpr int kQBytes = NH * kQHalfBytes;
   static constexpr int kTileBytes = BK * 128 * kChunks;   // one K or V tile
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kAlignSlack = 1024;
   static constexpr int kSmemMax = 232448;                 // 227 KB per CTA
-  static constexpr int kStageBytes = 2 * kTileBytes;      // one ring stage: K and V of one key block
-  static constexpr int kStagesFit = (kSmemMax - kQBytes - kBarBytes - kAlignSlack) / kStageBytes;
-  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-  static constexpr int kSmemBytes = kQBytes + kStages * kStageBytes + kBarBytes + kAlignSlack;
+  // K and V tiles live in two rings: K of a step is needed when its S MMA is
+  // issued, V one softmax step later, so V gets the deeper ring.
+  static constexpr int kTilesFit = (kSmemMax - kQBytes - kBarBytes - kAlignSlack) / kTileBytes;
+  static constexpr int kKStages = kTilesFit / 2 > 8 ? 8 : kTilesFit / 2;
+  static constexpr int kVStages = kTilesFit - kKStages > 8 ? 8 : kTilesFit - kKStages;
+  static constexpr int kSmemBytes = kQBytes + (kKStages + kVStages) * kTileBytes + kBarBytes + kAlignSlack;
   static constexpr int kThreads = 128 + 128 * NH;
   static constexpr uint32_t kTmemCols = NH == 2 ? 512 : 256;
   static constexpr uint32_t kOCol = NH * 128;             // O_h at kOCol + 128 h
-  static_assert(kStages >= 2, "not enough shared memory for a K/V ring");
+  static_assert(kKStages >= 2 && kVStages >= 2, "not enough shared memory for the K/V rings");
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(BK == 64 || BK == 128, "key block");
 };
@@ -97,6 +102,7 @@ struct TileInfo {
   int bl, b, qb, h, hk, L, valid_kv;
   int n;          // list entries (key blocks of the lists' geometry)
   int steps;      // key tiles the kernel walks: n, or ceil(n / 2) when 64-key blocks are paired
+  int nb, c0, c1; // steps both halves attend, only half 0, only half 1 (nb = steps unless merged)
   const int32_t* idx;
 };
 
@@ -129,11 +135,29 @@ __device__ __forceinline__ TileInfo decode_tile(const FmhaParams& p, int t, int 
     ti.n = (kv_end + KB - 1) / KB;
   } else {
     const int c = p.counts[row];
-    ti.n = c < 0 ? 0 : (c > p.nKb ? p.nKb : c);
+    ti.n = c < 0 ? 0 : (c > p.list_stride ? p.list_stride : c);
   }
-  ti.idx = p.indices ? p.indices + row * p.nKb : nullptr;
+  ti.idx = p.indices ? p.indices + row * p.list_stride : nullptr;
   ti.steps = KB < BK ? (ti.n + 1) / 2 : ti.n;
+  ti.c0 = ti.c1 = 0;
+  if (p.classes && ti.steps > 0) {
+    ti.c0 = min(max(p.classes[2 * row], 0), ti.steps);
+    ti.c1 = min(max(p.classes[2 * row + 1], 0), ti.steps - ti.c0);
+  }
+  ti.nb = ti.steps - ti.c0 - ti.c1;
   return ti;
+}
+
+// K/V stage order of step k of half hh.  Merged lists come in three classes
+// (see merge_lists_kernel): the key tiles both halves attend (positions
+// 0 .. nb-1), then the tiles only one half attends, one for half 0 and one for
+// half 1 in turn while both classes last, then the rest of the longer class.
+// Other lists have nb = steps: step k is position k for both halves.
+__device__ __forceinline__ int step_pos(const TileInfo& ti, int hh, int k) {
+  if (k < ti.nb) return k;
+  k -= ti.nb;
+  const int m = min(ti.c0, ti.c1);
+  return k < m ? ti.nb + 2 * k + hh : ti.nb + m + k;
 }
 
 // Max of v[LO .. LO + N) in four independent chains of three-input max.
@@ -184,24 +208,28 @@ template <int D, int BK, int NH, int KB = BK>
 __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ FmhaParams p) {
   static_assert(KB == BK || (KB == 64 && BK == 128), "key block pairing");
+  static_assert(NH == 2, "two 128-row halves per work tile");
   using C = Cfg<D, BK, NH>;
+  constexpr int kK = C::kKStages, kV = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* q_smem = smem;
-  uint8_t* kv_smem = smem + C::kQBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(kv_smem + C::kStages * C::kStageBytes);
+  uint8_t* k_smem = smem + C::kQBytes;
+  uint8_t* v_smem = k_smem + kK * C::kTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(v_smem + kV * C::kTileBytes);
   // barrier slots
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
   uint64_t* s_full = bars + 2;            // [2]
   uint64_t* p_full = bars + 4;            // [2]
   uint64_t* o_full = bars + 6;            // [2]
-  uint64_t* kv_full = bars + 8;           // [kStages]
-  uint64_t* kv_empty = bars + 8 + C::kStages;
-  uint64_t* tile_full = bars + 8 + 2 * C::kStages;    // [2] tile-id ring
-  uint64_t* tile_empty = bars + 10 + 2 * C::kStages;  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12 + 2 * C::kStages);
+  uint64_t* tile_full = bars + 8;         // [2] tile-id ring
+  uint64_t* tile_empty = bars + 10;       // [2]
+  uint64_t* kv_full = bars + 12;          // [kK] K tile and V tile of one step landed
+  uint64_t* k_empty = kv_full + kK;       // [kK]
+  uint64_t* v_empty = k_empty + kK;       // [kV]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(v_empty + kV);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* tile_ids = reinterpret_cast<volatile int*>(tmem_slot + 2);   // [2]
 
@@ -216,10 +244,11 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       mbar_init(smem_u32(p_full + i), 128);
       mbar_init(smem_u32(o_full + i), 1);
     }
-    for (int i = 0; i < C::kStages; ++i) {
+    for (int i = 0; i < kK; ++i) {
       mbar_init(smem_u32(kv_full + i), 1);
-      mbar_init(smem_u32(kv_empty + i), 1);
+      mbar_init(smem_u32(k_empty + i), 1);
     }
+    for (int i = 0; i < kV; ++i) mbar_init(smem_u32(v_empty + i), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(tile_full + i), 1);
       mbar_init(smem_u32(tile_empty + i), 1 + 128 * NH);   // MMA thread + softmax threads
@@ -246,10 +275,14 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
   if (warp < 4) {
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer ---
-    Ring ring;
+    // Key tiles in step order into the K ring and the V ring.  A step's K
+    // and V tiles complete on one barrier (kv_full, indexed like the K
+    // ring); the two rings' slots are released on their own barriers.
+    Ring kr, vr;
     uint32_t qi = 0;
     const uint32_t q_base = smem_u32(q_smem);
-    const uint32_t kv_base = smem_u32(kv_smem);
+    const uint32_t k_base = smem_u32(k_smem);
+    const uint32_t v_base = smem_u32(v_smem);
     const uint64_t q_policy = l2_policy_evict_first();   // Q is read once
     bool ok = true;
     TileRing tr;
@@ -299,25 +332,25 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
             if (jj + 1 < m && t1 >= 0 && t1 < p.nKb) kb1 = t1;
           }
           if (lane == 0) {
-            // K at the stage base, V right after it; one barrier for both.
-            ok = mbar_wait(smem_u32(kv_empty + ring.stage), ring.phase ^ 1u, abort_flag);
-            if (ok) {
-              const uint32_t fb = smem_u32(kv_full + ring.stage);
-              mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
-              for (int which = 0; which < 2; ++which) {
-                const CUtensorMap* tm = which == 0 ? &p.tk[ti.bl] : &p.tv[ti.bl];
-                for (int c = 0; c < C::kChunks; ++c) {
-                  const uint32_t dst = kv_base + ring.stage * C::kStageBytes + which * C::kTileBytes + c * (BK * 128);
-                  if constexpr (KB == BK) {
-                    tma_load_3d(dst, tm, fb, c * 64, kb * BK, ti.hk);
-                  } else {            // rows 0..63 from the first block, 64..127 from the second
-                    tma_load_3d(dst, tm, fb, c * 64, kb * KB, ti.hk);
-                    tma_load_3d(dst + KB * 128, tm, fb, c * 64, kb1 * KB, ti.hk);
-                  }
+            ok = mbar_wait(smem_u32(k_empty + kr.stage), kr.phase ^ 1u, abort_flag) &&
+                 mbar_wait(smem_u32(v_empty + vr.stage), vr.phase ^ 1u, abort_flag);
+            const uint32_t fb = smem_u32(kv_full + kr.stage);
+            if (ok) mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
+            for (int which = 0; which < 2 && ok; ++which) {
+              const CUtensorMap* tm = which == 0 ? &p.tk[ti.bl] : &p.tv[ti.bl];
+              const uint32_t base = which == 0 ? k_base + kr.stage * C::kTileBytes : v_base + vr.stage * C::kTileBytes;
+              for (int c = 0; c < C::kChunks; ++c) {
+                const uint32_t dst = base + c * (BK * 128);
+                if constexpr (KB == BK) {
+                  tma_load_3d(dst, tm, fb, c * 64, kb * BK, ti.hk);
+                } else {            // rows 0..63 from the first block, 64..127 from the second
+                  tma_load_3d(dst, tm, fb, c * 64, kb * KB, ti.hk);
+                  tma_load_3d(dst + KB * 128, tm, fb, c * 64, kb1 * KB, ti.hk);
                 }
               }
-              ring.next<C::kStages>();
             }
+            kr.next<kK>();
+            vr.next<kV>();
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
@@ -330,10 +363,9 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, BK, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, true);
       const uint32_t q_base = smem_u32(q_smem);
-      const uint32_t kv_base = smem_u32(kv_smem);
-      Ring ring;
+      Ring kc, vc;         // K and V ring cursors: the next tile to be used
       uint32_t qi = 0;
-      uint32_t pph[2] = {0u, 0u};
+      uint32_t pph0 = 0u, pph1 = 0u;
       bool ok = true;
       // Shared-memory descriptors are computed once: a descriptor's start
       // address field is (address >> 4) in its low 14 bits, so moving the
@@ -344,9 +376,9 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       uint64_t qdesc[NH];
 #pragma unroll
       for (int hh = 0; hh < NH; ++hh) qdesc[hh] = sdesc_sw128(q_base + hh * C::kChunks * 16384, 16, 1024);
-      const uint64_t kdesc0 = sdesc_sw128(kv_base, 16, 1024);
-      const uint64_t vdesc0 = sdesc_sw128(kv_base, BK * 128, 1024);
-      // issue_s / issue_pv take the byte offset of the K or V tile in the ring.
+      const uint64_t kdesc0 = sdesc_sw128(smem_u32(k_smem), 16, 1024);
+      const uint64_t vdesc0 = sdesc_sw128(smem_u32(v_smem), BK * 128, 1024);
+      // issue_s / issue_pv take the byte offset of the K or V tile in its ring.
       auto issue_s = [&](int hh, uint32_t tile_off) {
         const uint32_t d_t = tmem + hh * 128;
         const uint64_t bs = kdesc0 + (uint64_t)(tile_off >> 4);
@@ -374,52 +406,61 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
         const int t = tr.take(tile_full, tile_empty, tile_ids, abort_flag, ok);
         if (t < 0) break;
         const TileInfo ti = decode_tile(p, t, KB, BK);
-        const int n = ti.steps;
-        if (n == 0) continue;
+        if (ti.steps == 0) continue;
         ok = mbar_wait(smem_u32(q_full), qi & 1u, abort_flag);
         ++qi;
         if (!ok) break;
-        // K_j and V_j share stage sJ (K at +0, V at +kTileBytes).
-        uint32_t sJ = ring.stage;
-        ok = mbar_wait(smem_u32(kv_full + sJ), ring.phase, abort_flag);
-        ring.next<C::kStages>();
-        if (!ok) break;
-        tc_fence_after();
-        for (int hh = 0; hh < NH; ++hh) {
-          issue_s(hh, sJ * C::kStageBytes);
-          mma_commit(smem_u32(s_full + hh));
-        }
-        if (n == 1) mma_commit(smem_u32(q_empty));
-        for (int j = 0; j < n && ok; ++j) {
-          const bool has_next = j + 1 < n;
-          uint32_t sN = 0, sN_phase = 0;
-          if (has_next) {
-            sN = ring.stage;
-            sN_phase = ring.phase;
-            ring.next<C::kStages>();
-          }
-          for (int hh = 0; hh < NH && ok; ++hh) {
-            ok = mbar_wait(smem_u32(p_full + hh), pph[hh] & 1u, abort_flag);
-            ++pph[hh];
-            if (!ok) break;
+        // Each half walks its own steps (step_pos): its first nb steps are
+        // the key tiles both halves attend, used by half 0 first, so half 1's
+        // S and P V are their last uses and release the K and V slots.  While
+        // both halves have steps left they alternate, so the tensor pipe runs
+        // one half's MMAs while the other half's softmax works; the rest of
+        // the longer half-only class runs alone.  S and P V are issued in
+        // ring order (a shared tile by both halves in a row), so each ring
+        // has one cursor.  The half is a compile-time constant in each body
+        // (H0 / H1): its TMEM columns, barriers and descriptors stay in
+        // registers.
+        const int nb = ti.nb, nh0 = nb + ti.c0, nh1 = nb + ti.c1;
+        int s_left = nh0 + nh1;
+        auto start_s = [&](auto H, int k) -> bool {     // S of the half's step k
+          constexpr int hh = decltype(H)::value;
+          const bool last = hh == 1 || k >= nb;          // last use of the K tile
+          if (hh == 0 || k >= nb) {           // the step's K and V tiles have landed
+            if (!mbar_wait(smem_u32(kv_full + kc.stage), kc.phase, abort_flag)) return false;
             tc_fence_after();
-            issue_pv(hh, sJ * C::kStageBytes + C::kTileBytes, j > 0);
-            if (j == n - 1) mma_commit(smem_u32(o_full + hh));
-            if (has_next) {
-              if (hh == 0) {
-                ok = mbar_wait(smem_u32(kv_full + sN), sN_phase, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-              }
-              issue_s(hh, sN * C::kStageBytes);
-              mma_commit(smem_u32(s_full + hh));
-            }
           }
-          if (!ok) break;
-          // both halves are done with stage sJ once PV_1(j) completes
-          mma_commit(smem_u32(kv_empty + sJ));
-          if (has_next && j + 2 == n) mma_commit(smem_u32(q_empty));
-          sJ = sN;
+          issue_s(hh, kc.stage * C::kTileBytes);
+          mma_commit(smem_u32(s_full + hh));
+          if (last) {
+            mma_commit(smem_u32(k_empty + kc.stage));
+            kc.template next<kK>();
+          }
+          if (--s_left == 0) mma_commit(smem_u32(q_empty));
+          return true;
+        };
+        auto step = [&](auto H, int& k, uint32_t& ph, int nh) -> bool {   // P V of step k, S of k + 1
+          constexpr int hh = decltype(H)::value;
+          const bool last = hh == 1 || k >= nb;          // last use of the V tile
+          if (!mbar_wait(smem_u32(p_full + hh), ph & 1u, abort_flag)) return false;
+          ++ph;
+          tc_fence_after();                      // V landed with K, waited for before this step's S
+          issue_pv(hh, vc.stage * C::kTileBytes, k > 0);
+          if (last) {
+            mma_commit(smem_u32(v_empty + vc.stage));
+            vc.template next<kV>();
+          }
+          if (++k < nh) return start_s(H, k);
+          mma_commit(smem_u32(o_full + hh));
+          return true;
+        };
+        const std::integral_constant<int, 0> H0;
+        const std::integral_constant<int, 1> H1;
+        int k0 = 0, k1 = 0;
+        if (nh0 > 0) ok = start_s(H0, 0);
+        if (ok && nh1 > 0) ok = start_s(H1, 0);
+        while (ok && (k0 < nh0 || k1 < nh1)) {
+          if (k0 < nh0) ok = step(H0, k0, pph0, nh0);
+          if (ok && k1 < nh1) ok = step(H1, k1, pph1, nh1);
         }
       }
     }
@@ -446,7 +487,8 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
       const bool row_ok = row_exists && row < ti.L;
       __nv_bfloat16* orow = p.out + (((int64_t)ti.b * p.Sq + row) * p.Hq + ti.h) * D;
       float* lrow = p.lse ? p.lse + ((int64_t)ti.b * p.Hq + ti.h) * p.Sq + row : nullptr;
-      if (ti.n == 0) {
+      const int nsteps = ti.nb + (hh == 0 ? ti.c0 : ti.c1);   // this half's key tiles
+      if (nsteps == 0) {
         if (row_exists) {
           uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -470,7 +512,8 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
         if (p.masked && !((entry >> (kEntryGroupShift + row_in_blk / p.group_rows)) & 1)) kb = p.nKb;
         return kb;
       };
-      for (int j = 0; j < ti.steps; ++j) {
+      for (int kk = 0; kk < nsteps; ++kk) {
+        const int j = step_pos(ti, hh, kk);
         const int kb = entry_block(KB < BK ? 2 * j : j);
         const int kb1 = KB < BK ? entry_block(2 * j + 1) : 0;    // second 64-key half of the tile
         // keys of this block this row may see: the real keys, and in a causal
@@ -1214,6 +1257,8 @@ bsa_status launch_t(const ForwardArgs& a, cudaStream_t stream) {
     p.n_tiles = Bn * a.nQb * a.Hq;
     p.indices = a.indices;
     p.counts = a.counts;
+    p.classes = a.classes;
+    p.list_stride = a.list_stride > 0 ? a.list_stride : a.nKb;
     p.causal = a.causal ? 1 : 0;
     p.masked = a.masked ? 1 : 0;
     p.group_rows = a.group_rows > 0 ? a.group_rows : a.block_q;
@@ -1304,6 +1349,8 @@ bsa_status launch_pair(const ForwardArgs& a, cudaStream_t stream) {
     p.n_tiles = Bn * a.nQb * a.Hq;
     p.indices = a.indices;
     p.counts = a.counts;
+    p.classes = a.classes;
+    p.list_stride = a.list_stride > 0 ? a.list_stride : a.nKb;
     p.causal = a.causal ? 1 : 0;
     p.masked = a.masked ? 1 : 0;
     p.group_rows = a.group_rows > 0 ? a.group_rows : a.block_q;
@@ -1347,18 +1394,35 @@ bsa_status launch_fwd_wait_probe(unsigned long long limit_ns, cudaStream_t strea
 // ------------------------------------------------------ merged lists ---
 // For query blocks of 64 or 128 rows, the 256/block_q query blocks of each
 // 256-row super-block are attended together: one warp ORs their key-block
-// lists into bitmaps and writes the ascending union with one membership bit
-// per query block (kb | bits << 24).  The forward then runs its 256-row,
-// two-half ping-pong path over the union and masks, per row, the key blocks
-// the row's own query block did not select -- the same result as attending
-// each query block's list alone, with K/V tiles reused by 256 rows.
+// lists into bitmaps and writes the union with one membership bit per query
+// block (kb | bits << 24).  The forward then runs its 256-row, two-half
+// ping-pong path over the union and masks, per row, the key blocks the row's
+// own query block did not select -- the same result as attending each query
+// block's list alone, with K/V tiles reused by both 128-row halves where both
+// attend them.
+//
+// The union is written in steps of per_step entries (one key tile of the
+// forward: two 64-key blocks, or one 128-key block), in three classes, each
+// in ascending key order: the blocks both halves' query blocks selected, then
+// the blocks only half 0's or only half 1's selected, one step of each in
+// turn while both last, then the rest of the longer class.  A class whose
+// size is not a multiple of per_step ends with a padding entry (the block
+// past the end, no membership bit), so no step mixes classes and a half
+// skips every step of the other half's class (step_pos in the forward walks
+// the same order).  Per row: count = entries including padding, classes =
+// (steps of the half-0-only class, steps of the half-1-only class).
 struct MergeParams {
   const int32_t* indices;   // [B, Hq, nQb, nKb]
   const int32_t* counts;    // [B, Hq, nQb]
-  int32_t* uindices;        // [B, Hq, nSb, nKb]
+  int32_t* uindices;        // [B, Hq, nSb, stride]
   int32_t* ucounts;         // [B, Hq, nSb]
-  int Hq, nQb, nKb, nSb, ratio, words;
+  int32_t* uclasses;        // [B, Hq, nSb, 2]
+  int Hq, nQb, nKb, nSb, ratio, words, per_step, stride;
 };
+
+// Row length of a merged list: the union (at most nKb blocks) plus one
+// padding entry per class.
+inline int merged_stride(int nKb) { return nKb + 3; }
 
 __global__ void __launch_bounds__(32) merge_lists_kernel(const __grid_constant__ MergeParams p) {
   extern __shared__ uint32_t bm[];   // [ratio][words]
@@ -1378,40 +1442,76 @@ __global__ void __launch_bounds__(32) merge_lists_kernel(const __grid_constant__
     }
   }
   __syncwarp();
+  const int gh = p.ratio / 2;   // query blocks per 128-row half
+  // the three classes of word w: both halves, half 0 only, half 1 only
+  auto classes_of = [&](int w, uint32_t (&cl)[3]) {
+    uint32_t h0 = 0u, h1 = 0u;
+    if (w < p.words)
+      for (int g = 0; g < p.ratio; ++g) (g < gh ? h0 : h1) |= bm[g * p.words + w];
+    cl[0] = h0 & h1;
+    cl[1] = h0 & ~h1;
+    cl[2] = h1 & ~h0;
+  };
+  int nc[3] = {0, 0, 0};
+  for (int w = lane; w < p.words; w += 32) {
+    uint32_t cl[3];
+    classes_of(w, cl);
+    for (int c = 0; c < 3; ++c) nc[c] += __popc(cl[c]);
+  }
+  for (int c = 0; c < 3; ++c)
+    for (int o = 16; o > 0; o >>= 1) nc[c] += __shfl_xor_sync(0xffffffffu, nc[c], o);
+  const int S = p.per_step;
+  const int st[3] = {(nc[0] + S - 1) / S, (nc[1] + S - 1) / S, (nc[2] + S - 1) / S};
+  const int m = min(st[1], st[2]);
+  // entry e of class c -> its place in the merged row
+  auto out_pos = [&](int c, int e) {
+    if (c == 0) return e;
+    const int k = e / S;
+    const int step = st[0] + (k < m ? 2 * k + (c - 1) : m + k);
+    return step * S + e % S;
+  };
   const int64_t srow = ((int64_t)b * p.Hq + h) * p.nSb + sb;
-  int32_t* out = p.uindices + srow * p.nKb;
-  int running = 0;
+  int32_t* out = p.uindices + srow * p.stride;
+  int running[3] = {0, 0, 0};
   for (int w0 = 0; w0 < p.words; w0 += 32) {
     const int w = w0 + lane;
-    uint32_t m[4] = {0u, 0u, 0u, 0u};
-    uint32_t u = 0u;
-    if (w < p.words)
-      for (int g = 0; g < p.ratio; ++g) { m[g] = bm[g * p.words + w]; u |= m[g]; }
-    const int cnt = __popc(u);
-    int incl = cnt;
+    uint32_t cl[3];
+    classes_of(w, cl);
+    for (int c = 0; c < 3; ++c) {
+      uint32_t u = cl[c];
+      const int cnt = __popc(u);
+      int incl = cnt;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      int e = running[c] + incl - cnt;
+      while (u) {
+        const int bit = __ffs(u) - 1;
+        u &= u - 1;
+        int mask = 0;
+        for (int g = 0; g < p.ratio; ++g) mask |= (int)((bm[g * p.words + w] >> bit) & 1u) << g;
+        out[out_pos(c, e++)] = (w * 32 + bit) | (mask << kEntryGroupShift);
+      }
+      running[c] += __shfl_sync(0xffffffffu, incl, 31);
     }
-    int pos = running + incl - cnt;
-    while (u) {
-      const int bit = __ffs(u) - 1;
-      u &= u - 1;
-      int mask = 0;
-      for (int g = 0; g < p.ratio; ++g) mask |= (int)((m[g] >> bit) & 1u) << g;
-      out[pos++] = (w * 32 + bit) | (mask << kEntryGroupShift);
-    }
-    running += __shfl_sync(0xffffffffu, incl, 31);
   }
-  if (lane == 0) p.ucounts[srow] = running;
+  if (lane == 0) {
+    for (int c = 0; c < 3; ++c)
+      for (int e = nc[c]; e < st[c] * S; ++e) out[out_pos(c, e)] = p.nKb;   // padding
+    p.ucounts[srow] = S * (st[0] + st[1] + st[2]);
+    p.uclasses[2 * srow] = st[1];
+    p.uclasses[2 * srow + 1] = st[2];
+  }
 }
 
 size_t merged_list_bytes(int B, int Hq, int Sq, int Skv, int block_q, int block_k) {
   if (block_q >= 256) return 0;
-  const size_t nSb = (size_t)cdiv64(Sq, 256), nKb = (size_t)cdiv64(Skv, block_k);
+  const size_t rows = (size_t)B * Hq * (size_t)cdiv64(Sq, 256);
+  const size_t stride = (size_t)merged_stride((int)cdiv64(Skv, block_k));
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return al((size_t)B * Hq * nSb * nKb * 4) + al((size_t)B * Hq * nSb * 4);
+  return al(rows * stride * 4) + al(rows * 4) + al(rows * 8);
 }
 
 bsa_status launch_forward(const ForwardArgs& a_in, cudaStream_t stream) {
@@ -1422,18 +1522,25 @@ bsa_status launch_forward(const ForwardArgs& a_in, cudaStream_t stream) {
     const int nSb = (int)cdiv64(a.Sq, 256);
     if (a.indices) {
       char* mws = static_cast<char*>(a.workspace) + forward_chunk_bytes(a.Hq) * (size_t)cdiv64(a.B, kMaxFwdBatch);
-      const size_t ul_bytes = ((size_t)a.B * a.Hq * nSb * a.nKb * 4 + 255) & ~(size_t)255;
+      auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+      const size_t rows = (size_t)a.B * a.Hq * nSb;
+      const int stride = merged_stride(a.nKb);
       MergeParams mp{};
       mp.indices = a.indices; mp.counts = a.counts;
       mp.uindices = reinterpret_cast<int32_t*>(mws);
-      mp.ucounts = reinterpret_cast<int32_t*>(mws + ul_bytes);
+      mp.ucounts = reinterpret_cast<int32_t*>(mws + al(rows * stride * 4));
+      mp.uclasses = reinterpret_cast<int32_t*>(mws + al(rows * stride * 4) + al(rows * 4));
       mp.Hq = a.Hq; mp.nQb = a.nQb; mp.nKb = a.nKb; mp.nSb = nSb; mp.ratio = ratio;
       mp.words = (a.nKb + 31) / 32;
+      mp.per_step = a.block_k == 64 ? 2 : 1;   // 64-key blocks: two per 128-key tile
+      mp.stride = stride;
       merge_lists_kernel<<<dim3(nSb, a.Hq, a.B), 32, sizeof(uint32_t) * ratio * mp.words, stream>>>(mp);
       bsa_status st = cuda_check(cudaGetLastError(), "merge_lists_kernel launch");
       if (st != BSA_OK) return st;
       a.indices = mp.uindices;
       a.counts = mp.ucounts;
+      a.classes = mp.uclasses;
+      a.list_stride = stride;
       a.masked = true;
     }
     a.group_rows = a.block_q;

@@ -82,6 +82,8 @@ struct ForwardArgs {
   bool causal;               // key position <= query row (dense pass over the prefix only)
   bool masked = false;       // internal: merged lists with membership bits
   int group_rows = 0;        // internal: rows per original query block of merged lists
+  const int32_t* classes = nullptr;   // internal: merged lists' per-row class sizes
+  int list_stride = 0;       // internal: entries per list row (0: nKb)
 };
 // Workspace bytes of the merged lists used when block_q < 256 (0 otherwise).
 size_t merged_list_bytes(int B, int Hq, int Sq, int Skv, int block_q, int block_k);

@@ -176,9 +176,10 @@ def test_forward_workspace_required(lib):
     need = lib.bsa_forward_workspace_size(1, 4, 512, 768, 256, 128)
     assert need == 256 + 256      # tile counter + group order (8 requests x 4 heads x 4 B, rounded)
     assert lib.bsa_forward_workspace_size(9, 4, 512, 768, 256, 128) == 2 * need   # two launch chunks of 8
-    # 64-row query blocks: + merged lists [1, 4, 2 super-blocks, 12 key blocks] int32 and counts
+    # 64-row query blocks: + merged lists [1, 4, 2 super-blocks, 12 key blocks + 3 padding entries]
+    # int32, their counts and their class sizes (two int32 per row)
     m = lib.bsa_forward_workspace_size(1, 4, 512, 768, 64, 64)
-    assert m == need + ((4 * 2 * 12 * 4 + 255) // 256) * 256 + 256
+    assert m == need + ((4 * 2 * 15 * 4 + 255) // 256) * 256 + 256 + 256
     st = call_forward(lib, q, k, v, prefix=256)
     assert st == 3 and "workspace is NULL" in err(lib)
     st = call_forward(lib, q, k, v, prefix=256, ws=FAKE, ws_bytes=need - 1)

@@ -229,16 +229,50 @@ def test_merged_small_query_blocks_match_per_block_lists(name):
         out_g, lse_g = run_forward(inp, idx, cnt_g)
         for qb in range(g, cnt.shape[2], ratio):
             r0, r1 = qb * c.block_q, min((qb + 1) * c.block_q, c.Sq)
-            if c.block_k == 128:
-                assert torch.equal(out[:, r0:r1], out_g[:, r0:r1])
-                assert torch.equal(lse[:, :, r0:r1], lse_g[:, :, r0:r1])
-            else:
-                # 64-key blocks are attended two per 128-key tile, in list
-                # order, so the pairs (and the fp32 order of the row sums)
-                # follow the list: equal up to rounding.  A row that saw
-                # another block's selection would differ by far more.
-                assert torch.allclose(out[:, r0:r1].float(), out_g[:, r0:r1].float(), rtol=1e-2, atol=1e-3)
-                assert torch.allclose(lse[:, :, r0:r1], lse_g[:, :, r0:r1], rtol=0, atol=1e-4)
+            # The merged list puts the blocks both 128-row halves selected
+            # first, so a row's blocks come in another order than in a list
+            # of its own query block alone (and 64-key blocks pair up
+            # differently): the fp32 row sums are equal up to rounding.  A
+            # row that saw another block's selection would differ by far more.
+            assert torch.allclose(out[:, r0:r1].float(), out_g[:, r0:r1].float(), rtol=1e-2, atol=1e-3)
+            assert torch.allclose(lse[:, :, r0:r1], lse_g[:, :, r0:r1], rtol=0, atol=1e-4)
+
+
+@pytest.mark.parametrize("name", ["small_64x64_d128", "small_mqa_d64", "small_mha_perhead"])
+def test_merged_lists_of_every_class_shape(name):
+    """Hand-made lists that give the merged 256-row lists every shape the
+    forward walks: one 128-row half with no block at all, halves with disjoint
+    selections of odd sizes (a padding entry per class when 64-key blocks are
+    paired), one half with blocks of its own past the other's (a tail one half
+    walks alone), and blocks both halves share next to blocks of one half."""
+    inp = cuda_inputs(name, pad_fill=float("nan"))
+    c = inp["cfg"]
+    nQb, nKb = -(-c.Sq // c.block_q), -(-c.Skv // c.block_k)
+    per_half = 128 // c.block_q
+    rng = np.random.default_rng(4242)
+    idx = np.full((c.B, c.Hq, nQb, nKb), -1, np.int32)
+    cnt = np.zeros((c.B, c.Hq, nQb), np.int32)
+    for b, L in enumerate(inp["seq_lens"]):
+        for h in range(c.Hq):
+            for qb in range(-(-L // c.block_q)):
+                kind = (qb // (2 * per_half) + h + b) % 4
+                half = (qb % (2 * per_half)) // per_half
+                if kind == 0:        # half 1 attends nothing
+                    blocks = [] if half else rng.choice(nKb, min(5, nKb), replace=False)
+                elif kind == 1:      # disjoint, 3 and 5 blocks
+                    blocks = range(3) if half == 0 else range(nKb - 5, nKb)
+                elif kind == 2:      # two shared blocks, half 0 has 7 more
+                    blocks = [1, 2] + ([] if half else list(range(4, min(nKb, 11))))
+                else:                # anything
+                    blocks = rng.choice(nKb, int(rng.integers(1, nKb + 1)), replace=False)
+                blocks = sorted(set(int(x) for x in blocks))
+                idx[b, h, qb, :len(blocks)] = blocks
+                cnt[b, h, qb] = len(blocks)
+    out, lse = run_forward(inp, torch.from_numpy(idx).cuda(), torch.from_numpy(cnt).cuda())
+    qf, kf, vf = (to_f32_np(inp[x]).astype(np.float64) for x in ("q", "k", "v"))
+    o_ref, l_ref = O.attention(qf, kf, vf, idx, cnt, c.prefix, inp["seq_lens"], c.block_q, c.block_k)
+    stats = compare_attention(out.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, inp["seq_lens"])
+    print(name, stats)
 
 
 def test_keep_zero_without_prefix_gives_empty_rows():
