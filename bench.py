@@ -498,8 +498,9 @@ def other_workloads(bsa, pk, stream, step_inputs, step_fwd_ms, step_ms, step_spa
     """Forward time of the dense pass on the step's own inputs (the north
     star's 'speedup over this library's own dense pass'), and the forward of
     the other video-latent workloads (480p at 75 %, 480p dense, the ragged
-    1280x736 batch, with its dense pass); plus the pages' dense->sparse
-    schedules evaluated from those call times.  Outside the timed step."""
+    1280x736 batch, with its dense pass, and 480p at 75 % with the 64x64
+    block geometry); plus the pages' dense->sparse schedules evaluated from
+    those call times.  Outside the timed step."""
     import torch
     from bsa_inputs import CONFIGS, make_inputs
     res = {}
@@ -521,7 +522,7 @@ def other_workloads(bsa, pk, stream, step_inputs, step_fwd_ms, step_ms, step_spa
     schedules = {"cosmos3_on_" + c.name: {"dense_call_ms": d_ms, "sparse_call_ms": step_ms,
                                           **schedule_arms("cosmos3", d_ms, step_ms)}}
     del out, fws
-    for name, n in (("480p_75", 5), ("480p_dense", 5), ("1280x736_ragged", 3)):
+    for name, n in (("480p_75", 5), ("480p_dense", 5), ("1280x736_ragged", 3), ("480p_75_64x64", 5)):
         cfg = CONFIGS[name]
         inp = make_inputs(cfg, "cuda", pad_fill=0.0)
         q2, k2, v2, L2 = inp["q"], inp["k"], inp["v"], inp["seq_lens"]

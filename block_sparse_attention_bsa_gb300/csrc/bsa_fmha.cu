@@ -211,6 +211,11 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
   static_assert(NH == 2, "two 128-row halves per work tile");
   using C = Cfg<D, BK, NH>;
   constexpr int kK = C::kKStages, kV = C::kVStages;
+  // Rings of equal depth (head dim 64) act as one ring: a step's K and V
+  // slots are released together after its last P V, one commit per step.
+  // With a shallower K ring (head dim 128) K is released after its last S,
+  // so that the next tiles' K can land while P V still reads V.
+  constexpr bool kJointRelease = kK == kV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
             if (jj + 1 < m && t1 >= 0 && t1 < p.nKb) kb1 = t1;
           }
           if (lane == 0) {
-            ok = mbar_wait(smem_u32(k_empty + kr.stage), kr.phase ^ 1u, abort_flag) &&
+            ok = (kJointRelease || mbar_wait(smem_u32(k_empty + kr.stage), kr.phase ^ 1u, abort_flag)) &&
                  mbar_wait(smem_u32(v_empty + vr.stage), vr.phase ^ 1u, abort_flag);
             const uint32_t fb = smem_u32(kv_full + kr.stage);
             if (ok) mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
@@ -432,7 +437,7 @@ __global__ void __launch_bounds__(Cfg<D, BK, NH>::kThreads, 1)
           issue_s(hh, kc.stage * C::kTileBytes);
           mma_commit(smem_u32(s_full + hh));
           if (last) {
-            mma_commit(smem_u32(k_empty + kc.stage));
+            if (!kJointRelease) mma_commit(smem_u32(k_empty + kc.stage));
             kc.template next<kK>();
           }
           if (--s_left == 0) mma_commit(smem_u32(q_empty));
