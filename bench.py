@@ -77,8 +77,8 @@ def peaks():
 # `sha`.  When the sources change the figure no longer applies and traffic is
 # null.
 FMHA_TRAFFIC = {
-    "sha": "43c163fd0d8cd03b",
-    "720p_75": 21705600512 + 1439234816,
+    "sha": "cce7a0c141738317",
+    "720p_75": 21628736512 + 1439542528,
 }
 
 
