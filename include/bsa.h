@@ -193,9 +193,11 @@ BSA_API bsa_status bsa_select_noalloc(const bsa_tensor* q, const bsa_tensor* k, 
  * Workspace bytes bsa_forward (and bsa_forward_causal) need: per launch chunk
  * of up to 8 requests, a work-tile counter and the order of the (request, KV
  * head) groups; with block_q of 64 or 128, also the merged key-block lists of
- * each 256-row super-block (int32 [B, Hq, ceil(Sq/256), nKb] plus counts):
- * those query blocks are attended 256 rows at a time over the union of their
- * lists, each row masking the blocks its own query block did not select. */
+ * each 256-row super-block (int32 [B, Hq, ceil(Sq/256), nKb + 3], their
+ * counts and two class sizes per row): those query blocks are attended 256
+ * rows at a time over the union of their lists, each row masking the blocks
+ * its own query block did not select, and each 128-row half of a super-block
+ * skipping the key tiles only the other half's query blocks selected. */
 BSA_API size_t bsa_forward_workspace_size(int B, int Hq, int Sq, int Skv, int block_q, int block_k);
 
 /* Selected-block attention forward (PR 8335, Purpose: the adapter executes
