@@ -172,11 +172,10 @@ BSA_API bsa_status bsa_select_rope(const bsa_tensor* q, const bsa_tensor* k,
  *    (see bsa_select_workspace_size) returns BSA_ERR_UNSUPPORTED naming the
  *    size and the limit.
  *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before capturing any stream on the device.  The address belongs to the
- *    context it was looked up in: after a cudaDeviceReset the next call sees
- *    a new context (by its unique ID) and looks the address up again, so
- *    make that call, too, before any capture.
+ *    (cudaGetSymbolAddress, with that device current).  The address belongs
+ *    to the context it was looked up in: after a cudaDeviceReset the next
+ *    call sees a new context (by its unique ID) and looks the address up
+ *    again.
  *  - Arguments are checked under this entry point's name before the scratch
  *    is touched: invalid arguments return the same codes as bsa_select.
  *  - All calls share the one array and it keeps the last call's contents
