@@ -34,6 +34,10 @@ CASES = {
     "batch_10_64x64": Config("batch_10_64x64", B=10, Hq=2, Hkv=1, d=128, prefix=100,
                              lens=(130, 64, 0, 1, 250, 65, 190, 7, 128, 99), block_q=64, block_k=64, keep=0.3,
                              recipe="iid", seed=3006),
+    # head dim 128 with 128-key blocks (the CTA-pair kernel) over two launches
+    "batch_9_pairs": Config("batch_9_pairs", B=9, Hq=4, Hkv=2, d=128, prefix=128,
+                            lens=(520, 0, 1, 257, 256, 33, 700, 128, 255), block_q=256, block_k=128, keep=0.4,
+                            recipe="iid", seed=3007),
 }
 
 
