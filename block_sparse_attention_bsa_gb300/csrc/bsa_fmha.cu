@@ -1091,8 +1091,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<NS>::kThread
             ls1 = __fadd2_rn(ls1, e1);
             pk[c / 2] = pack_bf16x2(e0.x, e0.y);
             pk[c / 2 + 1] = pack_bf16x2(e1.x, e1.y);
+            // each 32 keys of P go to TMEM as soon as they are packed
+            if (c == 28) tmem_st16(s_t + cc * 32, pk);
           }
-          tmem_st32(s_t + cc * 32, pk);
+          tmem_st16(s_t + cc * 32 + 16, pk + 16);
         }
         const float lsum = (ls0.x + ls0.y) + (ls1.x + ls1.y);
         l = l * alpha + lsum;
