@@ -77,8 +77,8 @@ def peaks():
 # `sha`.  When the sources change the figure no longer applies and traffic is
 # null.
 FMHA_TRAFFIC = {
-    "sha": "cce7a0c141738317",
-    "720p_75": 21628736512 + 1439542528,
+    "sha": "2fa5a295630cd3fb",
+    "720p_75": 21828103936 + 1439569152,
 }
 
 
