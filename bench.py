@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="bsa", choices=["bsa", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="replace the workload's generation length (every request) by this many tokens; "
+                         "the latent grid grows or shrinks by whole frames")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--backward", action="store_true",
@@ -107,6 +110,21 @@ def fmha_traffic(cfg, counts):
     if cfg.name in FMHA_TRAFFIC:
         return float(FMHA_TRAFFIC[cfg.name]), f"ncu capture of {cfg.name}"
     return None, f"no ncu capture of {cfg.name} for these forward sources"
+
+
+def workload_config(name: str, seq_len=None):
+    """The named workload, or the same workload with every request's
+    generation length set to seq_len (frames of the latent grid added or
+    removed to hold it; the name records the length)."""
+    import dataclasses
+    from bsa_inputs import CONFIGS
+    cfg = CONFIGS[name]
+    if not seq_len:
+        return cfg
+    grid = cfg.grid
+    if grid is not None:
+        grid = (-(-seq_len // (grid[1] * grid[2])), grid[1], grid[2])
+    return dataclasses.replace(cfg, name=f"{cfg.name}_L{seq_len}", lens=(seq_len,) * cfg.B, grid=grid)
 
 
 def dense_tiles(lens, prefix, Hq, bq, bk) -> int:
@@ -665,7 +683,7 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     bsa.build()
-    cfg = CONFIGS[args.config]
+    cfg = workload_config(args.config, args.seq_len)
     inp = make_inputs(cfg, "cuda", pad_fill=0.0)
     q, k, v = inp["q"], inp["k"], inp["v"]
     P, lens, bq, bk, keep = cfg.prefix, inp["seq_lens"], cfg.block_q, cfg.block_k, inp["keep_ratio"]
@@ -948,7 +966,7 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "strong" if split else "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": args.config, "B": B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "d": d, "prefix": P,
+            "config": {"workload": cfg.name, "B": B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "d": d, "prefix": P,
                        "seq_lens": lens, "block_q": bq, "block_k": bk, "keep_ratio": keep[:4],
                        "parallelism": (f"KV-head split x{world}" if split else f"replicas x{world}")
                        if world > 1 else "single GPU",
@@ -968,9 +986,9 @@ def main():
                          "algorithmic_bytes": algorithmic_bytes(cfg, cnt_np),
                          "algorithmic_flops": flops},
             "clocks": clocks,
-            **({"dense_fwd_ms": workloads[args.config]["dense_fwd_ms"],
-                "dense_over_sparse": workloads[args.config]["dense_over_sparse_fwd"],
-                "dense_over_sparse_ideal": workloads[args.config]["dense_over_sparse_ideal"],
+            **({"dense_fwd_ms": workloads[cfg.name]["dense_fwd_ms"],
+                "dense_over_sparse": workloads[cfg.name]["dense_over_sparse_fwd"],
+                "dense_over_sparse_ideal": workloads[cfg.name]["dense_over_sparse_ideal"],
                 "workloads": workloads, "schedules": schedules} if workloads else {}),
             "e2e": e2e,
             **({"backward": bwd} if bwd is not None else {}),

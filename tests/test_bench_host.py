@@ -135,3 +135,16 @@ def test_tiny_oracle_timing_runs_in_child_processes():
     t = bench.tiny_oracle_timing()
     assert t["one_core"]["threads"] == 1 and t["one_core"]["seconds"] > 0
     assert t["all_cores"]["threads"] == (os.cpu_count() or 1) and t["all_cores"]["tflops"] > 0
+
+
+def test_workload_config_replaces_the_generation_length():
+    assert bench.workload_config("720p_75") is CONFIGS["720p_75"]
+    c = bench.workload_config("720p_75", 75000)
+    assert c.name == "720p_75_L75000" and c.lens == (75000,)
+    assert (c.Hq, c.Hkv, c.d, c.prefix, c.block_q, c.block_k) == (32, 8, 128, 1024, 256, 128)
+    F, Y, X = c.grid
+    assert (Y, X) == (45, 80) and F * Y * X >= 75000 > (F - 1) * Y * X
+    inp = make_inputs(bench.workload_config("small_gqa", 500), "cpu")   # grid large enough for the recipe
+    assert inp["q"].shape[1] == 500 and list(inp["seq_lens"]) == [500, 500]
+    # a length that is not captured reports no traffic figure
+    assert bench.fmha_traffic(c, np.zeros(1))[0] is None
