@@ -838,7 +838,7 @@ def main():
                         "drain_ms": computed[n - 1].elapsed_time(end)}
             return start.elapsed_time(end) / n, compute, h2d_ms, d2h_ms, timeline
 
-        run_e2e(2)
+        run_e2e(NBUF + 1)                    # every device and host buffer used once before timing
         bsa.bsa_device_status(stream)
         e_ms, e_compute_ms, h2d_ms, d2h_ms, e_timeline = run_e2e(n_e2e)
         e_ms = max_over_ranks(e_ms, device="cuda")
