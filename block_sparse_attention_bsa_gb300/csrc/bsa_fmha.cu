@@ -14,17 +14,20 @@
 //    SMs of a TPC attends one 256-row query block, 128 rows per CTA, with
 //    M = 256 MMAs (cta_group::2) issued by two threads of the even CTA (one
 //    for S = Q K^T, one for O += P V).  See the comment above the kernel.
-//  * fmha_fwd_kernel (head dim 64): one persistent CTA per SM and 256-row
-//    query block, the two 128-row halves ping-ponged by one MMA thread.
+//  * fmha_fwd_kernel (head dim 64, and 64-key blocks at head dim 128): one
+//    persistent CTA per SM and 256-row query block, the two 128-row halves
+//    ping-ponged by one MMA thread; over merged lists (64/128-row query
+//    blocks) each half walks only the key tiles its own query blocks selected.
 //
 // Common to both:
 //  * Persistent CTAs walk work tiles (b, query block, head) in (request, KV
 //    head) groups, GQA siblings innermost, so the running CTAs share one KV
 //    head's K/V in L2.
 //  * Warp 0 is the TMA producer: Q once per work tile, then K and V tiles of
-//    the listed blocks, gathered by index (row = index * block_k), into a
-//    ring of shared-memory stages.  Per-request tensor maps bound the rows at
-//    prefix + L_b, so padded keys/values load as zeros.
+//    the listed blocks, gathered by index (row = index * block_k), into
+//    shared-memory rings (one of K/V stages in the pair kernel, a K ring and a
+//    V ring in the single-CTA kernel).  Per-request tensor maps bound the rows
+//    at prefix + L_b, so padded keys/values load as zeros.
 //  * Softmax warps: thread r owns query row r (TMEM lane r): tcgen05.ld of
 //    its S row, key mask, online softmax in the log2 domain with a lazy
 //    rescale (O is rescaled in TMEM only when the running max grows by more

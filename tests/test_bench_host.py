@@ -148,3 +148,11 @@ def test_workload_config_replaces_the_generation_length():
     assert inp["q"].shape[1] == 500 and list(inp["seq_lens"]) == [500, 500]
     # a length that is not captured reports no traffic figure
     assert bench.fmha_traffic(c, np.zeros(1))[0] is None
+
+
+def test_code_hash_ignores_comments_but_not_code():
+    src = 'int f(int x) { // note\n  return x + 1; /* more */ }\nconst char* s = "// kept";\n'
+    assert bench.strip_c_comments(src) == 'int f(int x) { \n  return x + 1;  }\nconst char* s = "// kept";\n'
+    n = lambda x: " ".join(bench.strip_c_comments(x).split())
+    assert n(src) == n(src.replace("// note", "// another note\n// and a line"))
+    assert n(src) != n(src.replace("x + 1", "x + 2"))
